@@ -1,0 +1,233 @@
+"""CPU oracle for the forward implicit-GEMM convolution and the fp8 pack.
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(the CUDA library and its Python binding) never imports it and shares no code
+with it.
+
+The arithmetic lives in ``conv_oracle.c`` (plain C, fp64, OpenMP), compiled
+with gcc into ``liboracle.so`` beside it.  This module only marshals numpy
+arrays into that library.
+
+Sources followed (each C function cites its passage):
+  * FlyDSL PR #860 "fp8 conv3d: 8-wave GEMM pipeline + BIG_IN fix" -- PR
+    summary (GEMM view M x K-filters x crs, KTRSC weight, E4M3FN inputs,
+    fp8-cast conv reference) and the commit verifying against
+    torch.nn.functional.conv3d (torch conv semantics).
+  * MIOpen PR #10912 "Use a single GEMM for point-output conv ..." --
+    description (point-output conv == one GEMM over channel-last rows).
+
+Pins: every function here is pinned by ``tests/test_oracle_*.py`` against
+torch CPU fp64 ``F.conv3d``, a scatter-form brute force, closed forms
+(1x1x1 == matmul, point-output == GEMM, delta filter == shifted copy,
+linearity) and the E4M3FN format definition.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ELEM_BF16 = 0
+ELEM_E4M3 = 1
+ELEM_F64 = 2
+
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_I32P = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile conv_oracle.c into liboracle.so with gcc (-O2 -fopenmp)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_amax_bf16.restype = ctypes.c_float
+        lib.oracle_amax_bf16.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+        lib.oracle_fp8_scale.restype = ctypes.c_float
+        lib.oracle_fp8_scale.argtypes = [ctypes.c_float]
+        lib.oracle_quantize_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_e4m3.argtypes = [ctypes.c_uint16, ctypes.c_float]
+        lib.oracle_pack_ncdhw_to_ndhwc_bf16.restype = None
+        lib.oracle_pack_ncdhw_to_ndhwc_bf16.argtypes = [ctypes.c_void_p, _I64P, ctypes.c_void_p]
+        lib.oracle_pack_ncdhw_to_ndhwc_fp8.restype = None
+        lib.oracle_pack_ncdhw_to_ndhwc_fp8.argtypes = [
+            ctypes.c_void_p, _I64P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
+        lib.oracle_out_extent.restype = ctypes.c_int64
+        lib.oracle_out_extent.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int]
+        conv_args = [ctypes.c_void_p, _I64P, ctypes.c_void_p, _I64P, _I32P, _I32P, _I32P,
+                     ctypes.c_int, ctypes.c_double, ctypes.c_double]
+        lib.oracle_conv3d_fwd.restype = ctypes.c_int
+        lib.oracle_conv3d_fwd.argtypes = conv_args + [ctypes.c_void_p]
+        lib.oracle_conv3d_fwd_points.restype = ctypes.c_int
+        lib.oracle_conv3d_fwd_points.argtypes = conv_args + [_I64P, ctypes.c_int64,
+                                                             ctypes.c_void_p]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _dims(v, n):
+    arr = (ctypes.c_int64 * n)(*[int(a) for a in v])
+    return arr
+
+
+def _ints3(v):
+    return (ctypes.c_int * 3)(*[int(a) for a in v])
+
+
+def _elem_of(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return ELEM_BF16
+    if a.dtype == np.uint8:
+        return ELEM_E4M3
+    if a.dtype == np.float64:
+        return ELEM_F64
+    raise TypeError(f"oracle takes bf16 bits (uint16), e4m3 bytes (uint8) or float64, got {a.dtype}")
+
+
+# ---------------------------------------------------------------- decoders
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().oracle_bf16_to_f64(int(bits))
+
+
+def e4m3_to_f64(code: int) -> float:
+    return _load().oracle_e4m3_to_f64(int(code))
+
+
+def f32_to_e4m3(v: float) -> int:
+    return int(_load().oracle_f32_to_e4m3(float(v)))
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """float64[256]: the value of every E4M3FN code (NaN for 0x7F/0xFF)."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+
+
+def quantize_e4m3(xbits: np.ndarray, scale: float) -> np.ndarray:
+    """Elementwise q = E4M3FN_satfinite_rne(f32(x)/scale) (small arrays only)."""
+    lib = _load()
+    flat = np.ascontiguousarray(xbits, dtype=np.uint16).ravel()
+    out = np.fromiter((lib.oracle_quantize_e4m3(int(b), float(scale)) for b in flat),
+                      dtype=np.uint8, count=flat.size)
+    return out.reshape(np.shape(xbits))
+
+
+def amax_bf16(xbits: np.ndarray) -> float:
+    a = np.ascontiguousarray(xbits, dtype=np.uint16)
+    return float(_load().oracle_amax_bf16(a.ctypes.data, a.size))
+
+
+def fp8_scale(amax: float) -> float:
+    return float(_load().oracle_fp8_scale(float(amax)))
+
+
+# ---------------------------------------------------------------- pack
+
+def pack_ncdhw_to_ndhwc_bf16(xbits: np.ndarray) -> np.ndarray:
+    """[N,C,D,H,W] bf16 bits -> [N,D,H,W,C] bf16 bits."""
+    a = np.ascontiguousarray(xbits, dtype=np.uint16)
+    N, C, D, H, W = a.shape
+    out = np.empty((N, D, H, W, C), dtype=np.uint16)
+    _load().oracle_pack_ncdhw_to_ndhwc_bf16(a.ctypes.data, _dims(a.shape, 5), out.ctypes.data)
+    return out
+
+
+def pack_ncdhw_to_ndhwc_fp8(xbits: np.ndarray):
+    """[N,C,D,H,W] bf16 bits -> ([N,D,H,W,C] e4m3 bytes, binary32 scale)."""
+    a = np.ascontiguousarray(xbits, dtype=np.uint16)
+    N, C, D, H, W = a.shape
+    out = np.empty((N, D, H, W, C), dtype=np.uint8)
+    scale = ctypes.c_float(0.0)
+    _load().oracle_pack_ncdhw_to_ndhwc_fp8(a.ctypes.data, _dims(a.shape, 5), out.ctypes.data,
+                                           ctypes.byref(scale))
+    return out, float(np.float32(scale.value))
+
+
+# ---------------------------------------------------------------- conv
+
+def out_extent(inp: int, filt: int, stride: int, pad: int, dil: int) -> int:
+    return int(_load().oracle_out_extent(inp, filt, stride, pad, dil))
+
+
+def out_dims(x_shape, w_shape, stride, pad, dil):
+    N, D, H, W, C = x_shape
+    K, T, R, S, _ = w_shape
+    return (N, out_extent(D, T, stride[0], pad[0], dil[0]),
+            out_extent(H, R, stride[1], pad[1], dil[1]),
+            out_extent(W, S, stride[2], pad[2], dil[2]), K)
+
+
+def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1, 1, 1),
+           scale_x: float = 1.0, scale_w: float = 1.0) -> np.ndarray:
+    """Full fp64 forward conv.  x [N,D,H,W,C], w [K,T,R,S,C]; both bf16 bits
+    (uint16), e4m3 bytes (uint8) or float64.  Returns fp64 [N,Do,Ho,Wo,K]."""
+    x = np.ascontiguousarray(x)
+    w = np.ascontiguousarray(w)
+    elem = _elem_of(x)
+    if _elem_of(w) != elem:
+        raise TypeError("x and w must have the same element type")
+    od = out_dims(x.shape, w.shape, stride, pad, dil)
+    out = np.zeros(od, dtype=np.float64)
+    rc = _load().oracle_conv3d_fwd(x.ctypes.data, _dims(x.shape, 5), w.ctypes.data,
+                                   _dims(w.shape, 5), _ints3(stride), _ints3(pad), _ints3(dil),
+                                   elem, float(scale_x), float(scale_w), out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_conv3d_fwd: bad shapes")
+    return out
+
+
+def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1),
+                  pad=(0, 0, 0), dil=(1, 1, 1), scale_x: float = 1.0,
+                  scale_w: float = 1.0) -> np.ndarray:
+    """fp64 conv evaluated at flat NDHWC output indices ``idx`` (int64)."""
+    x = np.ascontiguousarray(x)
+    w = np.ascontiguousarray(w)
+    elem = _elem_of(x)
+    if _elem_of(w) != elem:
+        raise TypeError("x and w must have the same element type")
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    vals = np.empty(idx.shape, dtype=np.float64)
+    rc = _load().oracle_conv3d_fwd_points(
+        x.ctypes.data, _dims(x.shape, 5), w.ctypes.data, _dims(w.shape, 5), _ints3(stride),
+        _ints3(pad), _ints3(dil), elem, float(scale_x), float(scale_w),
+        idx.ctypes.data_as(_I64P), idx.size, vals.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_conv3d_fwd_points: bad shapes or index out of range")
+    return vals
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
