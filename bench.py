@@ -1,0 +1,457 @@
+"""Benchmark: forward implicit-GEMM convolution throughput on GB300.
+
+One step = one conv_fwd call (the whole hot path: dispatch, TMA operand
+loads, tcgen05 MMA, epilogue, and split-K reduce when planned) over the
+headline workload, the 2048-channel 3x3x3 video convolution (M = 216000
+output positions, K = 2048 filters, R = 55296), with inputs resident in HBM.
+Throughput is 2*M*K*R / step time.  The same JSON line carries the
+end-to-end number (host -> device inputs from pinned memory, conv, output
+back to the host, all timed), the roofline fraction of the conv kernel, the
+fp64 CPU oracle's rate on a bounded sample (the reference arm), sampled
+clocks, and secondary workloads (fp8 with and without its pack, the
+>2^31-element temporal conv, the patch embedding).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch under torch.distributed.run; each rank runs an independent
+replica (the problem has no exchange step) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import conv_workloads as cw  # noqa: E402
+
+HEADLINE = "video_conv3d_bf16"
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "conv fwd TFLOPS (2*M*N*R/time) bf16 & fp8 on 1 GB300; % of dense tensor peak"
+# MI355X figure for the same shape (C=K=2048, 3x3x3, M~216k): FlyDSL PR #860, async-DMA commit
+PAGE_BASELINE_TFLOPS = {"video_conv3d_bf16": 967.0}
+
+
+def gemm_dims(wl: cw.Workload):
+    """(M, N, R) of the GEMM view of workload wl."""
+    if wl.x_layout == "ncdhw":
+        N, C, D, H, W = wl.x_shape
+    else:
+        N, D, H, W, C = wl.x_shape
+    if wl.w_layout == "kctrs":
+        K, _, T, R, S = wl.w_shape
+    else:
+        K, T, R, S, _ = wl.w_shape
+    ext = []
+    for i, (n, f) in enumerate(((D, T), (H, R), (W, S))):
+        ext.append((n + 2 * wl.pad[i] - wl.dil[i] * (f - 1) - 1) // wl.stride[i] + 1)
+    return N * ext[0] * ext[1] * ext[2], K, C * T * R * S
+
+
+def flops(wl: cw.Workload) -> float:
+    M, N, R = gemm_dims(wl)
+    return 2.0 * M * N * R
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "implicit_gemm_convolution_conv3d_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the conv kernel from the committed ncu summary,
+    or None when the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("kernel_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, pw, reasons = [], 0.0, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+                pw.append(float(f[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        hi = max(pw) if pw else 0.0
+        loaded = [s for s, p in zip(sm, pw) if p >= 0.5 * hi] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": hi}
+
+
+class Timer:
+    """Per-step CUDA-event timing on the launching stream, L2 flushed between steps."""
+
+    def __init__(self, steps: int, flush: torch.Tensor):
+        self.steps = steps
+        self.flush = flush
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+
+    def run(self, fn):
+        stream = torch.cuda.current_stream()
+        for i in range(self.steps):
+            self.flush.zero_()
+            self.ev[i][0].record(stream)
+            fn()
+            self.ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in self.ev]
+
+
+def physical_gpu_index(local: int) -> int:
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if local < len(vis) and vis[local].isdigit():
+        return int(vis[local])
+    return local
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- workloads
+
+def prepare(pkg, wl: cw.Workload, device):
+    """Device-resident operands of workload wl in the layout conv_fwd takes."""
+    x, w = cw.make_inputs(wl, device)
+    if wl.dtype == "fp8":
+        qx, sx = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)
+        qw, sw = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(w)
+        return {"x": qx, "w": qw, "sx": sx, "sw": sw, "x_bf16_ncdhw": x, "w_ncdhw": w}
+    return {"x": x, "w": w, "sx": None, "sw": None}
+
+
+def conv_step(pkg, wl, ops, out, ws):
+    return lambda: pkg.conv_fwd(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil, scale_x=ops["sx"],
+                                scale_w=ops["sw"], out=out, workspace=ws)
+
+
+def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True):
+    ops = prepare(pkg, wl, device)
+    x, w = ops["x"], ops["w"]
+    plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
+                             1 if wl.dtype == "fp8" else 0)
+    od = pkg.conv_out_dims(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil)
+    out = torch.empty(od, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=device)
+    step = conv_step(pkg, wl, ops, out, ws)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if pkg.conv_get_device_status() != 0:
+        raise RuntimeError("device status reports a timeout")
+    times = Timer(steps, flush).run(step)
+    res = {"plan": plan, "ms": times, "flop": flops(wl),
+           "launches_per_step": 1 + (1 if plan["splits"] > 1 else 0)}
+    if wl.dtype == "fp8":
+        # with the pack of the activation (the weight pack is a one-off prep)
+        xb = ops["x_bf16_ncdhw"]
+        pk_ws = torch.empty(16, dtype=torch.uint8, device=device)
+
+        def full():
+            pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb, out=ops["x"], scale=ops["sx"], workspace=pk_ws)
+            step()
+        for _ in range(warmup):
+            full()
+        res["ms_with_pack"] = Timer(steps, flush).run(full)
+
+        def pack_only():
+            pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb, out=ops["x"], scale=ops["sx"], workspace=pk_ws)
+        res["ms_pack"] = Timer(steps, flush).run(pack_only)
+        res["pack_bytes"] = xb.numel() * 2 * 2 + xb.numel()   # amax read, pack read, fp8 write
+    if with_e2e:
+        res["e2e"] = run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush)
+    del ops
+    return res
+
+
+def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
+    """Same conv through the public API with inputs coming from pinned host
+    memory and the output going back to pinned host memory, all timed."""
+    # the host holds the activation as the user has it (bf16 NCDHW for the fp8
+    # workload, which is packed on the device every step) and the prepared weight
+    dx = ops["x_bf16_ncdhw"] if wl.dtype == "fp8" else ops["x"]
+    hx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+    hx.copy_(dx)
+    hw = torch.empty(ops["w"].shape, dtype=ops["w"].dtype, pin_memory=True)
+    hw.copy_(ops["w"])
+    pk_ws = torch.empty(16, dtype=torch.uint8, device=out.device)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        ops["w"].copy_(hw, non_blocking=True)
+        if wl.dtype == "fp8":
+            pkg.pack_ncdhw_bf16_to_ndhwc_fp8(dx, out=ops["x"], scale=ops["sx"], workspace=pk_ws)
+        pkg.conv_fwd(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil, scale_x=ops["sx"],
+                     scale_w=ops["sw"], out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    times = Timer(steps, flush).run(step)
+    h2d = hx.numel() * hx.element_size() + hw.numel() * hw.element_size()
+    d2h = hout.numel() * hout.element_size()
+    return {"ms": times, "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+def cpu_oracle_rate(wl: cw.Workload, x_host, w_host, target_s: float = 10.0):
+    """fp64 oracle TFLOPS on a bounded sample of output elements, sized for
+    about target_s seconds of work on all host cores."""
+    import oracle
+    M, N, R = gemm_dims(wl)
+    total = M * N
+    rng = np.random.default_rng(wl.sample_seed)
+    probe = rng.integers(0, total, size=256)
+    t0 = time.perf_counter()
+    oracle.conv3d_points(x_host, w_host, probe, wl.stride, wl.pad, wl.dil)
+    per = (time.perf_counter() - t0) / probe.size
+    n = int(min(max(256, target_s / max(per, 1e-9)), 5_000_000))
+    idx = rng.integers(0, total, size=n)
+    t0 = time.perf_counter()
+    oracle.conv3d_points(x_host, w_host, idx, wl.stride, wl.pad, wl.dil)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * n * R / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} output elements of {wl.name} (each a {R}-term fp64 dot product), "
+                      f"{dt:.1f} s"}
+
+
+def host_inputs(wl: cw.Workload):
+    """The workload's operands as the host bytes the oracle reads (generated
+    on the CPU with the same seeds and recipe)."""
+    x, w = cw.make_inputs(wl, "cpu")
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    wb = w.view(torch.int16).numpy().view(np.uint16)
+    return xb, wb
+
+
+def reference_arm(args):
+    dist, rank, world, _ = dist_setup(args)
+    if rank != 0:
+        return
+    wl = cw.BY_NAME[args.workload]
+    if wl.dtype == "fp8":
+        raise SystemExit("the reference arm times bf16 workloads")
+    xb, wb = host_inputs(wl)
+    per_step_s = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(wl, xb, wb, target_s=min(per_step_s, 5.0))
+    vals = []
+    last = None
+    for _ in range(args.steps):
+        last = cpu_oracle_rate(wl, xb, wb, target_s=per_step_s)
+        vals.append(last["value"])
+    value = statistics.median(vals)
+    flop = flops(wl)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": flop / (value * 1e12) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": dict(last, value=value),
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(wl):
+    M, N, R = gemm_dims(wl)
+    return {"workload": wl.name, "x_shape": list(wl.x_shape), "x_layout": wl.x_layout,
+            "w_shape": list(wl.w_shape), "w_layout": wl.w_layout, "stride": list(wl.stride),
+            "pad": list(wl.pad), "dil": list(wl.dil), "M": M, "N": N, "R": R,
+            "flop_per_step": flops(wl),
+            "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"}
+
+
+# ---------------------------------------------------------------- main arm
+
+def main_arm(args):
+    dist, rank, world, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import implicit_gemm_convolution_conv3d_gb300 as pkg
+    pkg.load_library()
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    wl = cw.BY_NAME[args.workload]
+
+    barrier(dist)
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        res = run_workload(pkg, wl, device, args.steps, args.warmup, flush)
+    barrier(dist)
+    ms = statistics.mean(res["ms"])
+    ms_max = max_over_ranks(dist, ms, device)
+    e2e_ms = max_over_ranks(dist, statistics.mean(res["e2e"]["ms"]), device)
+    value = world * res["flop"] / (ms_max * 1e-3) / 1e12
+    e2e_value = world * res["flop"] / (e2e_ms * 1e-3) / 1e12
+
+    secondary = {}
+    if not args.no_secondary:
+        for name in [n for n in ("fp8_conv3d_1x3x3", "temporal_3x1x1_bf16_big", "patch_embed_bf16",
+                                 "tiny_conv3d_bf16") if n != wl.name]:
+            try:
+                r = run_workload(pkg, cw.BY_NAME[name], device, args.steps, args.warmup, flush,
+                                 with_e2e=False)
+                m = statistics.mean(r["ms"])
+                ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m, "plan": r["plan"]}
+                if "ms_with_pack" in r:
+                    mp = statistics.mean(r["ms_with_pack"])
+                    ent["tflops_with_pack"] = r["flop"] / (mp * 1e-3) / 1e12
+                    ent["ms_with_pack"] = mp
+                    pk = statistics.mean(r["ms_pack"])
+                    ent["pack_ms"] = pk
+                    ent["pack_gbs"] = r["pack_bytes"] / (pk * 1e-3) / 1e9
+                secondary[name] = ent
+            except Exception as e:  # a secondary workload never hides the headline line
+                secondary[name] = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+    peak = peaks["bf16_tflops"] if wl.dtype == "bf16" else 2.0 * peaks["bf16_tflops"]
+    achieved = res["flop"] / (ms * 1e-3) / 1e12
+    traffic = measured_traffic(wl.name)
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+            "kernel": "conv_igemm_kernel (tcgen05, TMA im2col)"}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        xb, wb = host_inputs(wl)
+        cpu = cpu_oracle_rate(wl, xb, wb)
+    base = PAGE_BASELINE_TFLOPS.get(wl.name)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": (value / base) if base else None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": dict(workload_config(wl), parallelism=f"replicas{world}",
+                           plan=res["plan"],
+                           baseline_note="vs_baseline divides by the MI355X figure for this shape "
+                                         "(967 TFLOPS, FlyDSL PR #860): context only"),
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": res["e2e"]["h2d"],
+                    "d2h_bytes_per_step": res["e2e"]["d2h"], "ms_per_step": e2e_ms},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(),
+            "workloads": secondary}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(cw.BY_NAME))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        main_arm(args)
+
+
+if __name__ == "__main__":
+    main()

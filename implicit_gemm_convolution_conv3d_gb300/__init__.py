@@ -1,0 +1,288 @@
+"""Forward implicit-GEMM convolution for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libconv3d.so`` (C ABI in ``include/conv3d.h``).
+It only marshals arguments: shapes, device pointers and the current CUDA
+stream of torch tensors.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and every call
+raises if the library is missing or returns an error.
+
+Names follow the C ABI (``conv_fwd``, ``pack_ncdhw_bf16_to_ndhwc``,
+``pack_ncdhw_bf16_to_ndhwc_fp8``, ...).  ``conv3d``, ``conv2d`` and
+``conv1d`` are the convenience wrappers: 2-D and 1-D convolutions run as the
+degenerate 3-D forms D=T=1 (and H=R=1 for 1-D), as the FlyDSL PR #860
+conv2d/conv1d wrapper commit does.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libconv3d.so")
+
+CONV_OK = 0
+CONV_ERR_INVALID = 1
+CONV_ERR_UNSUPPORTED = 2
+CONV_ERR_CUDA = 3
+CONV_ERR_TIMEOUT = 4
+
+CONV_DTYPE_BF16 = 0
+CONV_DTYPE_FP8_E4M3 = 1
+
+CLASS_NAMES = {0: "generic", 1: "temporal", 2: "point_gemm"}
+
+_I64_5 = ctypes.c_int64 * 5
+_I32_3 = ctypes.c_int * 3
+_lock = threading.Lock()
+_lib = None
+
+
+class ConvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {_status_string(status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def _status_string(s: int) -> str:
+    lib = _lib
+    if lib is None:
+        return f"status {s}"
+    return lib.conv_status_string(int(s)).decode()
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libconv3d.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -m implicit_gemm_convolution_conv3d_gb300.build`")
+        lib = ctypes.CDLL(path)
+        vp, i64p, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int)
+        lib.conv_out_dims.argtypes = [i64p, i64p, i32p, i32p, i32p, i64p]
+        lib.conv_out_dims.restype = ctypes.c_int
+        lib.conv_fwd_plan.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                      i32p, i32p, i32p, i32p, i32p, i32p,
+                                      ctypes.POINTER(ctypes.c_size_t)]
+        lib.conv_fwd_plan.restype = ctypes.c_int
+        lib.conv_fwd.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp, vp,
+                                 vp, ctypes.c_size_t, vp]
+        lib.conv_fwd.restype = ctypes.c_int
+        lib.pack_ncdhw_bf16_to_ndhwc.argtypes = [vp, i64p, vp, vp]
+        lib.pack_ncdhw_bf16_to_ndhwc.restype = ctypes.c_int
+        lib.pack_fp8_workspace_size.argtypes = []
+        lib.pack_fp8_workspace_size.restype = ctypes.c_size_t
+        lib.pack_ncdhw_bf16_to_ndhwc_fp8.argtypes = [vp, i64p, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.pack_ncdhw_bf16_to_ndhwc_fp8.restype = ctypes.c_int
+        lib.conv_get_device_status.argtypes = [i32p]
+        lib.conv_get_device_status.restype = ctypes.c_int
+        lib.conv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.conv_set_wait_limit_ns.restype = None
+        lib.conv_status_string.argtypes = [ctypes.c_int]
+        lib.conv_status_string.restype = ctypes.c_char_p
+        lib.conv_last_error.argtypes = []
+        lib.conv_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, where: str):
+    if rc != CONV_OK:
+        detail = _lib.conv_last_error().decode() if _lib is not None else ""
+        raise ConvError(rc, where, detail)
+
+
+def _triple(v: Union[int, Sequence[int]]) -> Tuple[int, int, int]:
+    if isinstance(v, int):
+        return (v, v, v)
+    t = tuple(int(a) for a in v)
+    if len(t) != 3:
+        raise ValueError("expected an int or a 3-sequence")
+    return t
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CONV_DTYPE_BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return CONV_DTYPE_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or float8_e4m3fn")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------------ host-only
+
+def conv_out_dims(x_shape, w_shape, stride=1, pad=0, dil=1) -> Tuple[int, ...]:
+    """(N, Do, Ho, Wo, K) of the forward conv of x [N,D,H,W,C] by w [K,T,R,S,C]."""
+    lib = load_library()
+    out = _I64_5()
+    _check(lib.conv_out_dims(_I64_5(*x_shape), _I64_5(*w_shape), _I32_3(*_triple(stride)),
+                             _I32_3(*_triple(pad)), _I32_3(*_triple(dil)), out), "conv_out_dims")
+    return tuple(int(v) for v in out)
+
+
+def conv_fwd_plan(x_shape, w_shape, stride=1, pad=0, dil=1, dtype: int = CONV_DTYPE_BF16,
+                  num_sms: int = 0) -> dict:
+    """The plan conv_fwd runs: class, tile N, k-step bytes, stages, split-K, CTAs,
+    workspace bytes.  ``num_sms > 0`` plans host-only for that SM count."""
+    lib = load_library()
+    v = [ctypes.c_int(0) for _ in range(6)]
+    ws = ctypes.c_size_t(0)
+    _check(lib.conv_fwd_plan(_I64_5(*x_shape), _I64_5(*w_shape), _I32_3(*_triple(stride)),
+                             _I32_3(*_triple(pad)), _I32_3(*_triple(dil)), int(dtype),
+                             int(num_sms), *[ctypes.byref(a) for a in v], ctypes.byref(ws)),
+           "conv_fwd_plan")
+    cls, bn, bk, st, sp, ctas = (a.value for a in v)
+    return {"class": CLASS_NAMES.get(cls, str(cls)), "tile_n": bn, "k_bytes": bk, "stages": st,
+            "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
+
+
+def conv_set_wait_limit_ns(ns: int) -> None:
+    load_library().conv_set_wait_limit_ns(int(ns))
+
+
+def conv_get_device_status() -> int:
+    """Synchronise the device, then read and clear its status word."""
+    lib = load_library()
+    v = ctypes.c_int(0)
+    _check(lib.conv_get_device_status(ctypes.byref(v)), "conv_get_device_status")
+    return int(v.value)
+
+
+# ------------------------------------------------------------------ device calls
+
+def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
+             scale_x: Optional[torch.Tensor] = None, scale_w: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None, split_k: bool = True) -> torch.Tensor:
+    """Forward conv: x NDHWC [N,D,H,W,C], w KTRSC [K,T,R,S,C] (both bf16, or
+    both float8_e4m3fn with fp32 device scales) -> out NDHWC [N,Do,Ho,Wo,K]
+    bf16.  A split-K workspace is taken from torch's allocator when the plan
+    wants one and none is given (``split_k=False`` runs without)."""
+    lib = load_library()
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError("x must be [N,D,H,W,C] and w [K,T,R,S,C]")
+    dtype = _dtype_code(x)
+    if _dtype_code(w) != dtype:
+        raise TypeError("x and w must have the same dtype")
+    for s in (scale_x, scale_w):
+        if s is not None and (s.dtype != torch.float32 or s.numel() < 1):
+            raise TypeError("scales must be float32 device tensors")
+    _require_cuda(x, w, scale_x, scale_w, out, workspace)
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    od = conv_out_dims(tuple(x.shape), tuple(w.shape), st, pa, di)
+    if out is None:
+        out = torch.empty(od, dtype=torch.bfloat16, device=x.device)
+    elif tuple(out.shape) != od or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 {od}")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    elif split_k:
+        need = conv_fwd_plan(tuple(x.shape), tuple(w.shape), st, pa, di, dtype)["workspace_bytes"]
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+            ws_ptr, ws_bytes = workspace.data_ptr(), need
+    rc = lib.conv_fwd(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                      _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x), _ptr(scale_w),
+                      out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(rc, "conv_fwd")
+    return out
+
+
+def pack_ncdhw_bf16_to_ndhwc(x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """bf16 NCDHW [N,C,D,H,W] -> bf16 NDHWC [N,D,H,W,C] (a torch weight
+    [K,C,T,R,S] gives the KTRSC weight)."""
+    lib = load_library()
+    if x.dim() != 5 or x.dtype != torch.bfloat16:
+        raise ValueError("x must be a bf16 [N,C,D,H,W] tensor")
+    N, C, D, H, W = x.shape
+    if out is None:
+        out = torch.empty((N, D, H, W, C), dtype=torch.bfloat16, device=x.device)
+    _require_cuda(x, out)
+    _check(lib.pack_ncdhw_bf16_to_ndhwc(x.data_ptr(), _I64_5(*x.shape), out.data_ptr(),
+                                        _stream_handle(stream)), "pack_ncdhw_bf16_to_ndhwc")
+    return out
+
+
+def pack_ncdhw_bf16_to_ndhwc_fp8(x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                                 scale: Optional[torch.Tensor] = None,
+                                 workspace: Optional[torch.Tensor] = None,
+                                 stream: Optional[torch.cuda.Stream] = None):
+    """bf16 NCDHW -> (e4m3 NDHWC, fp32 scale[1]) with scale = amax/448."""
+    lib = load_library()
+    if x.dim() != 5 or x.dtype != torch.bfloat16:
+        raise ValueError("x must be a bf16 [N,C,D,H,W] tensor")
+    N, C, D, H, W = x.shape
+    if out is None:
+        out = torch.empty((N, D, H, W, C), dtype=torch.float8_e4m3fn, device=x.device)
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    wsb = int(lib.pack_fp8_workspace_size())
+    if workspace is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=x.device)
+    _require_cuda(x, out, scale, workspace)
+    _check(lib.pack_ncdhw_bf16_to_ndhwc_fp8(
+        x.data_ptr(), _I64_5(*x.shape), out.data_ptr(), scale.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream)),
+        "pack_ncdhw_bf16_to_ndhwc_fp8")
+    return out, scale
+
+
+# ------------------------------------------------------------------ wrappers
+
+def conv3d(x, w, stride=1, padding=0, dilation=1, scale_x=None, scale_w=None, **kw):
+    """conv_fwd under its usual name (NDHWC x, KTRSC w)."""
+    return conv_fwd(x, w, stride, padding, dilation, scale_x, scale_w, **kw)
+
+
+def conv2d(x, w, stride=1, padding=0, dilation=1, scale_x=None, scale_w=None, **kw):
+    """NHWC x [N,H,W,C], KRSC w [K,R,S,C] -> NHWC [N,Ho,Wo,K], as the D=T=1 conv3d."""
+    s = (stride, stride) if isinstance(stride, int) else tuple(stride)
+    p = (padding, padding) if isinstance(padding, int) else tuple(padding)
+    d = (dilation, dilation) if isinstance(dilation, int) else tuple(dilation)
+    y = conv_fwd(x.unsqueeze(1), w.unsqueeze(1), (1,) + s, (0,) + p, (1,) + d, scale_x, scale_w,
+                 **kw)
+    return y.squeeze(1)
+
+
+def conv1d(x, w, stride=1, padding=0, dilation=1, scale_x=None, scale_w=None, **kw):
+    """NWC x [N,W,C], KSC w [K,S,C] -> NWC [N,Wo,K], as the D=T=H=R=1 conv3d."""
+    s = stride if isinstance(stride, int) else int(stride[0])
+    p = padding if isinstance(padding, int) else int(padding[0])
+    d = dilation if isinstance(dilation, int) else int(dilation[0])
+    y = conv_fwd(x[:, None, None], w[:, None, None], (1, 1, s), (0, 0, p), (1, 1, d), scale_x,
+                 scale_w, **kw)
+    return y[:, 0, 0]
+
+
+__all__ = [
+    "conv_fwd", "conv_fwd_plan", "conv_out_dims", "conv_get_device_status",
+    "conv_set_wait_limit_ns", "pack_ncdhw_bf16_to_ndhwc", "pack_ncdhw_bf16_to_ndhwc_fp8",
+    "conv3d", "conv2d", "conv1d", "load_library", "ConvError", "LIB_PATH",
+]

@@ -1,0 +1,248 @@
+// aux_kernels.cu -- HBM-bound kernels around the convolution:
+//   * split-K reduction (FlyDSL PR #860, split-K commits): fp32 partials
+//     summed in fixed split order, scaled, rounded to bf16;
+//   * amax of a bf16 tensor, and the tiled NCDHW -> NDHWC pack with optional
+//     per-tensor fp8-e4m3 quantisation (FlyDSL PR #860, commit adding the
+//     tiled bf16 -> fp8 transpose that replaces torch.permute, and the commit
+//     fixing its >2 GB addressing with 64-bit offsets).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+
+namespace c3d {
+
+namespace {
+
+// ----------------------------------------------------------------- split-K
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws,
+                                                            __nv_bfloat16* __restrict__ out,
+                                                            long long MK, int splits,
+                                                            const float* scale_x,
+                                                            const float* scale_w) {
+    float scale = 1.0f;
+    if (scale_x) scale *= *scale_x;
+    if (scale_w) scale *= *scale_w;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if ((MK & 3) == 0) {
+        const long long n4 = MK >> 2;
+        for (long long i = tid; i < n4; i += stride) {
+            float4 acc = reinterpret_cast<const float4*>(ws)[i];
+            for (int s = 1; s < splits; ++s) {
+                const float4 v = reinterpret_cast<const float4*>(ws + s * MK)[i];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * scale, acc.y * scale);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * scale, acc.w * scale);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&lo);
+            o.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(out)[i] = o;
+        }
+    } else {
+        for (long long i = tid; i < MK; i += stride) {
+            float acc = ws[i];
+            for (int s = 1; s < splits; ++s) acc += ws[s * MK + i];
+            out[i] = __float2bfloat16_rn(acc * scale);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- amax
+// max |x| of a bf16 tensor into *amax_bits (the bit pattern of a non-negative
+// binary32 orders like an unsigned integer, so atomicMax on the bits is the
+// float max).  *amax_bits must be zero before the launch.
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                        long long n, unsigned int* amax_bits) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    unsigned int m = 0;   // max over |x| as bf16 magnitude bits
+    const long long n8 = n >> 3;
+    const uint4* in8 = reinterpret_cast<const uint4*>(in);
+    for (long long i = tid; i < n8; i += stride) {
+        const uint4 v = __ldcs(in8 + i);
+        const unsigned int w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = max(m, w[j] & 0x7FFFu);
+            m = max(m, (w[j] >> 16) & 0x7FFFu);
+        }
+    }
+    const unsigned short* in16 = reinterpret_cast<const unsigned short*>(in);
+    for (long long i = (n8 << 3) + tid; i < n; i += stride) m = max(m, in16[i] & 0x7FFFu);
+    // bf16 magnitude bits << 16 are the binary32 bits of the same value
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __shared__ unsigned int red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned int b = 0;
+        for (int i = 0; i < (blockDim.x >> 5); ++i) b = max(b, red[i]);
+        atomicMax(amax_bits, b << 16);
+    }
+}
+
+// ----------------------------------------------------------------- pack
+// One CTA moves a tile of 64 channels x 64 spatial positions of one image:
+// coalesced reads of 64 rows of 64 spatial values (128 B each) into shared
+// memory, then each thread emits 16 consecutive channels of one spatial
+// position (16 B of fp8 or 32 B of bf16), four threads covering a 64-channel
+// run.  All offsets are 64-bit.
+constexpr int kPackC = 64;
+constexpr int kPackS = 64;
+constexpr int kPitch = kPackS + 2;   // bf16 elements per smem row (33 words: no bank conflicts)
+
+__device__ __forceinline__ float fp8_scale_of(const unsigned int* amax_bits) {
+    const float amax = __uint_as_float(*amax_bits);
+    return amax == 0.0f ? 1.0f : amax / 448.0f;   // IEEE division (no fast-math)
+}
+
+template <int FP8>
+__global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restrict__ in,
+                                                   long long N, long long C, long long S,
+                                                   void* __restrict__ out,
+                                                   const unsigned int* amax_bits,
+                                                   float* scale_out, long long c_tiles,
+                                                   long long s_tiles) {
+    __shared__ __align__(16) unsigned short tile[kPackC * kPitch];
+    const long long b = blockIdx.x;
+    const long long st = b % s_tiles;
+    const long long rest = b / s_tiles;
+    const long long ct = rest % c_tiles;
+    const long long n = rest / c_tiles;
+    const long long s0 = st * kPackS, c0 = ct * kPackC;
+    const unsigned short* src = reinterpret_cast<const unsigned short*>(in);
+
+    // load: 64 channel rows x 64 positions; thread -> (row, 8-position piece)
+    const bool vec_in = (S % 8) == 0;
+    for (int i = threadIdx.x; i < kPackC * (kPackS / 8); i += blockDim.x) {
+        const int r = i >> 3, piece = i & 7;
+        const long long c = c0 + r, s = s0 + piece * 8;
+        unsigned short v[8];
+        if (c < C && vec_in && s + 8 <= S) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(src + (n * C + c) * S + s));
+            const unsigned int w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = static_cast<unsigned short>(w[j] & 0xFFFFu);
+                v[2 * j + 1] = static_cast<unsigned short>(w[j] >> 16);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = (c < C && s + j < S) ? src[(n * C + c) * S + s + j] : 0;
+        }
+        unsigned int* trow = reinterpret_cast<unsigned int*>(tile + r * kPitch + piece * 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) trow[j] = static_cast<unsigned int>(v[2 * j]) |
+                                              (static_cast<unsigned int>(v[2 * j + 1]) << 16);
+    }
+    __syncthreads();
+
+    float scale = 1.0f;
+    if (FP8) {
+        scale = fp8_scale_of(amax_bits);
+        if (b == 0 && threadIdx.x == 0) *scale_out = scale;
+    }
+    // store: thread -> (position, 16-channel group)
+    const int g = threadIdx.x & 3;
+    for (int sp = threadIdx.x >> 2; sp < kPackS; sp += blockDim.x >> 2) {
+        const long long s = s0 + sp;
+        const long long cb = c0 + g * 16;
+        if (s >= S || cb >= C) continue;
+        unsigned short v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = tile[(g * 16 + j) * kPitch + sp];
+        const long long obase = (n * S + s) * C + cb;
+        const bool full = (cb + 16 <= C);
+        if (FP8) {
+            unsigned char* o = reinterpret_cast<unsigned char*>(out);
+            unsigned char q[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float a = __uint_as_float(static_cast<unsigned int>(v[j]) << 16) / scale;
+                const float c2 = __uint_as_float(static_cast<unsigned int>(v[j + 1]) << 16) / scale;
+                const __nv_fp8x2_storage_t p2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(a, c2), __NV_SATFINITE, __NV_E4M3);
+                q[j] = static_cast<unsigned char>(p2 & 0xFFu);
+                q[j + 1] = static_cast<unsigned char>(p2 >> 8);
+            }
+            if (full && (C % 16) == 0) {
+                uint4 w;
+                w.x = q[0] | (q[1] << 8) | (q[2] << 16) | (static_cast<unsigned int>(q[3]) << 24);
+                w.y = q[4] | (q[5] << 8) | (q[6] << 16) | (static_cast<unsigned int>(q[7]) << 24);
+                w.z = q[8] | (q[9] << 8) | (q[10] << 16) | (static_cast<unsigned int>(q[11]) << 24);
+                w.w = q[12] | (q[13] << 8) | (q[14] << 16) | (static_cast<unsigned int>(q[15]) << 24);
+                *reinterpret_cast<uint4*>(o + obase) = w;
+            } else {
+                for (int j = 0; j < 16 && cb + j < C; ++j) o[obase + j] = q[j];
+            }
+        } else {
+            unsigned short* o = reinterpret_cast<unsigned short*>(out);
+            if (full && (C % 8) == 0) {
+                uint4 w0, w1;
+                w0.x = v[0] | (v[1] << 16);
+                w0.y = v[2] | (v[3] << 16);
+                w0.z = v[4] | (v[5] << 16);
+                w0.w = v[6] | (v[7] << 16);
+                w1.x = v[8] | (v[9] << 16);
+                w1.y = v[10] | (v[11] << 16);
+                w1.z = v[12] | (v[13] << 16);
+                w1.w = v[14] | (v[15] << 16);
+                reinterpret_cast<uint4*>(o + obase)[0] = w0;
+                reinterpret_cast<uint4*>(o + obase)[1] = w1;
+            } else {
+                for (int j = 0; j < 16 && cb + j < C; ++j) o[obase + j] = v[j];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
+                                 const float* scale_x, const float* scale_w, int num_sms,
+                                 cudaStream_t stream) {
+    const long long units = (MK & 3) == 0 ? (MK >> 2) : MK;
+    long long blocks = (units + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        ws, reinterpret_cast<__nv_bfloat16*>(out), MK, splits, scale_x, scale_w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax_bf16(const void* in, long long n, unsigned int* amax_bits, int num_sms,
+                             cudaStream_t stream) {
+    long long blocks = (n / 8 + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    amax_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(in), n, amax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const void* in, long long N, long long C, long long S, void* out, int fp8,
+                        const unsigned int* amax_bits, float* scale_out, cudaStream_t stream) {
+    const long long c_tiles = (C + kPackC - 1) / kPackC;
+    const long long s_tiles = (S + kPackS - 1) / kPackS;
+    const long long blocks = N * c_tiles * s_tiles;
+    if (blocks <= 0 || blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+    const auto* x = reinterpret_cast<const __nv_bfloat16*>(in);
+    if (fp8)
+        pack_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            x, N, C, S, out, amax_bits, scale_out, c_tiles, s_tiles);
+    else
+        pack_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            x, N, C, S, out, amax_bits, scale_out, c_tiles, s_tiles);
+    return cudaGetLastError();
+}
+
+}  // namespace c3d

@@ -1,0 +1,709 @@
+// conv3d_api.cu -- the C ABI of libconv3d.so (declared in include/conv3d.h):
+// argument checks, output dims, dispatch class, tile plan, TMA descriptor
+// encoding and kernel launches.  No allocation: every buffer is the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "conv3d.h"
+#include "internal.h"
+#include "tile_table.h"
+
+namespace c3d {
+
+__device__ int g_device_status;
+
+namespace {
+
+thread_local char t_last_error[256] = "";
+
+void set_error(const char* fmt, const char* a = "", long long b = 0) {
+    std::snprintf(t_last_error, sizeof t_last_error, fmt, a, b);
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(t_last_error, sizeof t_last_error, "%s: %s", where, cudaGetErrorString(e));
+    return CONV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ driver entry points
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                   cuuint32_t, cuuint32_t, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_entry_once;
+EncodeTiledFn g_encode_tiled = nullptr;
+EncodeIm2colFn g_encode_im2col = nullptr;
+
+bool load_entry_points() {
+    std::call_once(g_entry_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(fn);
+    });
+    return g_encode_tiled != nullptr && g_encode_im2col != nullptr;
+}
+
+// ------------------------------------------------------------ per-device state
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready;
+    int num_sms;
+    int smem_optin;
+    int* status;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device ordinal out of range");
+        return CONV_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major < 10) {
+            set_error("this library needs a Blackwell (sm_10x) GPU");
+            return CONV_ERR_UNSUPPORTED;
+        }
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress");
+        d.status = static_cast<int*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return CONV_OK;
+}
+
+unsigned long long g_wait_ns = 2000000000ull;
+
+// ------------------------------------------------------------ geometry
+struct Geo {
+    long long N, D, H, W, C, K, T, R, S;
+    int sd, sh, sw, pd, ph, pw, dd, dh, dw;
+    long long Do, Ho, Wo;
+};
+
+long long out_extent(long long in, long long f, int s, int p, int d) {
+    const long long span = in + 2LL * p - static_cast<long long>(d) * (f - 1) - 1;
+    if (span < 0) return 0;
+    return span / s + 1;
+}
+
+int make_geo(const int64_t xd[5], const int64_t wd[5], const int st[3], const int pa[3],
+             const int di[3], Geo* g) {
+    if (!xd || !wd || !st || !pa || !di) {
+        set_error("null shape argument");
+        return CONV_ERR_INVALID;
+    }
+    for (int i = 0; i < 5; ++i)
+        if (xd[i] <= 0 || wd[i] <= 0 || xd[i] > 0x7FFFFFFFll || wd[i] > 0x7FFFFFFFll) {
+            set_error("dims must be in [1, 2^31)");
+            return CONV_ERR_INVALID;
+        }
+    for (int i = 0; i < 3; ++i)
+        if (st[i] <= 0 || di[i] <= 0 || pa[i] < 0) {
+            set_error("strides and dilations must be positive, pads non-negative");
+            return CONV_ERR_INVALID;
+        }
+    if (xd[4] != wd[4]) {
+        set_error("x and w disagree on C");
+        return CONV_ERR_INVALID;
+    }
+    g->N = xd[0]; g->D = xd[1]; g->H = xd[2]; g->W = xd[3]; g->C = xd[4];
+    g->K = wd[0]; g->T = wd[1]; g->R = wd[2]; g->S = wd[3];
+    g->sd = st[0]; g->sh = st[1]; g->sw = st[2];
+    g->pd = pa[0]; g->ph = pa[1]; g->pw = pa[2];
+    g->dd = di[0]; g->dh = di[1]; g->dw = di[2];
+    g->Do = out_extent(g->D, g->T, g->sd, g->pd, g->dd);
+    g->Ho = out_extent(g->H, g->R, g->sh, g->ph, g->dh);
+    g->Wo = out_extent(g->W, g->S, g->sw, g->pw, g->dw);
+    if (g->Do <= 0 || g->Ho <= 0 || g->Wo <= 0) {
+        set_error("empty output");
+        return CONV_ERR_INVALID;
+    }
+    return CONV_OK;
+}
+
+// ------------------------------------------------------------ plan
+struct Plan {
+    int cls, amode, fp8, elt;
+    int BN, BK, stages, splits, group_m;
+    long long M;
+    int m_tiles, n_tiles, k_steps, taps, steps_per_split, hw_tiles, HW;
+    long long g_row_bytes;   // GEMM classes: bytes of one A / B row
+    int grid;
+    size_t smem;
+    uint32_t tmem_cols;
+    size_t ws_bytes;         // split-K workspace needed by this plan
+};
+
+int pick_bk(long long row_bytes) {
+    // bytes per k-step row: the choice that pads the channel / reduction run least
+    int best = 128;
+    long long best_pad = ((row_bytes + 127) / 128) * 128;
+    for (int bk : {64, 32}) {
+        const long long pad = ((row_bytes + bk - 1) / bk) * bk;
+        if (pad < best_pad) {
+            best = bk;
+            best_pad = pad;
+        }
+    }
+    return best;
+}
+
+int pick_bn(long long K) {
+    int best = 256;
+    long long best_pad = ((K + 255) / 256) * 256;
+    for (int bn = 224; bn >= 32; bn -= 32) {
+        const long long pad = ((K + bn - 1) / bn) * bn;
+        if (pad < best_pad) {
+            best = bn;
+            best_pad = pad;
+        }
+    }
+    return best;
+}
+
+const TileEntry* lookup_tile(int fp8, int cls, const Geo& g, long long M) {
+    const long long trs = g.T * g.R * g.S;
+    for (const TileEntry& e : kTileTable) {
+        if (e.C == 0) continue;
+        if (e.fp8 == fp8 && e.cls == cls && e.C == g.C && e.K == g.K && e.TRS == trs &&
+            M >= e.m_lo && M <= e.m_hi)
+            return &e;
+    }
+    return nullptr;
+}
+
+// CONV3D_FORCE_TILE="BN,BK,stages,group_m,splits" (0 keeps the default) -- for sweeps.
+void force_tile(int* bn, int* bk, int* st, int* grp, int* spl) {
+    const char* s = std::getenv("CONV3D_FORCE_TILE");
+    if (!s || !*s) return;
+    int v[5] = {0, 0, 0, 0, 0};
+    std::sscanf(s, "%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4]);
+    if (v[0] > 0) *bn = v[0];
+    if (v[1] > 0) *bk = v[1];
+    if (v[2] > 0) *st = v[2];
+    if (v[3] > 0) *grp = v[3];
+    if (v[4] > 0) *spl = v[4];
+}
+
+int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_split, Plan* P) {
+    if (dtype != CONV_DTYPE_BF16 && dtype != CONV_DTYPE_FP8_E4M3) {
+        set_error("unknown dtype");
+        return CONV_ERR_INVALID;
+    }
+    std::memset(P, 0, sizeof *P);
+    P->fp8 = dtype == CONV_DTYPE_FP8_E4M3;
+    P->elt = P->fp8 ? 1 : 2;
+    const long long elt = P->elt;
+    const bool zero_pad = g.pd == 0 && g.ph == 0 && g.pw == 0;
+    const bool unit_stride = g.sd == 1 && g.sh == 1 && g.sw == 1;
+    const bool point_output = zero_pad && g.D == g.T && g.H == g.R && g.W == g.S;
+    const bool pointwise = g.T == 1 && g.R == 1 && g.S == 1 && unit_stride && zero_pad;
+    long long rg = 0;   // GEMM reduction length (elements)
+    if (point_output || pointwise) {
+        P->cls = CONV_CLASS_POINT_GEMM;
+        P->M = point_output ? g.N : g.N * g.D * g.H * g.W;
+        rg = point_output ? g.T * g.R * g.S * g.C : g.C;
+        P->g_row_bytes = rg * elt;
+        if (P->g_row_bytes % 16 == 0)
+            P->amode = AM_GEMM_TMA;
+        else if (P->g_row_bytes % 4 == 0)
+            P->amode = AM_GEMM_GATHER;
+        else {
+            set_error("point-output GEMM needs T*R*S*C*elem_bytes %% 4 == 0");
+            return CONV_ERR_UNSUPPORTED;
+        }
+    } else {
+        if ((g.C * elt) % 16 != 0) {
+            set_error("implicit GEMM needs C*elem_bytes %% 16 == 0");
+            return CONV_ERR_UNSUPPORTED;
+        }
+        P->M = g.N * g.Do * g.Ho * g.Wo;
+        if (g.R == 1 && g.S == 1 && g.sh == 1 && g.sw == 1 && g.ph == 0 && g.pw == 0) {
+            P->cls = CONV_CLASS_TEMPORAL;
+            P->amode = AM_TEMPORAL;
+            if (g.H * g.W > 0x7FFFFFFFll || g.D > 0x7FFFFFFFll) {
+                set_error("temporal plane too large");
+                return CONV_ERR_UNSUPPORTED;
+            }
+        } else {
+            P->cls = CONV_CLASS_GENERIC;
+            P->amode = AM_IM2COL;
+            // im2col descriptor limits for a 5-D tensor: traversal stride <= 8, box
+            // corners in [-16, 15], tap offsets below 32
+            const int pads[3] = {g.pd, g.ph, g.pw};
+            const int sts[3] = {g.sd, g.sh, g.sw};
+            const long long ext[3] = {g.dd * (g.T - 1), g.dh * (g.R - 1), g.dw * (g.S - 1)};
+            for (int i = 0; i < 3; ++i) {
+                const long long up = pads[i] - ext[i];
+                if (sts[i] > 8 || pads[i] > 16 || up < -16 || up > 15 || ext[i] > 31) {
+                    set_error("im2col limits: stride <= 8, pad <= 16, dilated filter extent <= 32");
+                    return CONV_ERR_UNSUPPORTED;
+                }
+            }
+        }
+    }
+    if (P->M > 0x7FFFFFFFll * 128ll) {
+        set_error("too many output rows");
+        return CONV_ERR_UNSUPPORTED;
+    }
+
+    // tile defaults
+    int BN = pick_bn(g.K);
+    int BK = (P->amode == AM_GEMM_GATHER) ? 128 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? rg * elt : g.C * elt);
+    int stages = 0, group_m = 8, splits = 0;
+    if (const TileEntry* e = lookup_tile(P->fp8, P->cls, g, P->M)) {
+        if (e->BN) BN = e->BN;
+        if (e->BK) BK = e->BK;
+        if (e->stages) stages = e->stages;
+        if (e->group_m) group_m = e->group_m;
+        if (e->splits) splits = e->splits;
+    }
+    force_tile(&BN, &BK, &stages, &group_m, &splits);
+    if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128) ||
+        (P->amode == AM_GEMM_GATHER && BK != 128) || group_m < 1) {
+        set_error("invalid tile override");
+        return CONV_ERR_INVALID;
+    }
+    P->BN = BN;
+    P->BK = BK;
+    P->group_m = group_m;
+
+    if (P->cls == CONV_CLASS_POINT_GEMM) {
+        P->taps = 1;
+        P->k_steps = static_cast<int>((rg * elt + BK - 1) / BK);
+    } else {
+        P->taps = static_cast<int>(g.T * g.R * g.S);
+        const long long chunks = (g.C * elt + BK - 1) / BK;
+        P->k_steps = static_cast<int>(chunks * P->taps);
+    }
+    if (P->cls == CONV_CLASS_TEMPORAL) {
+        P->HW = static_cast<int>(g.H * g.W);
+        P->hw_tiles = (P->HW + kBM - 1) / kBM;
+        P->m_tiles = static_cast<int>(g.N * g.Do * P->hw_tiles);
+    } else {
+        P->m_tiles = static_cast<int>((P->M + kBM - 1) / kBM);
+    }
+    P->n_tiles = static_cast<int>((g.K + BN - 1) / BN);
+
+    // split-K when the output tiles leave most SMs idle
+    const long long tiles = static_cast<long long>(P->m_tiles) * P->n_tiles;
+    if (splits == 0) {
+        splits = 1;
+        if (tiles * 2 <= num_sms && P->k_steps >= 4)
+            splits = static_cast<int>(std::min<long long>({num_sms / tiles, P->k_steps / 2, 32}));
+    }
+    splits = std::max(1, std::min(splits, P->k_steps));
+    P->steps_per_split = (P->k_steps + splits - 1) / splits;
+    splits = (P->k_steps + P->steps_per_split - 1) / P->steps_per_split;
+    P->ws_bytes = splits > 1 ? static_cast<size_t>(splits) * P->M * g.K * sizeof(float) : 0;
+    if (splits > 1 && !allow_split) {
+        splits = 1;
+        P->steps_per_split = P->k_steps;
+    }
+    P->splits = splits;
+    if (tiles * splits > 0x7FFFFFFFll) {
+        set_error("too many work units");
+        return CONV_ERR_UNSUPPORTED;
+    }
+
+    // pipeline depth from the shared-memory budget
+    const size_t stage_bytes = static_cast<size_t>(kBM + BN) * BK;
+    const size_t fixed = 1024 + 256;
+    const int max_stages = static_cast<int>((smem_optin - fixed) / stage_bytes);
+    if (stages == 0) stages = std::min(8, max_stages);
+    const int min_stages = (P->amode == AM_GEMM_GATHER) ? 3 : 2;
+    if (stages < min_stages || stages > max_stages) {
+        set_error("pipeline depth out of range for this tile");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    P->stages = stages;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(2 * BN)) cols <<= 1;
+    P->tmem_cols = cols;
+    P->smem = fixed + stage_bytes * stages;
+    // a CTA holding all 512 TMEM columns must be alone on its SM
+    if (cols > 256 && P->smem < static_cast<size_t>(smem_optin) / 2 + 1024)
+        P->smem = static_cast<size_t>(smem_optin) / 2 + 1024;
+    const long long units = tiles * splits;
+    P->grid = static_cast<int>(std::min<long long>(units, num_sms));
+    return CONV_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+CUtensorMapSwizzle swizzle_for(int bk) {
+    return bk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : (bk == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+uint32_t desc_layout_for(int bk) { return bk == 128 ? 2u : (bk == 64 ? 4u : 6u); }
+
+int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, int bk) {
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode_tiled(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                rank, const_cast<void*>(ptr), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk),
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (code %s%lld)", "", static_cast<long long>(r));
+        return CONV_ERR_CUDA;
+    }
+    return CONV_OK;
+}
+
+int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtensorMap* tmA,
+               CUtensorMap* tmB) {
+    const cuuint64_t elt = static_cast<cuuint64_t>(P.elt);
+    const cuuint32_t bke = static_cast<cuuint32_t>(P.BK / P.elt);
+    if (P.amode == AM_GEMM_GATHER) {
+        std::memset(tmA, 0, sizeof *tmA);
+        std::memset(tmB, 0, sizeof *tmB);
+        return CONV_OK;
+    }
+    if (P.amode == AM_GEMM_TMA) {
+        const cuuint64_t rg = static_cast<cuuint64_t>(P.g_row_bytes) / elt;
+        const cuuint64_t adims[2] = {rg, static_cast<cuuint64_t>(P.M)};
+        const cuuint64_t astr[1] = {static_cast<cuuint64_t>(P.g_row_bytes)};
+        const cuuint32_t abox[2] = {bke, static_cast<cuuint32_t>(kBM)};
+        int rc = encode_tiled(tmA, P.fp8, 2, x, adims, astr, abox, P.BK);
+        if (rc) return rc;
+        const cuuint64_t bdims[2] = {rg, static_cast<cuuint64_t>(g.K)};
+        const cuuint32_t bbox[2] = {bke, static_cast<cuuint32_t>(P.BN)};
+        return encode_tiled(tmB, P.fp8, 2, w, bdims, astr, bbox, P.BK);
+    }
+    // weight: [K, T*R*S, C] -> dims {C, TRS, K}, box {bke, 1, BN}
+    {
+        const cuuint64_t trs = static_cast<cuuint64_t>(g.T * g.R * g.S);
+        const cuuint64_t bdims[3] = {static_cast<cuuint64_t>(g.C), trs, static_cast<cuuint64_t>(g.K)};
+        const cuuint64_t bstr[2] = {static_cast<cuuint64_t>(g.C) * elt,
+                                    static_cast<cuuint64_t>(g.C) * elt * trs};
+        const cuuint32_t bbox[3] = {bke, 1, static_cast<cuuint32_t>(P.BN)};
+        int rc = encode_tiled(tmB, P.fp8, 3, w, bdims, bstr, bbox, P.BK);
+        if (rc) return rc;
+    }
+    const cuuint64_t row = static_cast<cuuint64_t>(g.C) * elt;
+    if (P.amode == AM_TEMPORAL) {
+        // x as [N, D, H*W, C] -> dims {C, HW, D, N}, box {bke, 128, 1, 1}
+        const cuuint64_t hw = static_cast<cuuint64_t>(g.H * g.W);
+        const cuuint64_t adims[4] = {static_cast<cuuint64_t>(g.C), hw, static_cast<cuuint64_t>(g.D),
+                                     static_cast<cuuint64_t>(g.N)};
+        const cuuint64_t astr[3] = {row, row * hw, row * hw * static_cast<cuuint64_t>(g.D)};
+        const cuuint32_t abox[4] = {bke, static_cast<cuuint32_t>(kBM), 1, 1};
+        return encode_tiled(tmA, P.fp8, 4, x, adims, astr, abox, P.BK);
+    }
+    // generic: im2col over NDHWC -> dims {C, W, H, D, N}
+    const cuuint64_t adims[5] = {static_cast<cuuint64_t>(g.C), static_cast<cuuint64_t>(g.W),
+                                 static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.D),
+                                 static_cast<cuuint64_t>(g.N)};
+    const cuuint64_t astr[4] = {row, row * static_cast<cuuint64_t>(g.W),
+                                row * static_cast<cuuint64_t>(g.W * g.H),
+                                row * static_cast<cuuint64_t>(g.W * g.H * g.D)};
+    // bounding box of window corners along {W, H, D}: [-pad, extent - 1 + pad - dil*(f-1)]
+    const int lower[3] = {-g.pw, -g.ph, -g.pd};
+    const int upper[3] = {g.pw - g.dw * static_cast<int>(g.S - 1), g.ph - g.dh * static_cast<int>(g.R - 1),
+                          g.pd - g.dd * static_cast<int>(g.T - 1)};
+    const cuuint32_t es[5] = {1, static_cast<cuuint32_t>(g.sw), static_cast<cuuint32_t>(g.sh),
+                              static_cast<cuuint32_t>(g.sd), 1};
+    CUresult r = g_encode_im2col(
+        tmA, P.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+        const_cast<void*>(x), adims, astr, lower, upper, bke, static_cast<cuuint32_t>(kBM), es,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(P.BK), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeIm2col failed (code %s%lld)", "", static_cast<long long>(r));
+        return CONV_ERR_CUDA;
+    }
+    return CONV_OK;
+}
+
+uint32_t make_idesc(int fp8, int bn) {
+    uint32_t d = 0;
+    d |= 1u << 4;                       // D format: f32
+    if (!fp8) d |= (1u << 7) | (1u << 10);   // A, B format: bf16 (kind::f16); e4m3 = 0 (kind::f8f6f4)
+    d |= static_cast<uint32_t>(bn >> 3) << 17;   // N >> 3
+    d |= static_cast<uint32_t>(kBM >> 4) << 24;  // M >> 4
+    return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int* device_status_ptr() {
+    DeviceInfo* d = nullptr;
+    if (device_info(&d) != CONV_OK) return nullptr;
+    return d->status;
+}
+
+}  // namespace c3d
+
+using namespace c3d;
+
+extern "C" {
+
+const char* conv_last_error(void) { return t_last_error; }
+
+const char* conv_status_string(int status) {
+    switch (status) {
+        case CONV_OK: return "CONV_OK";
+        case CONV_ERR_INVALID: return "CONV_ERR_INVALID: invalid argument";
+        case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: shape not covered by the kernels";
+        case CONV_ERR_CUDA: return "CONV_ERR_CUDA: CUDA call failed";
+        case CONV_ERR_TIMEOUT: return "CONV_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+        default: return "unknown conv_status";
+    }
+}
+
+void conv_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns; }
+
+int conv_out_dims(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                  const int pad[3], const int dil[3], int64_t out_dims[5]) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!out_dims) {
+        set_error("null out_dims");
+        return CONV_ERR_INVALID;
+    }
+    out_dims[0] = g.N;
+    out_dims[1] = g.Do;
+    out_dims[2] = g.Ho;
+    out_dims[3] = g.Wo;
+    out_dims[4] = g.K;
+    return CONV_OK;
+}
+
+int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                  const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
+                  int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
+                  size_t* workspace_bytes) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    int sms = num_sms, smem = 232448;
+    if (sms <= 0) {
+        DeviceInfo* d = nullptr;
+        if ((rc = device_info(&d))) return rc;
+        sms = d->num_sms;
+        smem = d->smem_optin;
+    }
+    Plan P;
+    if ((rc = make_plan(g, dtype, sms, smem, true, &P))) return rc;
+    if (cls) *cls = P.cls;
+    if (tile_n) *tile_n = P.BN;
+    if (k_bytes) *k_bytes = P.BK;
+    if (stages) *stages = P.stages;
+    if (splits) *splits = P.splits;
+    if (ctas) *ctas = P.grid;
+    if (workspace_bytes) *workspace_bytes = P.ws_bytes;
+    return CONV_OK;
+}
+
+int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+             const int stride[3], const int pad[3], const int dil[3], int dtype,
+             const float* scale_x, const float* scale_w, void* out, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!x || !w || !out) {
+        set_error("null tensor pointer");
+        return CONV_ERR_INVALID;
+    }
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (workspace && !aligned16(workspace)) ||
+        (scale_x && (reinterpret_cast<uintptr_t>(scale_x) & 3u)) ||
+        (scale_w && (reinterpret_cast<uintptr_t>(scale_w) & 3u))) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    if (!load_entry_points()) {
+        set_error("cuTensorMapEncode* entry points unavailable");
+        return CONV_ERR_CUDA;
+    }
+    Plan P;
+    if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, true, &P))) return rc;
+    if (P.splits > 1 && (workspace == nullptr || workspace_bytes < P.ws_bytes)) {
+        if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, false, &P))) return rc;
+    }
+    CUtensorMap tmA, tmB;
+    if ((rc = build_maps(g, P, x, w, &tmA, &tmB))) return rc;
+
+    KParams k;
+    std::memset(&k, 0, sizeof k);
+    k.N = static_cast<int>(g.N); k.D = static_cast<int>(g.D); k.H = static_cast<int>(g.H);
+    k.W = static_cast<int>(g.W); k.C = static_cast<int>(g.C);
+    k.T = static_cast<int>(g.T); k.R = static_cast<int>(g.R); k.S = static_cast<int>(g.S);
+    k.Do = static_cast<int>(g.Do); k.Ho = static_cast<int>(g.Ho); k.Wo = static_cast<int>(g.Wo);
+    k.sd = g.sd; k.sh = g.sh; k.sw = g.sw; k.pd = g.pd; k.ph = g.ph; k.pw = g.pw;
+    k.dd = g.dd; k.dh = g.dh; k.dw = g.dw;
+    k.M = P.M;
+    k.K = static_cast<int>(g.K);
+    k.HW = P.HW;
+    k.hw_tiles = P.hw_tiles;
+    k.m_tiles = P.m_tiles;
+    k.n_tiles = P.n_tiles;
+    k.splits = P.splits;
+    k.k_steps = P.k_steps;
+    k.steps_per_split = P.steps_per_split;
+    k.taps = P.taps;
+    k.group_m = P.group_m;
+    k.BN = P.BN;
+    k.BK = P.BK;
+    k.stages = P.stages;
+    k.a_stage_bytes = static_cast<uint32_t>(kBM * P.BK);
+    k.b_stage_bytes = static_cast<uint32_t>(P.BN * P.BK);
+    k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
+    k.idesc = make_idesc(P.fp8, P.BN);
+    k.layout = desc_layout_for(P.BK);
+    k.sbo = static_cast<uint32_t>(8 * P.BK);
+    k.tmem_cols = P.tmem_cols;
+    k.ga = static_cast<const unsigned char*>(x);
+    k.gb = static_cast<const unsigned char*>(w);
+    k.g_row_bytes = P.g_row_bytes;
+    k.out = out;
+    k.ws = P.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    k.scale_x = scale_x;
+    k.scale_w = scale_w;
+    k.status = dev->status;
+    k.wait_ns = g_wait_ns;
+
+    if (std::getenv("CONV3D_LOG")) {
+        std::fprintf(stderr,
+                     "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
+                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u\n",
+                     P.cls, P.amode, P.fp8, P.M, k.K, P.BN, P.BK, P.stages, P.splits, P.k_steps,
+                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols);
+    }
+    cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, k, P.grid, P.smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
+    if (P.splits > 1) {
+        e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, dev->num_sms,
+                                 stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+    }
+    return CONV_OK;
+}
+
+int pack_ncdhw_bf16_to_ndhwc(const void* in, const int64_t dims[5], void* out,
+                             cudaStream_t stream) {
+    if (!in || !out || !dims) {
+        set_error("null argument");
+        return CONV_ERR_INVALID;
+    }
+    for (int i = 0; i < 5; ++i)
+        if (dims[i] <= 0) {
+            set_error("dims must be positive");
+            return CONV_ERR_INVALID;
+        }
+    if (!aligned16(in) || !aligned16(out)) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    const long long S = dims[2] * dims[3] * dims[4];
+    cudaError_t e = launch_pack(in, dims[0], dims[1], S, out, 0, nullptr, nullptr, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    return CONV_OK;
+}
+
+size_t pack_fp8_workspace_size(void) { return 16; }
+
+int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* out,
+                                 float* scale_out, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    if (!in || !out || !dims || !scale_out || !workspace) {
+        set_error("null argument");
+        return CONV_ERR_INVALID;
+    }
+    if (workspace_bytes < pack_fp8_workspace_size()) {
+        set_error("workspace too small");
+        return CONV_ERR_INVALID;
+    }
+    for (int i = 0; i < 5; ++i)
+        if (dims[i] <= 0) {
+            set_error("dims must be positive");
+            return CONV_ERR_INVALID;
+        }
+    if (!aligned16(in) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(scale_out) & 3u)) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    const long long S = dims[2] * dims[3] * dims[4];
+    const long long n = dims[0] * dims[1] * S;
+    unsigned int* amax = static_cast<unsigned int*>(workspace);
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    e = launch_amax_bf16(in, n, amax, dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "amax launch");
+    e = launch_pack(in, dims[0], dims[1], S, out, 1, amax, scale_out, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    return CONV_OK;
+}
+
+int conv_get_device_status(int* device_status) {
+    if (!device_status) {
+        set_error("null argument");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    *device_status = v;
+    return CONV_OK;
+}
+
+}  // extern "C"

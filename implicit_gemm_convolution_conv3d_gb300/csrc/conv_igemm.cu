@@ -1,0 +1,491 @@
+// conv_igemm.cu -- the forward implicit-GEMM convolution kernel for sm_103a.
+//
+// GEMM view (FlyDSL PR #860 "fp8 conv3d: 8-wave GEMM pipeline + BIG_IN fix",
+// PR summary): rows M = output positions (n, od, oh, ow), columns = the K
+// filters, reduction over (channel chunk, tap) of the KTRSC weight rows.  A
+// point-output conv is the same kernel with a plain row-major A (MIOpen PR
+// #10912, description).
+//
+// One persistent CTA per SM walks a strided list of work units (m-tile,
+// n-tile, split).  Warp roles:
+//   warp 0      TMA producer: one A box and one B box per k-step into a
+//               multi-stage shared-memory ring (full/empty mbarriers).  The A
+//               box is an im2col-mode box (generic conv), a 4-D tiled box of
+//               H*W rows (T x 1 x 1 temporal conv) or a 2-D tiled box (GEMM);
+//               padding taps read as zeros through TMA bounds.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (kind::f16 for
+//               bf16, kind::f8f6f4 for e4m3) into a double-buffered fp32
+//               accumulator and commits stages back to the producer.
+//   warps 2..5  epilogue: tcgen05.ld -> scale -> bf16 -> 16-byte stores (or
+//               fp32 split-K partials), overlapping the next tile's mainloop.
+//   warps 6..9  (row-gather GEMM only) cp.async producers for operands whose
+//               rows are not 16-byte aligned.
+// Every wait is bounded: on expiry the kernel records CONV_ERR_TIMEOUT,
+// drains its copies and MMAs in flight, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace c3d {
+
+namespace {
+
+constexpr int kStatusTimeout = 4;
+constexpr unsigned long long kDrainNs = 1000000000ull;
+
+struct Unit {
+    int m_tile, n_tile, split;
+};
+
+// Work unit -> (m-tile, n-tile, split).  Within a split, tiles are walked in
+// groups of `group_m` m-tiles: down M first, then across N, so that CTAs
+// running at the same time share both A rows and B columns in L2.
+__device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
+    const int tiles = p.m_tiles * p.n_tiles;
+    Unit r;
+    r.split = u / tiles;
+    const int t = u - r.split * tiles;
+    const int group = p.group_m * p.n_tiles;
+    const int g = t / group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.group_m, p.m_tiles - first_m);
+    const int local = t - g * group;
+    r.m_tile = first_m + local % gm;
+    r.n_tile = local / gm;
+    return r;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       int* status, unsigned long long limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1u;
+            atomicExch(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait on phase `parity` of an mbarrier; false on timeout or abort.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         int* status, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, status, limit_ns);
+}
+
+// Cleanup wait: bounded by a fixed limit, ignores the abort flag.
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainNs) return;
+    }
+}
+
+// Byte offset of (row, byte) inside a 128-byte-swizzled K-major tile whose
+// base is 1024-byte aligned: the 16-byte chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t swz128(int row, int byte) {
+    return static_cast<uint32_t>(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store 32 accumulator columns of one output row (bf16).
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                               float scale, int count, bool vec_ok) {
+    if (count == 32 && vec_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * scale, __uint_as_float(v[8 * i + 1]) * scale);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * scale, __uint_as_float(v[8 * i + 3]) * scale);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * scale, __uint_as_float(v[8 * i + 5]) * scale);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * scale, __uint_as_float(v[8 * i + 7]) * scale);
+            d4[i] = o;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < count) dst[i] = __float2bfloat16_rn(__uint_as_float(v[i]) * scale);
+    }
+}
+
+// Store 32 fp32 split-K partial columns of one output row.
+__device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&v)[32], int count,
+                                              bool vec_ok) {
+    if (count == 32 && vec_ok) {
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < count) dst[i] = __uint_as_float(v[i]);
+    }
+}
+
+// cp.async row-gather producer (AM_GEMM_GATHER): 128 threads copy the A and B
+// tiles of each k-step in VEC-byte pieces into the 128B-swizzled layout, zero
+// filling rows past M / K and columns past the reduction length.  A stage is
+// released LAG k-steps after its copies were issued.
+template <int VEC>
+__device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0, uint32_t empty0,
+                                volatile uint32_t* abort_flag, int g) {
+    constexpr int LAG = 2;
+    const int total_units = p.m_tiles * p.n_tiles * p.splits;
+    const int ppr = p.BK / VEC;
+    const int pieces = (kBM + p.BN) * ppr;
+    int stage = 0;
+    uint32_t phase = 0;
+    long long it = 0;
+    bool ok_run = true;
+    for (int u = blockIdx.x; u < total_units && ok_run; u += gridDim.x) {
+        const Unit t = decode_unit(u, p);
+        const int ks0 = t.split * p.steps_per_split;
+        const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+        const long long m0 = static_cast<long long>(t.m_tile) * kBM;
+        const long long n0 = static_cast<long long>(t.n_tile) * p.BN;
+        for (int ks = ks0; ks < ks1; ++ks) {
+            if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
+                ok_run = false;
+                break;
+            }
+            const uint32_t adst = tiles + stage * p.stage_bytes;
+            const uint32_t bdst = adst + p.a_stage_bytes;
+            const long long kb = static_cast<long long>(ks) * p.BK;
+            for (int i = g; i < pieces; i += kGatherThreads) {
+                const int row = i / ppr;
+                const int byte = (i - row * ppr) * VEC;
+                const long long colb = kb + byte;
+                const unsigned char* src;
+                uint32_t dst;
+                bool ok;
+                if (row < kBM) {
+                    const long long m = m0 + row;
+                    ok = (m < p.M) && (colb < p.g_row_bytes);
+                    src = ok ? p.ga + m * p.g_row_bytes + colb : p.ga;
+                    dst = adst + swz128(row, byte);
+                } else {
+                    const int nb = row - kBM;
+                    const long long n = n0 + nb;
+                    ok = (n < p.K) && (colb < p.g_row_bytes);
+                    src = ok ? p.gb + n * p.g_row_bytes + colb : p.gb;
+                    dst = bdst + swz128(nb, byte);
+                }
+                cp_async<VEC>(dst, src, ok ? VEC : 0u);
+            }
+            cp_async_commit();
+            if (it >= LAG) {
+                cp_async_wait<LAG>();
+                fence_proxy_async_smem();
+                mbar_arrive(full0 + 8 * static_cast<uint32_t>((it - LAG) % p.stages));
+            }
+            ++it;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    if (ok_run && !*abort_flag) {
+        for (long long j = (it > LAG ? it - LAG : 0); j < it; ++j)
+            mbar_arrive(full0 + 8 * static_cast<uint32_t>(j % p.stages));
+    }
+}
+
+template <int AMODE, int FP8>
+__global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
+    conv_igemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const KParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* base_ptr = smem_raw + (base - raw);
+    const uint32_t tiles = base;
+    const uint32_t ring_bytes = static_cast<uint32_t>(p.stages) * p.stage_bytes;
+    const uint32_t full0 = base + ring_bytes;
+    const uint32_t empty0 = full0 + 8u * p.stages;
+    const uint32_t tfull0 = empty0 + 8u * p.stages;
+    const uint32_t tempty0 = tfull0 + 16u;
+    const uint32_t drain_bar = tempty0 + 16u;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + ring_bytes + 16u * p.stages + 40u);
+    // misc[0] TMEM base, misc[1] abort flag, misc[2] k-steps issued, misc[3] k-steps consumed
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total_units = p.m_tiles * p.n_tiles * p.splits;
+    constexpr bool kGather = (AMODE == AM_GEMM_GATHER);
+    constexpr int kElt = FP8 ? 1 : 2;
+    const int bke = p.BK / kElt;   // elements of one row per k-step
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, kGather ? kGatherThreads : 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        misc[1] = 0u;
+        misc[2] = 0u;
+        misc[3] = 0u;
+        fence_mbar_init();
+        if (!kGather) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(misc), p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = misc[0];
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (!kGather && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok_run = true;
+            for (int u = blockIdx.x; u < total_units && ok_run; u += gridDim.x) {
+                const Unit t = decode_unit(u, p);
+                const int ks0 = t.split * p.steps_per_split;
+                const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+                const int n0 = t.n_tile * p.BN;
+                int aw = 0, ah = 0, ad = 0, an = 0, am0 = 0;
+                if (AMODE == AM_IM2COL) {
+                    const long long m0 = static_cast<long long>(t.m_tile) * kBM;
+                    const int ow = static_cast<int>(m0 % p.Wo);
+                    const long long q1 = m0 / p.Wo;
+                    const int oh = static_cast<int>(q1 % p.Ho);
+                    const long long q2 = q1 / p.Ho;
+                    const int od = static_cast<int>(q2 % p.Do);
+                    an = static_cast<int>(q2 / p.Do);
+                    aw = ow * p.sw - p.pw;
+                    ah = oh * p.sh - p.ph;
+                    ad = od * p.sd - p.pd;
+                } else if (AMODE == AM_TEMPORAL) {
+                    const int plane = t.m_tile / p.hw_tiles;
+                    const int hwb = t.m_tile - plane * p.hw_tiles;
+                    const int od = plane % p.Do;
+                    an = plane / p.Do;
+                    ad = od * p.sd - p.pd;
+                    ah = hwb * kBM;   // first H*W row of the tile
+                } else {
+                    am0 = t.m_tile * kBM;
+                }
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
+                        ok_run = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_arrive_expect_tx(fb, p.stage_bytes);
+                    const uint32_t adst = tiles + stage * p.stage_bytes;
+                    const uint32_t bdst = adst + p.a_stage_bytes;
+                    if (AMODE == AM_GEMM_TMA) {
+                        const int k0 = ks * bke;
+                        tma_load_2d(adst, &tmA, fb, k0, am0);
+                        tma_load_2d(bdst, &tmB, fb, k0, n0);
+                    } else {
+                        // reduction order: channel chunk (outer), tap (inner)
+                        const int chunk = ks / p.taps;
+                        const int tap = ks - chunk * p.taps;
+                        const int fs = tap % p.S;
+                        const int fr = (tap / p.S) % p.R;
+                        const int ft = tap / (p.S * p.R);
+                        const int c0 = chunk * bke;
+                        if (AMODE == AM_IM2COL) {
+                            tma_load_im2col_5d(adst, &tmA, fb, c0, aw, ah, ad, an,
+                                               static_cast<uint16_t>(fs * p.dw),
+                                               static_cast<uint16_t>(fr * p.dh),
+                                               static_cast<uint16_t>(ft * p.dd));
+                        } else {
+                            tma_load_4d(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
+                        }
+                        tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
+                    }
+                    misc[2] = ++issued;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc_iter = 0;
+            uint32_t phase = 0, consumed = 0;
+            bool ok_run = true;
+            const int kmma = p.BK / 32;   // 32-byte K slices per stage
+            for (int u = blockIdx.x; u < total_units && ok_run; u += gridDim.x) {
+                const Unit t = decode_unit(u, p);
+                const int ks0 = t.split * p.steps_per_split;
+                const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+                const int acc = acc_iter & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
+                if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
+                        ok_run = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    misc[3] = ++consumed;
+                    const uint32_t a_s = tiles + stage * p.stage_bytes;
+                    const uint32_t b_s = a_s + p.a_stage_bytes;
+                    for (int k = 0; k < kmma; ++k) {
+                        const uint64_t adesc = make_smem_desc(a_s + 32 * k, p.sbo, p.layout);
+                        const uint64_t bdesc = make_smem_desc(b_s + 32 * k, p.sbo, p.layout);
+                        const uint32_t accum = (ks > ks0 || k > 0) ? 1u : 0u;
+                        if (FP8)
+                            tc_mma_f8(d_tmem, adesc, bdesc, p.idesc, accum);
+                        else
+                            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, accum);
+                    }
+                    tc_commit(empty0 + 8 * stage);
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok_run) break;
+                tc_commit(tfull0 + 8 * acc);
+                ++acc_iter;
+            }
+        }
+    } else if (warp < 2 + kEpiWarps) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;   // TMEM lane quarter this warp may read
+        const int row = q * 32 + lane;
+        float scale = 1.0f;
+        if (p.scale_x) scale *= *p.scale_x;
+        if (p.scale_w) scale *= *p.scale_w;
+        const bool vec_out = (p.K % 8) == 0;
+        const bool vec_ws = (p.K % 4) == 0;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        int acc_iter = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+            const Unit t = decode_unit(u, p);
+            const int acc = acc_iter & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
+            if (!wait_bar(tfull0 + 8 * acc, acc_phase, abort_flag, p.status, p.wait_ns)) break;
+            tc_fence_after();
+            long long m;
+            bool valid;
+            if (AMODE == AM_TEMPORAL) {
+                const int plane = t.m_tile / p.hw_tiles;
+                const int hw = (t.m_tile - plane * p.hw_tiles) * kBM + row;
+                valid = hw < p.HW;
+                m = static_cast<long long>(plane) * p.HW + hw;
+            } else {
+                m = static_cast<long long>(t.m_tile) * kBM + row;
+                valid = m < p.M;
+            }
+            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(acc * p.BN);
+            for (int j = 0; j < p.BN / 32; ++j) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tb + 32 * j, v);
+                tmem_ld_wait();
+                const int n0 = t.n_tile * p.BN + 32 * j;
+                if (valid && n0 < p.K) {
+                    const int cnt = min(32, p.K - n0);
+                    if (p.splits == 1) {
+                        store_row_bf16(out + m * p.K + n0, v, scale, cnt, vec_out);
+                    } else {
+                        float* dst = p.ws + (static_cast<long long>(t.split) * p.M + m) * p.K + n0;
+                        store_row_f32(dst, v, cnt, vec_ws);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            ++acc_iter;
+        }
+    } else if (kGather) {
+        // ------------------------------------------------------ row gather
+        const int g = threadIdx.x - (2 + kEpiWarps) * 32;
+        if (p.g_row_bytes % 8 == 0)
+            gather_producer<8>(p, tiles, full0, empty0, abort_flag, g);
+        else
+            gather_producer<4>(p, tiles, full0, empty0, abort_flag, g);
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // drain: TMA boxes issued but never waited for, then the MMAs in flight
+        if (warp == 0 && lane == 0 && !kGather) {
+            const uint32_t issued = misc[2], consumed = misc[3];
+            for (uint32_t i = consumed; i < issued; ++i)
+                drain_wait(full0 + 8 * (i % static_cast<uint32_t>(p.stages)),
+                           (i / static_cast<uint32_t>(p.stages)) & 1u);
+        }
+        if (warp == 1 && lane == 0) {
+            tc_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+template <int AM, int F8>
+cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const KParams& p, int grid,
+                       size_t smem, cudaStream_t stream) {
+    auto kern = conv_igemm_kernel<AM, F8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int threads = (AM == AM_GEMM_GATHER) ? 320 : 192;
+    kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                         const KParams& p, int grid, size_t smem, cudaStream_t stream) {
+    switch (amode * 2 + (fp8 ? 1 : 0)) {
+        case AM_IM2COL * 2 + 0: return launch_one<AM_IM2COL, 0>(tmA, tmB, p, grid, smem, stream);
+        case AM_IM2COL * 2 + 1: return launch_one<AM_IM2COL, 1>(tmA, tmB, p, grid, smem, stream);
+        case AM_TEMPORAL * 2 + 0: return launch_one<AM_TEMPORAL, 0>(tmA, tmB, p, grid, smem, stream);
+        case AM_TEMPORAL * 2 + 1: return launch_one<AM_TEMPORAL, 1>(tmA, tmB, p, grid, smem, stream);
+        case AM_GEMM_TMA * 2 + 0: return launch_one<AM_GEMM_TMA, 0>(tmA, tmB, p, grid, smem, stream);
+        case AM_GEMM_TMA * 2 + 1: return launch_one<AM_GEMM_TMA, 1>(tmA, tmB, p, grid, smem, stream);
+        case AM_GEMM_GATHER * 2 + 0:
+            return launch_one<AM_GEMM_GATHER, 0>(tmA, tmB, p, grid, smem, stream);
+        case AM_GEMM_GATHER * 2 + 1:
+            return launch_one<AM_GEMM_GATHER, 1>(tmA, tmB, p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace c3d

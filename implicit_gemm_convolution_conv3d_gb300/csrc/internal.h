@@ -1,0 +1,80 @@
+// internal.h -- parameter blocks and launch entry points shared by the host
+// library (conv3d_api.cu) and the kernel translation units.  Not part of the
+// public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace c3d {
+
+// How the A operand (the implicit im2col matrix) reaches shared memory.
+enum AMode : int {
+    AM_IM2COL = 0,     // TMA im2col-mode box per (tap, channel chunk)
+    AM_TEMPORAL = 1,   // T x 1 x 1 filter: one TMA tiled 4-D box of HW rows
+    AM_GEMM_TMA = 2,   // plain GEMM, 16-byte aligned rows: TMA tiled 2-D boxes
+    AM_GEMM_GATHER = 3 // plain GEMM, rows not 16-byte aligned: cp.async gather
+};
+
+constexpr int kBM = 128;               // rows of a tile (tcgen05 M, one CTA)
+constexpr int kEpiWarps = 4;           // warps reading TMEM in the epilogue
+constexpr int kGatherThreads = 128;    // producer threads of AM_GEMM_GATHER
+
+struct KParams {
+    // convolution geometry (A coordinates)
+    int N, D, H, W, C;
+    int T, R, S;
+    int Do, Ho, Wo;
+    int sd, sh, sw, pd, ph, pw, dd, dh, dw;
+    // GEMM view
+    long long M;        // output rows
+    int K;              // output columns (filters)
+    int HW;             // temporal: H*W rows per (n, d) plane
+    int hw_tiles;       // temporal: ceil(HW / 128)
+    int m_tiles, n_tiles, splits;
+    int k_steps;        // k-steps of the whole reduction
+    int steps_per_split;
+    int taps;           // conv: T*R*S
+    int group_m;        // raster: consecutive m-tiles per group
+    // tile / pipeline shape (runtime)
+    int BN;             // tile columns, multiple of 32, <= 256
+    int BK;             // bytes of one row per k-step: 32, 64 or 128
+    int stages;
+    uint32_t a_stage_bytes, b_stage_bytes, stage_bytes;
+    uint32_t idesc;     // tcgen05 instruction descriptor
+    uint32_t layout;    // smem descriptor swizzle code
+    uint32_t sbo;       // smem descriptor stride byte offset (8 rows)
+    uint32_t tmem_cols; // allocated TMEM columns (power of two >= 2*BN)
+    // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
+    const unsigned char* ga;
+    const unsigned char* gb;
+    long long g_row_bytes;
+    // outputs
+    void* out;          // bf16 [M, K]
+    float* ws;          // split-K partials [splits, M, K]
+    const float* scale_x;
+    const float* scale_w;
+    int* status;        // device status word
+    unsigned long long wait_ns;
+};
+
+// Launch the implicit-GEMM kernel (AMODE x dtype) on grid/smem from the plan.
+cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                         const KParams& p, int grid, size_t smem, cudaStream_t stream);
+
+// Deterministic split-K reduction: out = bf16(scale * sum_s ws[s]) in split order.
+cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
+                                 const float* scale_x, const float* scale_w, int num_sms,
+                                 cudaStream_t stream);
+
+// Pack kernels.
+cudaError_t launch_amax_bf16(const void* in, long long n, unsigned int* amax_bits, int num_sms,
+                             cudaStream_t stream);
+cudaError_t launch_pack(const void* in, long long N, long long C, long long S, void* out,
+                        int fp8, const unsigned int* amax_bits, float* scale_out,
+                        cudaStream_t stream);
+
+int* device_status_ptr();   // device address of the status word (current device)
+
+}  // namespace c3d

@@ -1,0 +1,157 @@
+/*
+ * conv3d.h -- C ABI of libconv3d.so: forward implicit-GEMM convolution
+ * (conv3d; conv2d and conv1d as the degenerate D=T=1 / H=R=1 forms) over
+ * channel-last NDHWC activations and KTRSC weights on one GB300 (sm_103a),
+ * plus the NCDHW -> NDHWC layout / fp8-e4m3 quantisation pack.
+ *
+ * Where each operation is defined (pages of the method):
+ *   - conv_fwd: FlyDSL PR #860 "fp8 conv3d: 8-wave GEMM pipeline + BIG_IN
+ *     fix" -- PR summary (the conv as a GEMM: M = output positions, N = K
+ *     filters, reduction over crs = C*T*R*S; weight = a plain KTRSC (k, crs)
+ *     matrix; E4M3FN fp8 inputs; fp32 accumulation), and its commits on the
+ *     temporal-only 3x1x1 decode, >2^31-element addressing, split-K and the
+ *     conv2d/conv1d reshape wrappers.  Point-output (patch-embedding) shapes
+ *     are one plain GEMM: MIOpen PR #10912 "Use a single GEMM for
+ *     point-output conv in all three directions", description.
+ *   - pack_ncdhw_bf16_to_ndhwc(_fp8): FlyDSL PR #860, commit adding the
+ *     tiled NCDHW->NDHWC bf16->fp8 pack kernel (replacing torch.permute) and
+ *     the commit fixing its >2 GB addressing.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense and contiguous, in the stated layout.  Every
+ *     device pointer must be 16-byte aligned.
+ *   - The caller owns and allocates every buffer (inputs, outputs, scales,
+ *     workspace).  The library never allocates or frees caller memory.  It
+ *     keeps only a per-device status word and per-process host state
+ *     (function pointers, device attributes).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do
+ *     not synchronise the host, except conv_get_device_status.
+ *   - Every function returns a conv_status; no exception crosses the ABI.
+ *     On any non-OK return nothing has been launched.
+ *   - Shapes are int64; tensors above 2^31 elements (and 2^32 bytes) are
+ *     supported; each single dimension must be below 2^31.
+ */
+#ifndef CONV3D_GB300_H
+#define CONV3D_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONV_OK = 0,
+    CONV_ERR_INVALID = 1,     /* null pointer, bad dims, C mismatch, misaligned pointer */
+    CONV_ERR_UNSUPPORTED = 2, /* shape the kernels do not cover (see conv_fwd) */
+    CONV_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+    CONV_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (device status) */
+} conv_status;
+
+typedef enum {
+    CONV_DTYPE_BF16 = 0,      /* x, w: bfloat16 */
+    CONV_DTYPE_FP8_E4M3 = 1   /* x, w: fp8 E4M3FN bytes, dequantised by scale_x / scale_w */
+} conv_dtype;
+
+/* Dispatch classes chosen by conv_fwd (reported by conv_fwd_plan). */
+typedef enum {
+    CONV_CLASS_GENERIC = 0,   /* implicit GEMM, A gathered by TMA im2col */
+    CONV_CLASS_TEMPORAL = 1,  /* T x 1 x 1 filter, unit H/W stride, no H/W pad: tiled TMA rows */
+    CONV_CLASS_POINT_GEMM = 2,/* point-output / pointwise conv: one plain GEMM */
+    CONV_CLASS_NONE = -1
+} conv_class;
+
+/* Output dims of the forward conv (torch semantics: floor((in + 2p - d(f-1) - 1)/s) + 1).
+ *   x_dims  = {N, D, H, W, C}     activation, NDHWC
+ *   w_dims  = {K, T, R, S, C}     weight, KTRSC
+ *   stride, pad, dil = {d, h, w}  pad is symmetric per dimension
+ *   out_dims (out) = {N, Do, Ho, Wo, K}
+ * Returns CONV_ERR_INVALID for non-positive dims/strides/dilations, negative
+ * pads, C mismatch, or an empty output.  Host-only; needs no GPU. */
+int conv_out_dims(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                  const int pad[3], const int dil[3], int64_t out_dims[5]);
+
+/* The plan conv_fwd would run for this problem on the current device
+ * (class, tile N, bytes per k-step row, pipeline stages, split-K factor,
+ * CTAs launched), and the workspace bytes it needs for split-K.  Any output
+ * pointer may be NULL.  If no workspace (or a smaller one) is given to
+ * conv_fwd, it runs the same plan without split-K.  num_sms <= 0 means "ask
+ * the current device" (needs a GPU); a positive value plans for that many
+ * SMs host-only.  Returns CONV_ERR_UNSUPPORTED when conv_fwd would. */
+int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                  const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
+                  int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
+                  size_t* workspace_bytes);
+
+/* Forward convolution:
+ *   out[n,od,oh,ow,k] = bf16_rn( scale_x * scale_w *
+ *       sum_{t,r,s,c} x[n, od*sd-pd+t*dd, oh*sh-ph+r*dh, ow*sw-pw+s*dw, c] * w[k,t,r,s,c] )
+ * with x = 0 outside the input (zero padding; cross-correlation, no flip),
+ * products of the exact bf16 / e4m3 input values accumulated in fp32.
+ *   x        device, NDHWC [N,D,H,W,C], bf16 or e4m3 per dtype
+ *   w        device, KTRSC [K,T,R,S,C], same dtype as x
+ *   scale_x, scale_w  device pointers to one fp32 each, or NULL for 1.0
+ *   out      device, NDHWC [N,Do,Ho,Wo,K] bf16; fully overwritten
+ *   workspace, workspace_bytes  device scratch for split-K partials (may be
+ *            NULL/0: split-K is then not used); size from conv_fwd_plan
+ * Coverage: C*elem_bytes % 16 == 0 for the implicit-GEMM classes; the
+ * point-output class needs T*R*S*C*elem_bytes % 4 == 0; strides <= 8 and
+ * pads <= 15 for the im2col class.  Anything else: CONV_ERR_UNSUPPORTED
+ * (there is no fallback path).  Device-side wait timeouts are reported by
+ * conv_get_device_status, not by this return value. */
+int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+             const int stride[3], const int pad[3], const int dil[3], int dtype,
+             const float* scale_x, const float* scale_w, void* out, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream);
+
+/* Layout pack: out[n,d,h,w,c] = in[n,c,d,h,w] (bit copy).
+ *   in   device, bf16 NCDHW, dims = {N, C, D, H, W}
+ *   out  device, bf16 NDHWC [N,D,H,W,C]
+ * Also the weight pack: a torch weight [K,C,T,R,S] passed as N=K, D=T,
+ * H=R, W=S gives the KTRSC weight conv_fwd takes. */
+int pack_ncdhw_bf16_to_ndhwc(const void* in, const int64_t dims[5], void* out,
+                             cudaStream_t stream);
+
+/* Bytes of device workspace pack_ncdhw_bf16_to_ndhwc_fp8 needs (16). */
+size_t pack_fp8_workspace_size(void);
+
+/* Layout pack with per-tensor fp8 quantisation:
+ *   amax  = max |in| over the whole tensor
+ *   scale = amax / 448 (fp32, IEEE round to nearest; 1.0 if amax == 0)
+ *   out[n,d,h,w,c] = e4m3_satfinite_rn( fp32(in[n,c,d,h,w]) / scale )
+ *   in         device, bf16 NCDHW, dims = {N, C, D, H, W}
+ *   out        device, e4m3 NDHWC
+ *   scale_out  device, one fp32: receives scale (the dequantisation
+ *              multiplier to pass to conv_fwd as scale_x or scale_w)
+ *   workspace  device, >= pack_fp8_workspace_size() bytes of scratch
+ * Non-finite inputs are not supported. */
+int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* out,
+                                 float* scale_out, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/* Reads and clears the current device's status word, after synchronising
+ * the device.  *device_status receives CONV_OK, or CONV_ERR_TIMEOUT if a
+ * kernel gave up on a bounded wait since the last call.  Returns
+ * CONV_ERR_CUDA if the synchronisation or copy failed. */
+int conv_get_device_status(int* device_status);
+
+/* Upper bound, in nanoseconds, on every spin-wait inside the kernels
+ * (default 2e9 = 2 s).  A kernel that waits longer records CONV_ERR_TIMEOUT
+ * in the device status word, drains its own copies in flight, frees its
+ * tensor memory and returns.  Host-only setter; applies to later launches. */
+void conv_set_wait_limit_ns(uint64_t ns);
+
+/* Static description of a status code. */
+const char* conv_status_string(int status);
+
+/* Human-readable detail of the last non-OK return on the calling thread
+ * (thread-local, overwritten by the next failure). */
+const char* conv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV3D_GB300_H */

@@ -1,0 +1,228 @@
+"""GPU parity of the bf16 forward convolution against the fp64 oracle, element
+by element, through the C ABI.  Shapes span several tiles with ragged M and N
+tails and cover every dispatch class (im2col implicit GEMM, temporal T x 1 x 1,
+point-output / pointwise GEMM by TMA and by row gather), with and without
+split-K, plus forced tile shapes, exact delta filters, the 2-D / 1-D wrappers
+and NaN-prefilled canary guards."""
+import contextlib
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import conv_workloads as cw
+import oracle
+from _gpu_util import as_f64, assert_close, bits16, oracle_conv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import implicit_gemm_convolution_conv3d_gb300 as p
+    p.load_library()
+    return p
+
+
+@contextlib.contextmanager
+def forced_tile(spec):
+    old = os.environ.get("CONV3D_FORCE_TILE")
+    os.environ["CONV3D_FORCE_TILE"] = spec
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("CONV3D_FORCE_TILE", None)
+        else:
+            os.environ["CONV3D_FORCE_TILE"] = old
+
+
+def _inputs(xs, ws, seed):
+    C = ws[4]
+    crs = ws[1] * ws[2] * ws[3] * C
+    x = cw.randn_bf16(xs, 100 + seed, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 200 + seed, 1.0 / np.sqrt(crs), "cuda")
+    return x, w
+
+
+def _run_and_check(pkg, xs, ws, stride, pad, dil, seed, split_k=True, what=""):
+    x, w = _inputs(xs, ws, seed)
+    y = pkg.conv_fwd(x, w, stride, pad, dil, split_k=split_k)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    st, pa, di = pkg._triple(stride), pkg._triple(pad), pkg._triple(dil)
+    ref = oracle_conv(x, w, st, pa, di)
+    assert_close(as_f64(y), ref, what or f"{xs} {ws} s{stride} p{pad} d{dil} split={split_k}")
+    return x, w, y
+
+
+GENERIC = [
+    ((1, 4, 8, 8, 16), (32, 3, 3, 3, 16), 1, 1, 1),
+    ((2, 5, 9, 11, 64), (48, 3, 3, 3, 64), 1, 1, 1),
+    ((1, 6, 10, 12, 24), (16, 3, 3, 3, 24), 1, 1, 1),
+    ((1, 3, 17, 13, 8), (32, 1, 3, 3, 8), 1, (0, 1, 1), 1),
+    ((2, 7, 9, 8, 136), (272, 3, 3, 3, 136), 1, 1, 1),
+    ((1, 9, 12, 10, 32), (40, 3, 3, 3, 32), 2, 1, 1),
+    ((1, 8, 11, 9, 16), (24, 3, 3, 3, 16), (1, 2, 3), (1, 0, 2), (2, 1, 1)),
+    ((3, 4, 6, 5, 16), (32, 2, 2, 2, 16), 2, 0, 1),
+    ((2, 5, 5, 5, 16), (32, 4, 4, 4, 16), 4, 0, 1),
+    ((1, 1, 16, 16, 64), (64, 1, 3, 3, 64), 1, (0, 1, 1), (1, 2, 2)),
+    ((1, 5, 20, 30, 256), (256, 3, 3, 3, 256), 1, 1, 1),
+]
+
+TEMPORAL = [
+    ((1, 5, 10, 20, 64), (32, 3, 1, 1, 64), 1, (1, 0, 0), 1),
+    ((2, 6, 8, 16, 16), (48, 3, 1, 1, 16), (2, 1, 1), (1, 0, 0), 1),
+    ((1, 7, 9, 9, 32), (64, 5, 1, 1, 32), 1, (2, 0, 0), 1),
+    ((1, 9, 4, 4, 128), (96, 3, 1, 1, 128), 1, (2, 0, 0), (2, 1, 1)),
+    ((1, 4, 3, 50, 16), (16, 1, 1, 1, 16), (2, 1, 1), 0, 1),
+    ((1, 6, 16, 90, 640), (640, 3, 1, 1, 640), 1, (1, 0, 0), 1),
+]
+
+POINT = [
+    ((300, 1, 14, 14, 3), (1280, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((129, 2, 4, 4, 8), (96, 2, 4, 4, 8), (2, 4, 4), 0, 1),
+    ((2, 3, 5, 7, 64), (80, 1, 1, 1, 64), 1, 0, 1),
+    ((50, 1, 16, 16, 3), (64, 1, 16, 16, 3), (1, 16, 16), 0, 1),
+    ((37, 1, 3, 3, 6), (40, 1, 3, 3, 6), (1, 3, 3), 0, 1),
+]
+
+
+def _ids(cases):
+    return [f"x{c[0]}-w{c[1]}-s{c[2]}-p{c[3]}-d{c[4]}".replace(" ", "") for c in cases]
+
+
+@pytest.mark.parametrize("case", GENERIC, ids=_ids(GENERIC))
+@pytest.mark.parametrize("split_k", [True, False])
+def test_generic_im2col(pkg, case, split_k):
+    xs, ws, st, pa, di = case
+    assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["class"] == "generic"
+    _run_and_check(pkg, xs, ws, st, pa, di, seed=GENERIC.index(case), split_k=split_k)
+
+
+@pytest.mark.parametrize("case", TEMPORAL, ids=_ids(TEMPORAL))
+@pytest.mark.parametrize("split_k", [True, False])
+def test_temporal(pkg, case, split_k):
+    xs, ws, st, pa, di = case
+    assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["class"] == "temporal"
+    _run_and_check(pkg, xs, ws, st, pa, di, seed=50 + TEMPORAL.index(case), split_k=split_k)
+
+
+@pytest.mark.parametrize("case", POINT, ids=_ids(POINT))
+@pytest.mark.parametrize("split_k", [True, False])
+def test_point_gemm(pkg, case, split_k):
+    xs, ws, st, pa, di = case
+    assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["class"] == "point_gemm"
+    _run_and_check(pkg, xs, ws, st, pa, di, seed=80 + POINT.index(case), split_k=split_k)
+
+
+@pytest.mark.parametrize("spec", ["32,32,2,1,1", "64,64,3,2,1", "128,128,4,1,1", "256,128,2,3,1",
+                                  "96,64,5,8,3", "160,128,3,2,2", "224,32,8,1,5"])
+def test_forced_tiles_generic(pkg, spec):
+    with forced_tile(spec):
+        _run_and_check(pkg, (2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1, seed=7,
+                       what=f"tile {spec}")
+
+
+@pytest.mark.parametrize("spec", ["64,128,3,1,1", "256,128,4,4,1", "128,64,6,2,4"])
+def test_forced_tiles_temporal_and_gemm(pkg, spec):
+    bk = int(spec.split(",")[1])
+    with forced_tile(spec):
+        _run_and_check(pkg, (1, 5, 10, 20, 64), (200, 3, 1, 1, 64), 1, (1, 0, 0), 1, seed=9,
+                       what=f"temporal tile {spec}")
+        _run_and_check(pkg, (150, 1, 4, 4, 16), (100, 1, 4, 4, 16), (1, 4, 4), 0, 1, seed=10,
+                       what=f"gemm tile {spec}")
+        if bk == 128:
+            _run_and_check(pkg, (300, 1, 14, 14, 3), (200, 1, 14, 14, 3), (1, 14, 14), 0, 1,
+                           seed=11, what=f"gather tile {spec}")
+
+
+def test_tiny_workload(pkg):
+    wl = cw.BY_NAME["tiny_conv3d_bf16"]
+    x, w = cw.make_inputs(wl, "cuda")
+    for split_k in (True, False):
+        y = pkg.conv_fwd(x, w, wl.stride, wl.pad, wl.dil, split_k=split_k)
+        torch.cuda.synchronize()
+        assert_close(as_f64(y), oracle_conv(x, w, wl.stride, wl.pad, wl.dil), wl.name)
+
+
+def test_split_k_is_deterministic(pkg):
+    x, w = _inputs((1, 4, 8, 8, 16), (32, 3, 3, 3, 16), 3)
+    a = pkg.conv_fwd(x, w, 1, 1, 1)
+    b = pkg.conv_fwd(x, w, 1, 1, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_delta_filter_is_exact_shift(pkg):
+    """One unit tap per output channel: every output is a single bf16 input
+    value, so the GPU result must equal the shifted copy bit for bit."""
+    C = 32
+    x = cw.randn_bf16((2, 5, 7, 9, C), 5, 1.0, "cuda")
+    for (T, R, S), tap, st, pa, di in [((3, 3, 3), (2, 0, 1), 1, 1, 1),
+                                       ((1, 3, 3), (0, 2, 2), (1, 2, 1), (0, 1, 1), (1, 1, 2)),
+                                       ((3, 1, 1), (0, 0, 0), (2, 1, 1), (1, 0, 0), (2, 1, 1))]:
+        w = torch.zeros((C, T, R, S, C), dtype=torch.bfloat16, device="cuda")
+        for k in range(C):
+            w[k, tap[0], tap[1], tap[2], k] = 1.0
+        y = pkg.conv_fwd(x, w, st, pa, di)
+        torch.cuda.synchronize()
+        ref = oracle_conv(x, w, pkg._triple(st), pkg._triple(pa), pkg._triple(di))
+        assert np.array_equal(as_f64(y), ref)
+
+
+def test_conv2d_and_conv1d_wrappers(pkg):
+    x2 = cw.randn_bf16((2, 13, 11, 32), 21, 1.0, "cuda")
+    w2 = cw.randn_bf16((48, 3, 3, 32), 22, 1.0 / np.sqrt(288), "cuda")
+    y2 = pkg.conv2d(x2, w2, stride=(2, 1), padding=1)
+    torch.cuda.synchronize()
+    ref = oracle_conv(x2.unsqueeze(1), w2.unsqueeze(1), (1, 2, 1), (0, 1, 1), (1, 1, 1))
+    assert_close(as_f64(y2), ref[:, 0], "conv2d")
+    x1 = cw.randn_bf16((3, 41, 16), 23, 1.0, "cuda")
+    w1 = cw.randn_bf16((24, 5, 16), 24, 1.0 / np.sqrt(80), "cuda")
+    y1 = pkg.conv1d(x1, w1, stride=1, padding=2, dilation=2)
+    torch.cuda.synchronize()
+    ref = oracle_conv(x1[:, None, None], w1[:, None, None], (1, 1, 1), (0, 0, 2), (1, 1, 2))
+    assert_close(as_f64(y1), ref[:, 0, 0], "conv1d")
+
+
+def test_output_fully_written_and_canaries_untouched(pkg):
+    """NaN-prefilled output inside a larger buffer: every output element is
+    overwritten, and 4 KB guard regions on both sides stay NaN."""
+    for xs, ws, st, pa in [((2, 5, 9, 11, 64), (48, 3, 3, 3, 64), 1, 1),
+                           ((1, 5, 10, 20, 64), (40, 3, 1, 1, 64), 1, (1, 0, 0)),
+                           ((37, 1, 3, 3, 6), (40, 1, 3, 3, 6), (1, 3, 3), 0)]:
+        x, w = _inputs(xs, ws, 31)
+        od = pkg.conv_out_dims(xs, ws, st, pa, 1)
+        n = int(np.prod(od))
+        guard = 2048   # bf16 elements = 4 KB
+        buf = torch.full((guard + n + guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        out = buf[guard:guard + n].view(od)
+        for split_k in (True, False):
+            buf[guard:guard + n] = float("nan")
+            pkg.conv_fwd(x, w, st, pa, 1, out=out, split_k=split_k)
+            torch.cuda.synchronize()
+            assert not torch.isnan(out).any()
+            assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[guard + n:]).all()
+        ref = oracle_conv(x, w, pkg._triple(st), pkg._triple(pa), (1, 1, 1))
+        assert_close(as_f64(out), ref, f"canary {xs}")
+
+
+def test_scales_apply_to_bf16(pkg):
+    x, w = _inputs((1, 4, 8, 8, 16), (32, 3, 3, 3, 16), 40)
+    sx = torch.tensor([0.5], device="cuda")
+    sw = torch.tensor([3.0], device="cuda")
+    y = pkg.conv_fwd(x, w, 1, 1, 1, scale_x=sx, scale_w=sw)
+    torch.cuda.synchronize()
+    assert_close(as_f64(y), oracle_conv(x, w, (1, 1, 1), (1, 1, 1), (1, 1, 1), 0.5, 3.0), "scaled")
+
+
+def test_unsupported_shape_raises(pkg):
+    x = torch.zeros((1, 4, 8, 8, 12), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 3, 3, 3, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkg.ConvError) as e:
+        pkg.conv_fwd(x, w, 1, 1, 1)
+    assert e.value.status == pkg.CONV_ERR_UNSUPPORTED

@@ -1,0 +1,120 @@
+"""GPU parity of the NCDHW -> NDHWC pack (bf16 copy and fp8-e4m3 quantisation)
+and of the fp8 forward convolution.
+
+The pack must equal the oracle bit for bit: every output byte and the scale's
+bits.  The codec is exercised exhaustively: every finite bf16 pattern below a
+chosen amax, at several amax values.  The fp8 conv is compared with the
+oracle's conv of the very bytes the GPU pack produced (the fp8-cast conv
+reference), times both scales."""
+import numpy as np
+import pytest
+import torch
+
+import conv_workloads as cw
+import oracle
+from _gpu_util import as_f64, assert_close, bits16, bytes8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import implicit_gemm_convolution_conv3d_gb300 as p
+    p.load_library()
+    return p
+
+
+PACK_SHAPES = [(1, 16, 2, 3, 8), (2, 64, 3, 5, 7), (1, 100, 1, 9, 13), (3, 24, 2, 8, 8),
+               (1, 1024, 2, 16, 9), (1, 8, 1, 1, 1), (2, 130, 3, 3, 11)]
+
+
+@pytest.mark.parametrize("shape", PACK_SHAPES)
+def test_pack_bf16_bit_exact(pkg, shape):
+    x = cw.randn_bf16(shape, 300, 1.0, "cuda")
+    y = pkg.pack_ncdhw_bf16_to_ndhwc(x)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(y), oracle.pack_ncdhw_to_ndhwc_bf16(bits16(x)))
+
+
+@pytest.mark.parametrize("shape", PACK_SHAPES)
+def test_pack_fp8_bit_exact(pkg, shape):
+    x = cw.randn_bf16(shape, 301, 3.0, "cuda")
+    q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)
+    torch.cuda.synchronize()
+    ref_q, ref_s = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(x))
+    assert np.float32(s.item()).tobytes() == np.float32(ref_s).tobytes()
+    assert np.array_equal(bytes8(q), ref_q)
+
+
+@pytest.mark.parametrize("amax", [448.0, 1.0, 3.0, 1e-3, 2.0 ** -7, 6.5e4, 1.7e38])
+def test_pack_fp8_codec_exhaustive(pkg, amax):
+    """All finite bf16 patterns with |v| <= amax (amax itself included) packed
+    as one tensor: the device cvt.rn.satfinite path against the oracle's
+    nearest-code search, byte for byte."""
+    pats = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    keep = np.isfinite(pats) & (np.abs(pats) <= np.float32(amax))
+    vals = pats[keep]
+    amax_bf16 = np.float32(torch.tensor(amax).to(torch.bfloat16).float().item())
+    vals = np.concatenate([vals, np.array([amax_bf16, -amax_bf16], dtype=np.float32)])
+    n = vals.size
+    C = 16
+    S = (n + C - 1) // C
+    flat = np.zeros(S * C, dtype=np.float32)
+    flat[:n] = vals
+    xb = torch.from_numpy(flat).to(torch.bfloat16).view(1, C, 1, 1, S).cuda()
+    q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb)
+    torch.cuda.synchronize()
+    ref_q, ref_s = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(xb))
+    assert np.float32(s.item()).tobytes() == np.float32(ref_s).tobytes()
+    assert np.array_equal(bytes8(q), ref_q)
+
+
+def test_pack_fp8_all_zero_tensor(pkg):
+    x = torch.zeros((1, 32, 2, 2, 2), dtype=torch.bfloat16, device="cuda")
+    q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)
+    torch.cuda.synchronize()
+    assert s.item() == 1.0 and not bytes8(q).any()
+
+
+def _fp8_operands(pkg, x_ncdhw, w_kctrs):
+    qx, sx = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x_ncdhw)
+    qw, sw = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(w_kctrs)
+    torch.cuda.synchronize()
+    # the pack is itself checked against the oracle before the conv is
+    ref_qx, ref_sx = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(x_ncdhw))
+    ref_qw, ref_sw = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(w_kctrs))
+    assert np.array_equal(bytes8(qx), ref_qx) and np.array_equal(bytes8(qw), ref_qw)
+    assert sx.item() == ref_sx and sw.item() == ref_sw
+    return qx, sx, qw, sw
+
+
+FP8_CASES = [
+    # (x NCDHW, w KCTRS, stride, pad, dil, class)
+    ((1, 64, 4, 9, 11), (96, 64, 1, 3, 3), 1, (0, 1, 1), 1, "generic"),
+    ((2, 32, 5, 7, 6), (48, 32, 3, 3, 3), 1, 1, 1, "generic"),
+    ((1, 144, 3, 10, 12), (272, 144, 1, 3, 3), (1, 2, 1), (0, 1, 1), 1, "generic"),
+    ((1, 16, 6, 8, 16), (32, 16, 3, 1, 1), 1, (1, 0, 0), 1, "temporal"),
+    ((1, 128, 5, 12, 20), (160, 128, 3, 1, 1), 1, (1, 0, 0), 1, "temporal"),
+    ((40, 3, 1, 16, 16), (64, 3, 1, 16, 16), (1, 16, 16), 0, 1, "point_gemm"),
+    ((70, 3, 1, 14, 14), (96, 3, 1, 14, 14), (1, 14, 14), 0, 1, "point_gemm"),
+    ((2, 64, 2, 3, 5), (40, 64, 1, 1, 1), 1, 0, 1, "point_gemm"),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[str(i) for i in range(len(FP8_CASES))])
+@pytest.mark.parametrize("split_k", [True, False])
+def test_fp8_conv(pkg, case, split_k):
+    xs, ws, st, pa, di, cls = case
+    crs = ws[1] * ws[2] * ws[3] * ws[4]
+    x = cw.randn_bf16(xs, 400 + FP8_CASES.index(case), 1.0, "cuda")
+    w = cw.randn_bf16(ws, 500 + FP8_CASES.index(case), 1.0 / np.sqrt(crs), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    assert pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), st, pa, di, 1)["class"] == cls
+    y = pkg.conv_fwd(qx, qw, st, pa, di, scale_x=sx, scale_w=sw, split_k=split_k)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    ref = oracle.conv3d(bytes8(qx), bytes8(qw), pkg._triple(st), pkg._triple(pa), pkg._triple(di),
+                        sx.item(), sw.item())
+    assert_close(as_f64(y), ref, f"fp8 {case} split={split_k}")
