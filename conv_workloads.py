@@ -74,7 +74,19 @@ WORKLOADS = [
              (1, 1, 1), (1, 0, 0)),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Reduced-depth variants of the large workloads for multi-pass profiler
+# captures: same channels, filters and padding, fewer frames; every input is
+# still larger than the 129 MB L2.
+PROFILE_WORKLOADS = [
+    Workload("video_conv3d_bf16_small", 5, (1, 3, 120, 120, 2048), (2048, 3, 3, 3, 2048),
+             (1, 1, 1), (1, 1, 1)),
+    Workload("fp8_conv3d_1x3x3_small", 6, (1, 1024, 16, 160, 90), (1024, 1024, 1, 3, 3),
+             (1, 1, 1), (0, 1, 1), dtype="fp8", x_layout="ncdhw", w_layout="kctrs"),
+    Workload("temporal_3x1x1_bf16_small", 7, (1, 16, 160, 90, 640), (640, 3, 1, 1, 640),
+             (1, 1, 1), (1, 0, 0)),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
 
 
 def randn_bf16(shape, seed: int, std: float = 1.0, device="cpu",
