@@ -78,6 +78,9 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp, vp,
                                  vp, ctypes.c_size_t, vp]
         lib.conv_fwd.restype = ctypes.c_int
+        lib.conv_fwd_noalloc.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
+                                         vp, vp, vp]
+        lib.conv_fwd_noalloc.restype = ctypes.c_int
         lib.pack_ncdhw_bf16_to_ndhwc.argtypes = [vp, i64p, vp, vp]
         lib.pack_ncdhw_bf16_to_ndhwc.restype = ctypes.c_int
         lib.pack_fp8_workspace_size.argtypes = []
@@ -214,6 +217,29 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
     return out
 
 
+def conv_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
+                     scale_x: Optional[torch.Tensor] = None,
+                     scale_w: Optional[torch.Tensor] = None, out: torch.Tensor = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """conv_fwd for callers that cannot allocate device memory: the caller
+    passes ``out`` (bf16, the output shape) and the library keeps any split-K
+    partials in its own static device scratch (see include/conv3d.h for the
+    size limit and the rule that overlapping calls race on that scratch)."""
+    lib = load_library()
+    if out is None:
+        raise ValueError("conv_fwd_noalloc writes into a caller-provided out tensor")
+    dtype = _dtype_code(x)
+    if _dtype_code(w) != dtype:
+        raise TypeError("x and w must have the same dtype")
+    _require_cuda(x, w, scale_x, scale_w, out)
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    rc = lib.conv_fwd_noalloc(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                              _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
+                              _ptr(scale_w), out.data_ptr(), _stream_handle(stream))
+    _check(rc, "conv_fwd_noalloc")
+    return out
+
+
 def pack_ncdhw_bf16_to_ndhwc(x: torch.Tensor, out: Optional[torch.Tensor] = None,
                              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """bf16 NCDHW [N,C,D,H,W] -> bf16 NDHWC [N,D,H,W,C] (a torch weight
@@ -282,7 +308,7 @@ def conv1d(x, w, stride=1, padding=0, dilation=1, scale_x=None, scale_w=None, **
 
 
 __all__ = [
-    "conv_fwd", "conv_fwd_plan", "conv_out_dims", "conv_get_device_status",
+    "conv_fwd", "conv_fwd_noalloc", "conv_fwd_plan", "conv_out_dims", "conv_get_device_status",
     "conv_set_wait_limit_ns", "pack_ncdhw_bf16_to_ndhwc", "pack_ncdhw_bf16_to_ndhwc_fp8",
     "conv3d", "conv2d", "conv1d", "load_library", "ConvError", "LIB_PATH",
 ]

@@ -467,6 +467,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof t_last_error, "%s", msg); }
+
 int* device_status_ptr() {
     DeviceInfo* d = nullptr;
     if (device_info(&d) != CONV_OK) return nullptr;

@@ -77,4 +77,7 @@ cudaError_t launch_pack(const void* in, long long N, long long C, long long S, v
 
 int* device_status_ptr();   // device address of the status word (current device)
 
+// Record a failure description for conv_last_error() on the calling thread.
+void set_last_error(const char* msg);
+
 }  // namespace c3d

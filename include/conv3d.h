@@ -131,6 +131,38 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
                                  float* scale_out, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+/* Size of the static device scratch conv_fwd_noalloc uses: 8 MiB. */
+#define CONV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* conv_fwd for callers that cannot allocate device memory.  The pages of the
+ * method have no counterpart of this entry point.
+ *
+ * conv_fwd takes its split-K scratch from the caller.  Some callers cannot
+ * provide one: code that must not call cudaMalloc at run time (engines that
+ * reserve all device memory up front, or latency-bound code that cannot
+ * afford cudaMalloc's implicit device synchronisation).  This entry point
+ * takes the same arguments as conv_fwd minus the workspace, runs the same
+ * plan, and keeps the split-K partials in a static device array of
+ * CONV_NOALLOC_SCRATCH_BYTES that is part of the library: every GPU that
+ * loads the library holds that array until the process exits.  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.  The caller still
+ * passes x, w, the scales and out.
+ *   - A problem whose split-K partials need more than
+ *     CONV_NOALLOC_SCRATCH_BYTES is rejected with CONV_ERR_INVALID
+ *     (conv_last_error says how many bytes it needed).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents.  Each call overwrites the partials it reads, so
+ *     nothing needs clearing; but calls whose kernels overlap on the GPU
+ *     (different streams, or threads racing on one device) race on the
+ *     array and give wrong results.  Serialise them. */
+int conv_fwd_noalloc(const void* x, const int64_t x_dims[5], const void* w,
+                     const int64_t w_dims[5], const int stride[3], const int pad[3],
+                     const int dil[3], int dtype, const float* scale_x, const float* scale_w,
+                     void* out, cudaStream_t stream);
+
 /* Reads and clears the current device's status word, after synchronising
  * the device.  *device_status receives CONV_OK, or CONV_ERR_TIMEOUT if a
  * kernel gave up on a bounded wait since the last call.  Returns
