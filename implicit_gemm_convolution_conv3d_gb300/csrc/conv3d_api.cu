@@ -186,17 +186,14 @@ int pick_bk(long long row_bytes) {
     return best;
 }
 
+// Tile columns: a tcgen05.mma of M=128 costs about the same issue time for
+// any N, so the fewest column tiles wins; among those, the narrowest tile
+// (least padding in the B loads and the epilogue).
 int pick_bn(long long K) {
-    int best = 256;
-    long long best_pad = ((K + 255) / 256) * 256;
-    for (int bn = 224; bn >= 32; bn -= 32) {
-        const long long pad = ((K + bn - 1) / bn) * bn;
-        if (pad < best_pad) {
-            best = bn;
-            best_pad = pad;
-        }
-    }
-    return best;
+    const long long tiles = (K + 255) / 256;
+    for (int bn = 32; bn <= 256; bn += 32)
+        if ((K + bn - 1) / bn == tiles) return bn;
+    return 256;
 }
 
 const TileEntry* lookup_tile(int fp8, int cls, const Geo& g, long long M) {

@@ -56,13 +56,18 @@ __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     return r;
 }
 
+// The bound is counted in SM clock cycles (clock64 is a cheap SM-local
+// register; the global nanosecond timer is far slower to read and would sit on
+// every producer / MMA / epilogue hand-off).  Two cycles per nanosecond is the
+// SM clock's upper end, so at any lower clock the wall-clock bound only grows.
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        int* status, unsigned long long limit_ns) {
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
+    const long long limit_cycles = static_cast<long long>(limit_ns > (1ull << 61) ? (1ull << 61) : limit_ns) * 2;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
+        if (clock64() - t0 > limit_cycles) {
             *abort_flag = 1u;
             atomicExch(status, kStatusTimeout);
             return false;
@@ -83,12 +88,6 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > kDrainNs) return;
     }
-}
-
-// Byte offset of (row, byte) inside a 128-byte-swizzled K-major tile whose
-// base is 1024-byte aligned: the 16-byte chunk index is XORed with row % 8.
-__device__ __forceinline__ uint32_t swz128(int row, int byte) {
-    return static_cast<uint32_t>(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -134,16 +133,22 @@ __device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&v)[32
 }
 
 // cp.async row-gather producer (AM_GEMM_GATHER): 128 threads copy the A and B
-// tiles of each k-step in VEC-byte pieces into the 128B-swizzled layout, zero
-// filling rows past M / K and columns past the reduction length.  A stage is
-// released LAG k-steps after its copies were issued.
+// tiles of each k-step (128-byte rows) in VEC-byte pieces into the
+// 128B-swizzled layout, zero filling rows past M / K and columns past the
+// reduction length.  Each thread owns one piece position and every RPP-th
+// row, so per piece it only steps a source pointer and a destination offset.
+// A stage is released LAG k-steps after its copies were issued.
 template <int VEC>
 __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0, uint32_t empty0,
                                 volatile uint32_t* abort_flag, int g) {
     constexpr int LAG = 2;
+    constexpr int PPR = 128 / VEC;                 // pieces per 128-byte row
+    constexpr int RPP = kGatherThreads / PPR;      // rows covered per pass
     const int total_units = p.m_tiles * p.n_tiles * p.splits;
-    const int ppr = p.BK / VEC;
-    const int pieces = (kBM + p.BN) * ppr;
+    const int row0 = g / PPR;
+    const int byte = (g % PPR) * VEC;
+    const int chunk = byte >> 4, lo = byte & 15;
+    const long long rb = p.g_row_bytes;
     int stage = 0;
     uint32_t phase = 0;
     long long it = 0;
@@ -152,8 +157,8 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
         const Unit t = decode_unit(u, p);
         const int ks0 = t.split * p.steps_per_split;
         const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
-        const long long m0 = static_cast<long long>(t.m_tile) * kBM;
-        const long long n0 = static_cast<long long>(t.n_tile) * p.BN;
+        const long long m0 = static_cast<long long>(t.m_tile) * kBM + row0;
+        const long long n0 = static_cast<long long>(t.n_tile) * p.BN + row0;
         for (int ks = ks0; ks < ks1; ++ks) {
             if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
                 ok_run = false;
@@ -161,27 +166,31 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
             }
             const uint32_t adst = tiles + stage * p.stage_bytes;
             const uint32_t bdst = adst + p.a_stage_bytes;
-            const long long kb = static_cast<long long>(ks) * p.BK;
-            for (int i = g; i < pieces; i += kGatherThreads) {
-                const int row = i / ppr;
-                const int byte = (i - row * ppr) * VEC;
-                const long long colb = kb + byte;
-                const unsigned char* src;
-                uint32_t dst;
-                bool ok;
-                if (row < kBM) {
-                    const long long m = m0 + row;
-                    ok = (m < p.M) && (colb < p.g_row_bytes);
-                    src = ok ? p.ga + m * p.g_row_bytes + colb : p.ga;
-                    dst = adst + swz128(row, byte);
-                } else {
-                    const int nb = row - kBM;
-                    const long long n = n0 + nb;
-                    ok = (n < p.K) && (colb < p.g_row_bytes);
-                    src = ok ? p.gb + n * p.g_row_bytes + colb : p.gb;
-                    dst = bdst + swz128(nb, byte);
+            const long long colb = static_cast<long long>(ks) * 128 + byte;
+            const bool col_ok = colb < rb;
+            {
+                const unsigned char* src = p.ga + m0 * rb + colb;
+                long long m = m0;
+#pragma unroll 4
+                for (int row = row0; row < kBM; row += RPP) {
+                    const bool ok = col_ok && m < p.M;
+                    const uint32_t dst = adst + row * 128 + (((chunk ^ (row & 7)) << 4) | lo);
+                    cp_async<VEC>(dst, ok ? src : p.ga, ok ? VEC : 0u);
+                    src += RPP * rb;
+                    m += RPP;
                 }
-                cp_async<VEC>(dst, src, ok ? VEC : 0u);
+            }
+            {
+                const unsigned char* src = p.gb + n0 * rb + colb;
+                long long n = n0;
+#pragma unroll 4
+                for (int row = row0; row < p.BN; row += RPP) {
+                    const bool ok = col_ok && n < p.K;
+                    const uint32_t dst = bdst + row * 128 + (((chunk ^ (row & 7)) << 4) | lo);
+                    cp_async<VEC>(dst, ok ? src : p.gb, ok ? VEC : 0u);
+                    src += RPP * rb;
+                    n += RPP;
+                }
             }
             cp_async_commit();
             if (it >= LAG) {
@@ -201,6 +210,57 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
     if (ok_run && !*abort_flag) {
         for (long long j = (it > LAG ? it - LAG : 0); j < it; ++j)
             mbar_arrive(full0 + 8 * static_cast<uint32_t>(j % p.stages));
+    }
+}
+
+// The MMA issuer (one thread): per k-step, wait for the stage, issue KMMA
+// tcgen05.mma over its 32-byte K slices into the tile's TMEM accumulator, and
+// commit the stage back to the producer; per tile, commit the accumulator to
+// the epilogue.  Shared-memory descriptors are built once and advanced by
+// adding encoded byte offsets (address field = bytes >> 4).
+template <int KMMA, int FP8>
+__device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uint32_t full0,
+                                           uint32_t empty0, uint32_t tfull0, uint32_t tempty0,
+                                           uint32_t tmem_base, uint32_t* misc,
+                                           volatile uint32_t* abort_flag) {
+    const int total_units = p.m_tiles * p.n_tiles * p.splits;
+    const uint64_t adesc0 = make_smem_desc(tiles, p.sbo, p.layout);
+    const uint64_t bdesc0 = make_smem_desc(tiles + p.a_stage_bytes, p.sbo, p.layout);
+    const uint32_t stage_step = p.stage_bytes >> 4;
+    int stage = 0, acc_iter = 0;
+    uint32_t phase = 0, consumed = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        const Unit t = decode_unit(u, p);
+        const int ks0 = t.split * p.steps_per_split;
+        const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+        const int acc = acc_iter & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
+        if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns)) return;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+        uint32_t accum = 0u;
+        for (int ks = ks0; ks < ks1; ++ks) {
+            if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) return;
+            tc_fence_after();
+            misc[3] = ++consumed;
+            const uint64_t off = static_cast<uint64_t>(stage) * stage_step;
+            const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
+#pragma unroll
+            for (int k = 0; k < KMMA; ++k) {
+                if (FP8)
+                    tc_mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                else
+                    tc_mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                accum = 1u;
+            }
+            tc_commit(empty0 + 8 * stage);
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        tc_commit(tfull0 + 8 * acc);
+        ++acc_iter;
     }
 }
 
@@ -291,6 +351,12 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 } else {
                     am0 = t.m_tile * kBM;
                 }
+                // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
+                // position is decoded once per unit and then stepped incrementally.
+                int tap = ks0 % p.taps;
+                int c0 = (ks0 / p.taps) * bke;
+                int fs = tap % p.S, fr = (tap / p.S) % p.R, ft = tap / (p.S * p.R);
+                int k0 = ks0 * bke;   // GEMM modes: first reduction element of the k-step
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
                         ok_run = false;
@@ -301,17 +367,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     const uint32_t adst = tiles + stage * p.stage_bytes;
                     const uint32_t bdst = adst + p.a_stage_bytes;
                     if (AMODE == AM_GEMM_TMA) {
-                        const int k0 = ks * bke;
                         tma_load_2d(adst, &tmA, fb, k0, am0);
                         tma_load_2d(bdst, &tmB, fb, k0, n0);
+                        k0 += bke;
                     } else {
-                        // reduction order: channel chunk (outer), tap (inner)
-                        const int chunk = ks / p.taps;
-                        const int tap = ks - chunk * p.taps;
-                        const int fs = tap % p.S;
-                        const int fr = (tap / p.S) % p.R;
-                        const int ft = tap / (p.S * p.R);
-                        const int c0 = chunk * bke;
                         if (AMODE == AM_IM2COL) {
                             tma_load_im2col_5d(adst, &tmA, fb, c0, aw, ah, ad, an,
                                                static_cast<uint16_t>(fs * p.dw),
@@ -321,6 +380,18 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                             tma_load_4d(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
                         }
                         tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
+                        ++tap;
+                        if (++fs == p.S) {
+                            fs = 0;
+                            if (++fr == p.R) {
+                                fr = 0;
+                                if (++ft == p.T) {
+                                    ft = 0;
+                                    tap = 0;
+                                    c0 += bke;
+                                }
+                            }
+                        }
                     }
                     misc[2] = ++issued;
                     if (++stage == p.stages) {
@@ -333,48 +404,15 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int stage = 0, acc_iter = 0;
-            uint32_t phase = 0, consumed = 0;
-            bool ok_run = true;
-            const int kmma = p.BK / 32;   // 32-byte K slices per stage
-            for (int u = blockIdx.x; u < total_units && ok_run; u += gridDim.x) {
-                const Unit t = decode_unit(u, p);
-                const int ks0 = t.split * p.steps_per_split;
-                const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
-                const int acc = acc_iter & 1;
-                const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
-                if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns))
-                    break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
-                for (int ks = ks0; ks < ks1; ++ks) {
-                    if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
-                        ok_run = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    misc[3] = ++consumed;
-                    const uint32_t a_s = tiles + stage * p.stage_bytes;
-                    const uint32_t b_s = a_s + p.a_stage_bytes;
-                    for (int k = 0; k < kmma; ++k) {
-                        const uint64_t adesc = make_smem_desc(a_s + 32 * k, p.sbo, p.layout);
-                        const uint64_t bdesc = make_smem_desc(b_s + 32 * k, p.sbo, p.layout);
-                        const uint32_t accum = (ks > ks0 || k > 0) ? 1u : 0u;
-                        if (FP8)
-                            tc_mma_f8(d_tmem, adesc, bdesc, p.idesc, accum);
-                        else
-                            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, accum);
-                    }
-                    tc_commit(empty0 + 8 * stage);
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok_run) break;
-                tc_commit(tfull0 + 8 * acc);
-                ++acc_iter;
-            }
+            if (p.BK == 128)
+                mma_issuer<4, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                   abort_flag);
+            else if (p.BK == 64)
+                mma_issuer<2, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                   abort_flag);
+            else
+                mma_issuer<1, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                   abort_flag);
         }
     } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------ epilogue
