@@ -169,6 +169,7 @@ struct Plan {
     int grid;
     size_t smem;
     uint32_t tmem_cols;
+    uint32_t epi_bytes;      // TMA-store epilogue staging (0: direct stores)
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
@@ -341,9 +342,14 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
         return CONV_ERR_UNSUPPORTED;
     }
 
+    // bf16 output leaves through TMA stores when its rows are 16-byte aligned;
+    // split-K partials are written directly
+    // (the short point-output GEMM tiles keep the lighter direct stores)
+    P->epi_bytes = (splits == 1 && g.K % 8 == 0 && P->cls != CONV_CLASS_POINT_GEMM)
+                       ? kEpiStageBytes : 0u;
     // pipeline depth from the shared-memory budget
     const size_t stage_bytes = static_cast<size_t>(kBM + BN) * BK;
-    const size_t fixed = 1024 + 256;
+    const size_t fixed = 1024 + 256 + P->epi_bytes;
     const int max_stages = static_cast<int>((smem_optin - fixed) / stage_bytes);
     if (stages == 0) stages = std::min(8, max_stages);
     const int min_stages = (P->amode == AM_GEMM_GATHER) ? 3 : 2;
@@ -384,6 +390,27 @@ int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuin
         return CONV_ERR_CUDA;
     }
     return CONV_OK;
+}
+
+// Output map for the TMA-store epilogue: [M, K] bf16 rows (or, for the
+// temporal class, [N*Do planes, H*W, K] so stores clip at each plane's edge),
+// 32x32 boxes with the 64-byte swizzle the epilogue writes.
+int build_out_map(const Geo& g, const Plan& P, void* out, CUtensorMap* tmC) {
+    std::memset(tmC, 0, sizeof *tmC);
+    if (!P.epi_bytes) return CONV_OK;
+    const cuuint64_t row = static_cast<cuuint64_t>(g.K) * 2;
+    if (P.amode == AM_TEMPORAL) {
+        const cuuint64_t hw = static_cast<cuuint64_t>(P.HW);
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.K), hw,
+                                    static_cast<cuuint64_t>(g.N * g.Do)};
+        const cuuint64_t str[2] = {row, row * hw};
+        const cuuint32_t box[3] = {32, 32, 1};
+        return encode_tiled(tmC, 0, 3, out, dims, str, box, 64);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(P.M)};
+    const cuuint64_t str[1] = {row};
+    const cuuint32_t box[2] = {32, 32};
+    return encode_tiled(tmC, 0, 2, out, dims, str, box, 64);
 }
 
 int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtensorMap* tmA,
@@ -564,8 +591,9 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if (P.splits > 1 && (workspace == nullptr || workspace_bytes < P.ws_bytes)) {
         if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, false, &P))) return rc;
     }
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     if ((rc = build_maps(g, P, x, w, &tmA, &tmB))) return rc;
+    if ((rc = build_out_map(g, P, out, &tmC))) return rc;
 
     KParams k;
     std::memset(&k, 0, sizeof k);
@@ -596,6 +624,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.layout = desc_layout_for(P.BK);
     k.sbo = static_cast<uint32_t>(8 * P.BK);
     k.tmem_cols = P.tmem_cols;
+    k.epi_bytes = P.epi_bytes;
     k.ga = static_cast<const unsigned char*>(x);
     k.gb = static_cast<const unsigned char*>(w);
     k.g_row_bytes = P.g_row_bytes;
@@ -609,11 +638,11 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
                      "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
-                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u\n",
+                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u\n",
                      P.cls, P.amode, P.fp8, P.M, k.K, P.BN, P.BK, P.stages, P.splits, P.k_steps,
-                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols);
+                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes);
     }
-    cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, k, P.grid, P.smem, stream);
+    cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
         e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, dev->num_sms,

@@ -90,6 +90,13 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -137,11 +144,11 @@ __device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&v)[32
 // 128B-swizzled layout, zero filling rows past M / K and columns past the
 // reduction length.  Each thread owns one piece position and every RPP-th
 // row, so per piece it only steps a source pointer and a destination offset.
-// A stage is released LAG k-steps after its copies were issued.
-template <int VEC>
+// A stage is released LAG k-steps after its copies were issued, so LAG
+// k-steps of copies stay in flight per thread.
+template <int VEC, int LAG>
 __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0, uint32_t empty0,
                                 volatile uint32_t* abort_flag, int g) {
-    constexpr int LAG = 2;
     constexpr int PPR = 128 / VEC;                 // pieces per 128-byte row
     constexpr int RPP = kGatherThreads / PPR;      // rows covered per pass
     const int total_units = p.m_tiles * p.n_tiles * p.splits;
@@ -267,19 +274,22 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
 template <int AMODE, int FP8>
 __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     conv_igemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const KParams p) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* base_ptr = smem_raw + (base - raw);
     const uint32_t tiles = base;
     const uint32_t ring_bytes = static_cast<uint32_t>(p.stages) * p.stage_bytes;
-    const uint32_t full0 = base + ring_bytes;
+    const uint32_t epi0 = base + ring_bytes;   // epilogue staging (1024-aligned)
+    const uint32_t full0 = epi0 + p.epi_bytes;
     const uint32_t empty0 = full0 + 8u * p.stages;
     const uint32_t tfull0 = empty0 + 8u * p.stages;
     const uint32_t tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + ring_bytes + 16u * p.stages + 40u);
+    uint32_t* misc =
+        reinterpret_cast<uint32_t*>(base_ptr + ring_bytes + p.epi_bytes + 16u * p.stages + 40u);
     // misc[0] TMEM base, misc[1] abort flag, misc[2] k-steps issued, misc[3] k-steps consumed
     volatile uint32_t* abort_flag = misc + 1;
 
@@ -308,6 +318,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
         }
+        if (p.epi_bytes) prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), p.tmem_cols);
@@ -424,7 +435,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         const bool vec_out = (p.K % 8) == 0;
         const bool vec_ws = (p.K % 4) == 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        int acc_iter = 0;
+        int acc_iter = 0, epi_iter = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
             const Unit t = decode_unit(u, p);
             const int acc = acc_iter & 1;
@@ -444,6 +455,58 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             }
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(acc * p.BN);
+            if (p.epi_bytes) {
+                // TMA-store epilogue: the warp's 32 rows leave in 32x32 chunks
+                // staged in shared memory (64-byte swizzle, two buffers).
+                int row0, plane = 0;
+                bool any;
+                if (AMODE == AM_TEMPORAL) {
+                    plane = t.m_tile / p.hw_tiles;
+                    row0 = (t.m_tile - plane * p.hw_tiles) * kBM + q * 32;
+                    any = row0 < p.HW;
+                } else {
+                    row0 = t.m_tile * kBM + q * 32;
+                    any = row0 < p.M;
+                }
+                if (any) {
+                    const uint32_t bufs = epi0 + static_cast<uint32_t>(warp - 2) * 2u * kEpiChunkBytes;
+                    for (int j = 0; j < p.BN / 32; ++j) {
+                        const int n0 = t.n_tile * p.BN + 32 * j;
+                        if (n0 >= p.K) break;
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tb + 32 * j, v);
+                        tmem_ld_wait();
+                        const uint32_t buf = bufs + static_cast<uint32_t>(epi_iter & 1) * kEpiChunkBytes;
+                        ++epi_iter;
+                        if (lane == 0) bulk_wait_read<1>();   // this buffer's last store has read it
+                        __syncwarp();
+                        const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 64u;
+                        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * c + 0]) * scale, __uint_as_float(v[8 * c + 1]) * scale);
+                            const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * c + 2]) * scale, __uint_as_float(v[8 * c + 3]) * scale);
+                            const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * c + 4]) * scale, __uint_as_float(v[8 * c + 5]) * scale);
+                            const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * c + 6]) * scale, __uint_as_float(v[8 * c + 7]) * scale);
+                            st_shared_v4(rowaddr + ((static_cast<uint32_t>(c) ^ sw) << 4), w0, w1, w2, w3);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (AMODE == AM_TEMPORAL)
+                                tma_store_3d(&tmC, buf, n0, row0, plane);
+                            else
+                                tma_store_2d(&tmC, buf, n0, row0);
+                            bulk_commit();
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                ++acc_iter;
+                continue;
+            }
             for (int j = 0; j < p.BN / 32; ++j) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tb + 32 * j, v);
@@ -464,13 +527,14 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
             ++acc_iter;
         }
+        if (p.epi_bytes && lane == 0) bulk_wait_all();   // stores done before the CTA leaves
     } else if (kGather) {
         // ------------------------------------------------------ row gather
         const int g = threadIdx.x - (2 + kEpiWarps) * 32;
         if (p.g_row_bytes % 8 == 0)
-            gather_producer<8>(p, tiles, full0, empty0, abort_flag, g);
+            gather_producer<8, 2>(p, tiles, full0, empty0, abort_flag, g);
         else
-            gather_producer<4>(p, tiles, full0, empty0, abort_flag, g);
+            gather_producer<4, 2>(p, tiles, full0, empty0, abort_flag, g);
     }
 
     __syncthreads();
@@ -496,32 +560,33 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
 }
 
 template <int AM, int F8>
-cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const KParams& p, int grid,
-                       size_t smem, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
+                       const KParams& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = conv_igemm_kernel<AM, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int threads = (AM == AM_GEMM_GATHER) ? 320 : 192;
-    kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, p);
+    kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, *tmC, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                         const KParams& p, int grid, size_t smem, cudaStream_t stream) {
+                         const CUtensorMap* tmC, const KParams& p, int grid, size_t smem,
+                         cudaStream_t stream) {
     switch (amode * 2 + (fp8 ? 1 : 0)) {
-        case AM_IM2COL * 2 + 0: return launch_one<AM_IM2COL, 0>(tmA, tmB, p, grid, smem, stream);
-        case AM_IM2COL * 2 + 1: return launch_one<AM_IM2COL, 1>(tmA, tmB, p, grid, smem, stream);
-        case AM_TEMPORAL * 2 + 0: return launch_one<AM_TEMPORAL, 0>(tmA, tmB, p, grid, smem, stream);
-        case AM_TEMPORAL * 2 + 1: return launch_one<AM_TEMPORAL, 1>(tmA, tmB, p, grid, smem, stream);
-        case AM_GEMM_TMA * 2 + 0: return launch_one<AM_GEMM_TMA, 0>(tmA, tmB, p, grid, smem, stream);
-        case AM_GEMM_TMA * 2 + 1: return launch_one<AM_GEMM_TMA, 1>(tmA, tmB, p, grid, smem, stream);
+        case AM_IM2COL * 2 + 0: return launch_one<AM_IM2COL, 0>(tmA, tmB, tmC, p, grid, smem, stream);
+        case AM_IM2COL * 2 + 1: return launch_one<AM_IM2COL, 1>(tmA, tmB, tmC, p, grid, smem, stream);
+        case AM_TEMPORAL * 2 + 0: return launch_one<AM_TEMPORAL, 0>(tmA, tmB, tmC, p, grid, smem, stream);
+        case AM_TEMPORAL * 2 + 1: return launch_one<AM_TEMPORAL, 1>(tmA, tmB, tmC, p, grid, smem, stream);
+        case AM_GEMM_TMA * 2 + 0: return launch_one<AM_GEMM_TMA, 0>(tmA, tmB, tmC, p, grid, smem, stream);
+        case AM_GEMM_TMA * 2 + 1: return launch_one<AM_GEMM_TMA, 1>(tmA, tmB, tmC, p, grid, smem, stream);
         case AM_GEMM_GATHER * 2 + 0:
-            return launch_one<AM_GEMM_GATHER, 0>(tmA, tmB, p, grid, smem, stream);
+            return launch_one<AM_GEMM_GATHER, 0>(tmA, tmB, tmC, p, grid, smem, stream);
         case AM_GEMM_GATHER * 2 + 1:
-            return launch_one<AM_GEMM_GATHER, 1>(tmA, tmB, p, grid, smem, stream);
+            return launch_one<AM_GEMM_GATHER, 1>(tmA, tmB, tmC, p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }

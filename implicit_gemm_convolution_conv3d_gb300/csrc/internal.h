@@ -20,6 +20,8 @@ enum AMode : int {
 constexpr int kBM = 128;               // rows of a tile (tcgen05 M, one CTA)
 constexpr int kEpiWarps = 4;           // warps reading TMEM in the epilogue
 constexpr int kGatherThreads = 128;    // producer threads of AM_GEMM_GATHER
+constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;              // one warp's 32x32 bf16 chunk
+constexpr uint32_t kEpiStageBytes = kEpiWarps * 2 * kEpiChunkBytes;   // double-buffered
 
 struct KParams {
     // convolution geometry (A coordinates)
@@ -46,6 +48,7 @@ struct KParams {
     uint32_t layout;    // smem descriptor swizzle code
     uint32_t sbo;       // smem descriptor stride byte offset (8 rows)
     uint32_t tmem_cols; // allocated TMEM columns (power of two >= 2*BN)
+    uint32_t epi_bytes; // shared staging of the TMA-store epilogue (0: direct stores)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;
     const unsigned char* gb;
@@ -61,7 +64,8 @@ struct KParams {
 
 // Launch the implicit-GEMM kernel (AMODE x dtype) on grid/smem from the plan.
 cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                         const KParams& p, int grid, size_t smem, cudaStream_t stream);
+                         const CUtensorMap* tmC, const KParams& p, int grid, size_t smem,
+                         cudaStream_t stream);
 
 // Deterministic split-K reduction: out = bf16(scale * sum_s ws[s]) in split order.
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
