@@ -671,7 +671,8 @@ int pack_ncdhw_bf16_to_ndhwc(const void* in, const int64_t dims[5], void* out,
     int rc = device_info(&dev);
     if (rc) return rc;
     const long long S = dims[2] * dims[3] * dims[4];
-    cudaError_t e = launch_pack(in, dims[0], dims[1], S, out, 0, nullptr, nullptr, stream);
+    cudaError_t e = launch_pack(in, dims[0], dims[1], S, out, 0, nullptr, nullptr, dev->num_sms,
+                                stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return CONV_OK;
 }
@@ -709,7 +710,7 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     e = launch_amax_bf16(in, n, amax, dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-    e = launch_pack(in, dims[0], dims[1], S, out, 1, amax, scale_out, stream);
+    e = launch_pack(in, dims[0], dims[1], S, out, 1, amax, scale_out, dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return CONV_OK;
 }

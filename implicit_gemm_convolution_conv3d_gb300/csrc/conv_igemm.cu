@@ -139,6 +139,20 @@ __device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&v)[32
     }
 }
 
+// L2 prefetch of rows [r0, r1) of a row-major matrix with row_bytes per row;
+// the byte range is trimmed inward to 16-byte boundaries (the allocation
+// starts 16-byte aligned), so it never leaves the matrix.
+__device__ __forceinline__ void prefetch_rows(const unsigned char* base, long long r0, long long r1,
+                                              long long row_bytes) {
+    if (r1 <= r0) return;
+    const long long lo = ((r0 * row_bytes) + 15) & ~15ll;
+    const long long hi = (r1 * row_bytes) & ~15ll;
+    for (long long a = lo; a < hi; a += 65536) {
+        const long long n = min(65536ll, hi - a);
+        prefetch_l2_bulk(base + a, static_cast<uint32_t>(n));
+    }
+}
+
 // cp.async row-gather producer (AM_GEMM_GATHER): 128 threads copy the A and B
 // tiles of each k-step (128-byte rows) in VEC-byte pieces into the
 // 128B-swizzled layout, zero filling rows past M / K and columns past the
@@ -330,6 +344,22 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     const uint32_t tmem_base = misc[0];
 
     if (warp == 0) {
+        if (kGather && lane == 0) {
+            // row-gather GEMM: warm L2 with the rows this CTA gathers, so the
+            // cp.async pieces hit L2 instead of DRAM; each A row block is
+            // prefetched once (by its first column tile), each B block by the
+            // first row tile
+            for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+                const Unit t = decode_unit(u, p);
+                const long long m0 = static_cast<long long>(t.m_tile) * kBM;
+                const long long n0 = static_cast<long long>(t.n_tile) * p.BN;
+                if (t.n_tile == 0 && t.split == 0)
+                    prefetch_rows(p.ga, m0, min(m0 + kBM, p.M), p.g_row_bytes);
+                if (t.m_tile == 0 && t.split == 0)
+                    prefetch_rows(p.gb, n0, min(n0 + p.BN, static_cast<long long>(p.K)),
+                                  p.g_row_bytes);
+            }
+        }
         // ------------------------------------------------------ TMA producer
         if (!kGather && lane == 0) {
             int stage = 0;

@@ -76,7 +76,7 @@ cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int s
 cudaError_t launch_amax_bf16(const void* in, long long n, unsigned int* amax_bits, int num_sms,
                              cudaStream_t stream);
 cudaError_t launch_pack(const void* in, long long N, long long C, long long S, void* out,
-                        int fp8, const unsigned int* amax_bits, float* scale_out,
+                        int fp8, const unsigned int* amax_bits, float* scale_out, int num_sms,
                         cudaStream_t stream);
 
 int* device_status_ptr();   // device address of the status word (current device)

@@ -116,6 +116,11 @@ __device__ __forceinline__ void bulk_wait_read() {
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// bulk prefetch of [src, src+bytes) into L2 (src and bytes multiples of 16)
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // size in {4, 8, 16}; src_bytes in {0, size}: 0 zero-fills the destination.
 template <int SIZE>

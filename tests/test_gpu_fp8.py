@@ -26,8 +26,11 @@ def pkg():
     return p
 
 
+# C % 16 == 0 and D*H*W % 8 == 0 take the register-blocked tile kernel (with
+# partial 64-channel / 64-position tiles here); the others the generic one.
 PACK_SHAPES = [(1, 16, 2, 3, 8), (2, 64, 3, 5, 7), (1, 100, 1, 9, 13), (3, 24, 2, 8, 8),
-               (1, 1024, 2, 16, 9), (1, 8, 1, 1, 1), (2, 130, 3, 3, 11)]
+               (1, 1024, 2, 16, 9), (1, 8, 1, 1, 1), (2, 130, 3, 3, 11), (2, 80, 3, 5, 8),
+               (1, 48, 1, 1, 24), (3, 176, 2, 7, 4)]
 
 
 @pytest.mark.parametrize("shape", PACK_SHAPES)
