@@ -170,6 +170,7 @@ struct Plan {
     size_t smem;
     uint32_t tmem_cols;
     uint32_t epi_bytes;      // TMA-store epilogue staging (0: direct stores)
+    int pair;                // CTA-pair kernel: 256-row units on clusters of two CTAs
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
@@ -312,13 +313,16 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
         const long long chunks = (g.C * elt + BK - 1) / BK;
         P->k_steps = static_cast<int>(chunks * P->taps);
     }
-    if (P->cls == CONV_CLASS_TEMPORAL) {
-        P->HW = static_cast<int>(g.H * g.W);
-        P->hw_tiles = (P->HW + kBM - 1) / kBM;
-        P->m_tiles = static_cast<int>(g.N * g.Do * P->hw_tiles);
-    } else {
-        P->m_tiles = static_cast<int>((P->M + kBM - 1) / kBM);
-    }
+    auto set_m_tiles = [&](int tile_m) {
+        if (P->cls == CONV_CLASS_TEMPORAL) {
+            P->HW = static_cast<int>(g.H * g.W);
+            P->hw_tiles = (P->HW + tile_m - 1) / tile_m;
+            P->m_tiles = static_cast<int>(g.N * g.Do * P->hw_tiles);
+        } else {
+            P->m_tiles = static_cast<int>((P->M + tile_m - 1) / tile_m);
+        }
+    };
+    set_m_tiles(kBM);
     P->n_tiles = static_cast<int>((g.K + BN - 1) / BN);
 
     // split-K when the output tiles leave most SMs idle
@@ -342,13 +346,30 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
         return CONV_ERR_UNSUPPORTED;
     }
 
+    // CTA pairs (tcgen05 cta_group::2): a cluster of two CTAs computes a
+    // 256-row unit, each SM holding half of the B tile, which halves the B
+    // bytes each SM stores and feeds to the tensor core.  Used when the
+    // problem has whole waves of such units; CONV3D_PAIR=0/1 overrides.
+    P->pair = 0;
+    if (P->amode != AM_GEMM_GATHER && splits == 1 && BN >= 64 && num_sms % 2 == 0) {
+        const long long pm = P->cls == CONV_CLASS_TEMPORAL
+                                 ? g.N * g.Do * ((g.H * g.W + 2 * kBM - 1) / (2 * kBM))
+                                 : (P->M + 2 * kBM - 1) / (2 * kBM);
+        int want = pm * P->n_tiles >= 2LL * num_sms ? 1 : 0;
+        if (const char* e = std::getenv("CONV3D_PAIR")) want = (e[0] == '1') ? 1 : 0;
+        if (want) {
+            P->pair = 1;
+            set_m_tiles(2 * kBM);
+        }
+    }
+
     // bf16 output leaves through TMA stores when its rows are 16-byte aligned;
     // split-K partials are written directly
     // (the short point-output GEMM tiles keep the lighter direct stores)
     P->epi_bytes = (splits == 1 && g.K % 8 == 0 && P->cls != CONV_CLASS_POINT_GEMM)
                        ? kEpiStageBytes : 0u;
-    // pipeline depth from the shared-memory budget
-    const size_t stage_bytes = static_cast<size_t>(kBM + BN) * BK;
+    // pipeline depth from the shared-memory budget (a pair CTA holds half of B)
+    const size_t stage_bytes = static_cast<size_t>(kBM + (BN >> P->pair)) * BK;
     const size_t fixed = 1024 + 256 + P->epi_bytes;
     const int max_stages = static_cast<int>((smem_optin - fixed) / stage_bytes);
     if (stages == 0) stages = std::min(8, max_stages);
@@ -365,8 +386,11 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
     // a CTA holding all 512 TMEM columns must be alone on its SM
     if (cols > 256 && P->smem < static_cast<size_t>(smem_optin) / 2 + 1024)
         P->smem = static_cast<size_t>(smem_optin) / 2 + 1024;
-    const long long units = tiles * splits;
-    P->grid = static_cast<int>(std::min<long long>(units, num_sms));
+    const long long units = static_cast<long long>(P->m_tiles) * P->n_tiles * splits;
+    if (P->pair)
+        P->grid = 2 * static_cast<int>(std::min<long long>(units, num_sms / 2));
+    else
+        P->grid = static_cast<int>(std::min<long long>(units, num_sms));
     return CONV_OK;
 }
 
@@ -430,7 +454,7 @@ int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtens
         int rc = encode_tiled(tmA, P.fp8, 2, x, adims, astr, abox, P.BK);
         if (rc) return rc;
         const cuuint64_t bdims[2] = {rg, static_cast<cuuint64_t>(g.K)};
-        const cuuint32_t bbox[2] = {bke, static_cast<cuuint32_t>(P.BN)};
+        const cuuint32_t bbox[2] = {bke, static_cast<cuuint32_t>(P.BN >> P.pair)};
         return encode_tiled(tmB, P.fp8, 2, w, bdims, astr, bbox, P.BK);
     }
     // weight: [K, T*R*S, C] -> dims {C, TRS, K}, box {bke, 1, BN}
@@ -439,7 +463,7 @@ int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtens
         const cuuint64_t bdims[3] = {static_cast<cuuint64_t>(g.C), trs, static_cast<cuuint64_t>(g.K)};
         const cuuint64_t bstr[2] = {static_cast<cuuint64_t>(g.C) * elt,
                                     static_cast<cuuint64_t>(g.C) * elt * trs};
-        const cuuint32_t bbox[3] = {bke, 1, static_cast<cuuint32_t>(P.BN)};
+        const cuuint32_t bbox[3] = {bke, 1, static_cast<cuuint32_t>(P.BN >> P.pair)};
         int rc = encode_tiled(tmB, P.fp8, 3, w, bdims, bstr, bbox, P.BK);
         if (rc) return rc;
     }
@@ -478,12 +502,12 @@ int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtens
     return CONV_OK;
 }
 
-uint32_t make_idesc(int fp8, int bn) {
+uint32_t make_idesc(int fp8, int bn, int m) {
     uint32_t d = 0;
     d |= 1u << 4;                       // D format: f32
     if (!fp8) d |= (1u << 7) | (1u << 10);   // A, B format: bf16 (kind::f16); e4m3 = 0 (kind::f8f6f4)
     d |= static_cast<uint32_t>(bn >> 3) << 17;   // N >> 3
-    d |= static_cast<uint32_t>(kBM >> 4) << 24;  // M >> 4
+    d |= static_cast<uint32_t>(m >> 4) << 24;    // M >> 4
     return d;
 }
 
@@ -618,13 +642,14 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.BK = P.BK;
     k.stages = P.stages;
     k.a_stage_bytes = static_cast<uint32_t>(kBM * P.BK);
-    k.b_stage_bytes = static_cast<uint32_t>(P.BN * P.BK);
+    k.b_stage_bytes = static_cast<uint32_t>((P.BN >> P.pair) * P.BK);
     k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
-    k.idesc = make_idesc(P.fp8, P.BN);
+    k.idesc = make_idesc(P.fp8, P.BN, kBM << P.pair);
     k.layout = desc_layout_for(P.BK);
     k.sbo = static_cast<uint32_t>(8 * P.BK);
     k.tmem_cols = P.tmem_cols;
     k.epi_bytes = P.epi_bytes;
+    k.pair = P.pair;
     k.ga = static_cast<const unsigned char*>(x);
     k.gb = static_cast<const unsigned char*>(w);
     k.g_row_bytes = P.g_row_bytes;
@@ -638,9 +663,9 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
                      "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
-                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u\n",
+                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d\n",
                      P.cls, P.amode, P.fp8, P.M, k.K, P.BN, P.BK, P.stages, P.splits, P.k_steps,
-                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes);
+                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair);
     }
     cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");

@@ -239,7 +239,7 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
 // commit the stage back to the producer; per tile, commit the accumulator to
 // the epilogue.  Shared-memory descriptors are built once and advanced by
 // adding encoded byte offsets (address field = bytes >> 4).
-template <int KMMA, int FP8>
+template <int KMMA, int FP8, int PAIR>
 __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uint32_t full0,
                                            uint32_t empty0, uint32_t tfull0, uint32_t tempty0,
                                            uint32_t tmem_base, uint32_t* misc,
@@ -250,7 +250,7 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
     const uint32_t stage_step = p.stage_bytes >> 4;
     int stage = 0, acc_iter = 0;
     uint32_t phase = 0, consumed = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    for (int u = static_cast<int>(blockIdx.x) >> PAIR; u < total_units; u += gridDim.x >> PAIR) {
         const Unit t = decode_unit(u, p);
         const int ks0 = t.split * p.steps_per_split;
         const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
@@ -268,24 +268,42 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
             const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
 #pragma unroll
             for (int k = 0; k < KMMA; ++k) {
-                if (FP8)
-                    tc_mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                else
-                    tc_mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                if (PAIR) {
+                    if (FP8)
+                        tc_mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                    else
+                        tc_mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                } else {
+                    if (FP8)
+                        tc_mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                    else
+                        tc_mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                }
                 accum = 1u;
             }
-            tc_commit(empty0 + 8 * stage);
+            // the stage is free in both CTAs once these MMAs have read it
+            if (PAIR)
+                tc_commit_pair(empty0 + 8 * stage, 3);
+            else
+                tc_commit(empty0 + 8 * stage);
             if (++stage == p.stages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        tc_commit(tfull0 + 8 * acc);
+        if (PAIR)
+            tc_commit_pair(tfull0 + 8 * acc, 3);
+        else
+            tc_commit(tfull0 + 8 * acc);
         ++acc_iter;
     }
 }
 
-template <int AMODE, int FP8>
+// PAIR = 1: CTA-pair variant (a cluster of two CTAs on two SMs computes a
+// 256-row tile with tcgen05.mma.cta_group::2; each CTA loads its own 128 A
+// rows and half of the tile's B rows, the pair's leader issues the MMAs, and
+// each CTA's epilogue drains its own TMEM half).
+template <int AMODE, int FP8, int PAIR>
 __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     conv_igemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -310,6 +328,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total_units = p.m_tiles * p.n_tiles * p.splits;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA within the pair
+    const int unit0 = static_cast<int>(blockIdx.x) >> PAIR;
+    const int ustride = static_cast<int>(gridDim.x) >> PAIR;
+    constexpr int kTileM = kBM << PAIR;                     // rows of a work unit
     constexpr bool kGather = (AMODE == AM_GEMM_GATHER);
     constexpr int kElt = FP8 ? 1 : 2;
     const int bke = p.BK / kElt;   // elements of one row per k-step
@@ -321,7 +343,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, kEpiWarps);
+            mbar_init(tempty0 + 8 * a, kEpiWarps * (1 + PAIR));
         }
         mbar_init(drain_bar, 1);
         misc[1] = 0u;
@@ -335,11 +357,17 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         if (p.epi_bytes) prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(misc), p.tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(misc), p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(misc), p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
 
@@ -365,14 +393,15 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok_run = true;
-            for (int u = blockIdx.x; u < total_units && ok_run; u += gridDim.x) {
+            for (int u = unit0; u < total_units && ok_run; u += ustride) {
                 const Unit t = decode_unit(u, p);
                 const int ks0 = t.split * p.steps_per_split;
                 const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
-                const int n0 = t.n_tile * p.BN;
+                // this CTA's B rows: all BN columns, or its half of them in a pair
+                const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (p.BN >> PAIR);
                 int aw = 0, ah = 0, ad = 0, an = 0, am0 = 0;
                 if (AMODE == AM_IM2COL) {
-                    const long long m0 = static_cast<long long>(t.m_tile) * kBM;
+                    const long long m0 = static_cast<long long>(t.m_tile) * kTileM + kBM * rank;
                     const int ow = static_cast<int>(m0 % p.Wo);
                     const long long q1 = m0 / p.Wo;
                     const int oh = static_cast<int>(q1 % p.Ho);
@@ -388,9 +417,9 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     const int od = plane % p.Do;
                     an = plane / p.Do;
                     ad = od * p.sd - p.pd;
-                    ah = hwb * kBM;   // first H*W row of the tile
+                    ah = hwb * kTileM + kBM * static_cast<int>(rank);   // first H*W row
                 } else {
-                    am0 = t.m_tile * kBM;
+                    am0 = t.m_tile * kTileM + kBM * static_cast<int>(rank);
                 }
                 // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
                 // position is decoded once per unit and then stepped incrementally.
@@ -403,24 +432,42 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                         ok_run = false;
                         break;
                     }
-                    const uint32_t fb = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(fb, p.stage_bytes);
+                    uint32_t fb = full0 + 8 * stage;
+                    if (PAIR) {
+                        // the leader's full barrier counts both CTAs' bytes
+                        if (rank == 0) mbar_arrive_expect_tx(fb, 2u * p.stage_bytes);
+                        fb = mapa_shared(fb, 0);
+                    } else {
+                        mbar_arrive_expect_tx(fb, p.stage_bytes);
+                    }
                     const uint32_t adst = tiles + stage * p.stage_bytes;
                     const uint32_t bdst = adst + p.a_stage_bytes;
                     if (AMODE == AM_GEMM_TMA) {
-                        tma_load_2d(adst, &tmA, fb, k0, am0);
-                        tma_load_2d(bdst, &tmB, fb, k0, n0);
+                        if (PAIR) {
+                            tma_load_2d_pair(adst, &tmA, fb, k0, am0);
+                            tma_load_2d_pair(bdst, &tmB, fb, k0, n0);
+                        } else {
+                            tma_load_2d(adst, &tmA, fb, k0, am0);
+                            tma_load_2d(bdst, &tmB, fb, k0, n0);
+                        }
                         k0 += bke;
                     } else {
-                        if (AMODE == AM_IM2COL) {
-                            tma_load_im2col_5d(adst, &tmA, fb, c0, aw, ah, ad, an,
-                                               static_cast<uint16_t>(fs * p.dw),
-                                               static_cast<uint16_t>(fr * p.dh),
-                                               static_cast<uint16_t>(ft * p.dd));
+                        const uint16_t ow = static_cast<uint16_t>(fs * p.dw);
+                        const uint16_t oh = static_cast<uint16_t>(fr * p.dh);
+                        const uint16_t od = static_cast<uint16_t>(ft * p.dd);
+                        if (PAIR) {
+                            if (AMODE == AM_IM2COL)
+                                tma_load_im2col_5d_pair(adst, &tmA, fb, c0, aw, ah, ad, an, ow, oh, od);
+                            else
+                                tma_load_4d_pair(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
+                            tma_load_3d_pair(bdst, &tmB, fb, c0, tap, n0);
                         } else {
-                            tma_load_4d(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
+                            if (AMODE == AM_IM2COL)
+                                tma_load_im2col_5d(adst, &tmA, fb, c0, aw, ah, ad, an, ow, oh, od);
+                            else
+                                tma_load_4d(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
+                            tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
                         }
-                        tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
                         ++tap;
                         if (++fs == p.S) {
                             fs = 0;
@@ -444,16 +491,16 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             if (p.BK == 128)
-                mma_issuer<4, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                   abort_flag);
+                mma_issuer<4, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                         abort_flag);
             else if (p.BK == 64)
-                mma_issuer<2, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                   abort_flag);
+                mma_issuer<2, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                         abort_flag);
             else
-                mma_issuer<1, FP8>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                   abort_flag);
+                mma_issuer<1, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
+                                         abort_flag);
         }
     } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------ epilogue
@@ -466,7 +513,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         const bool vec_ws = (p.K % 4) == 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         int acc_iter = 0, epi_iter = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        // the MMA issuer waits on the pair leader's accumulator-free barrier
+        const uint32_t tempty_dst0 = PAIR ? mapa_shared(tempty0, 0) : tempty0;
+        const int row_in_unit = kBM * static_cast<int>(rank) + row;
+        for (int u = unit0; u < total_units; u += ustride) {
             const Unit t = decode_unit(u, p);
             const int acc = acc_iter & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
@@ -476,11 +526,11 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             bool valid;
             if (AMODE == AM_TEMPORAL) {
                 const int plane = t.m_tile / p.hw_tiles;
-                const int hw = (t.m_tile - plane * p.hw_tiles) * kBM + row;
+                const int hw = (t.m_tile - plane * p.hw_tiles) * kTileM + row_in_unit;
                 valid = hw < p.HW;
                 m = static_cast<long long>(plane) * p.HW + hw;
             } else {
-                m = static_cast<long long>(t.m_tile) * kBM + row;
+                m = static_cast<long long>(t.m_tile) * kTileM + row_in_unit;
                 valid = m < p.M;
             }
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -492,10 +542,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 bool any;
                 if (AMODE == AM_TEMPORAL) {
                     plane = t.m_tile / p.hw_tiles;
-                    row0 = (t.m_tile - plane * p.hw_tiles) * kBM + q * 32;
+                    row0 = (t.m_tile - plane * p.hw_tiles) * kTileM + row_in_unit - lane;
                     any = row0 < p.HW;
                 } else {
-                    row0 = t.m_tile * kBM + q * 32;
+                    row0 = t.m_tile * kTileM + row_in_unit - lane;
                     any = row0 < p.M;
                 }
                 if (any) {
@@ -533,7 +583,12 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+                if (lane == 0) {
+                    if (PAIR)
+                        mbar_arrive_cluster(tempty_dst0 + 8 * acc);
+                    else
+                        mbar_arrive(tempty0 + 8 * acc);
+                }
                 ++acc_iter;
                 continue;
             }
@@ -554,7 +609,12 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cluster(tempty_dst0 + 8 * acc);
+                else
+                    mbar_arrive(tempty0 + 8 * acc);
+            }
             ++acc_iter;
         }
         if (p.epi_bytes && lane == 0) bulk_wait_all();   // stores done before the CTA leaves
@@ -568,37 +628,70 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     }
 
     __syncthreads();
+    // In a pair, both CTAs finish their roles (and the peer's last remote
+    // arrivals land) before either drains, frees TMEM or leaves.
+    if (PAIR) cluster_sync();
+    if (PAIR && *abort_flag) {
+        // a pair CTA's own loads signal the leader's barriers, so it cannot
+        // watch them land: after an abort both CTAs let ~100 us pass (far
+        // beyond any copy's latency) before draining and leaving
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000) {
+        }
+    }
     if (*abort_flag) {
-        // drain: TMA boxes issued but never waited for, then the MMAs in flight
-        if (warp == 0 && lane == 0 && !kGather) {
+        // drain: TMA boxes armed but never waited for, then the MMAs in flight
+        if (warp == 0 && lane == 0 && !kGather && rank == 0) {
             const uint32_t issued = misc[2], consumed = misc[3];
             for (uint32_t i = consumed; i < issued; ++i)
                 drain_wait(full0 + 8 * (i % static_cast<uint32_t>(p.stages)),
                            (i / static_cast<uint32_t>(p.stages)) & 1u);
         }
-        if (warp == 1 && lane == 0) {
-            tc_commit(drain_bar);
+        if (warp == 1 && lane == 0 && rank == 0) {
+            if (PAIR)
+                tc_commit_pair(drain_bar, 1);
+            else
+                tc_commit(drain_bar);
             drain_wait(drain_bar, 0);
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, p.tmem_cols);
     }
 }
 
-template <int AM, int F8>
+template <int AM, int F8, int PAIR>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                        const KParams& p, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = conv_igemm_kernel<AM, F8>;
+    auto kern = conv_igemm_kernel<AM, F8, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int threads = (AM == AM_GEMM_GATHER) ? 320 : 192;
-    kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, *tmC, p);
-    return cudaGetLastError();
+    if (!PAIR) {
+        kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, *tmC, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
 }
 
 }  // namespace
@@ -606,17 +699,25 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
 cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
                          const CUtensorMap* tmC, const KParams& p, int grid, size_t smem,
                          cudaStream_t stream) {
-    switch (amode * 2 + (fp8 ? 1 : 0)) {
-        case AM_IM2COL * 2 + 0: return launch_one<AM_IM2COL, 0>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_IM2COL * 2 + 1: return launch_one<AM_IM2COL, 1>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_TEMPORAL * 2 + 0: return launch_one<AM_TEMPORAL, 0>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_TEMPORAL * 2 + 1: return launch_one<AM_TEMPORAL, 1>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_GEMM_TMA * 2 + 0: return launch_one<AM_GEMM_TMA, 0>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_GEMM_TMA * 2 + 1: return launch_one<AM_GEMM_TMA, 1>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_GEMM_GATHER * 2 + 0:
-            return launch_one<AM_GEMM_GATHER, 0>(tmA, tmB, tmC, p, grid, smem, stream);
-        case AM_GEMM_GATHER * 2 + 1:
-            return launch_one<AM_GEMM_GATHER, 1>(tmA, tmB, tmC, p, grid, smem, stream);
+    const int key = (amode * 2 + (fp8 ? 1 : 0)) * 2 + (p.pair ? 1 : 0);
+    switch (key) {
+#define C3D_CASE(AM, F8, PR) \
+    case (AM * 2 + F8) * 2 + PR: return launch_one<AM, F8, PR>(tmA, tmB, tmC, p, grid, smem, stream);
+        C3D_CASE(AM_IM2COL, 0, 0)
+        C3D_CASE(AM_IM2COL, 1, 0)
+        C3D_CASE(AM_IM2COL, 0, 1)
+        C3D_CASE(AM_IM2COL, 1, 1)
+        C3D_CASE(AM_TEMPORAL, 0, 0)
+        C3D_CASE(AM_TEMPORAL, 1, 0)
+        C3D_CASE(AM_TEMPORAL, 0, 1)
+        C3D_CASE(AM_TEMPORAL, 1, 1)
+        C3D_CASE(AM_GEMM_TMA, 0, 0)
+        C3D_CASE(AM_GEMM_TMA, 1, 0)
+        C3D_CASE(AM_GEMM_TMA, 0, 1)
+        C3D_CASE(AM_GEMM_TMA, 1, 1)
+        C3D_CASE(AM_GEMM_GATHER, 0, 0)
+        C3D_CASE(AM_GEMM_GATHER, 1, 0)
+#undef C3D_CASE
         default: return cudaErrorInvalidValue;
     }
 }

@@ -49,6 +49,7 @@ struct KParams {
     uint32_t sbo;       // smem descriptor stride byte offset (8 rows)
     uint32_t tmem_cols; // allocated TMEM columns (power of two >= 2*BN)
     uint32_t epi_bytes; // shared staging of the TMA-store epilogue (0: direct stores)
+    int pair;           // 1: CTA-pair kernel (cluster of 2, 256-row units)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;
     const unsigned char* gb;

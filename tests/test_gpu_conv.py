@@ -226,3 +226,32 @@ def test_unsupported_shape_raises(pkg):
     with pytest.raises(pkg.ConvError) as e:
         pkg.conv_fwd(x, w, 1, 1, 1)
     assert e.value.status == pkg.CONV_ERR_UNSUPPORTED
+
+
+# CTA-pair kernel (two SMs per 256-row unit), forced on small shapes with
+# several units per pair and ragged M / N tails, for every TMA operand mode.
+PAIR_CASES = [
+    ((2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1, "128,128,0,0,1"),
+    ((2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1, "256,128,0,0,1"),
+    ((1, 6, 10, 12, 32), (96, 3, 3, 3, 32), (1, 2, 1), (1, 1, 0), (2, 1, 1), "96,64,0,0,1"),
+    ((1, 5, 10, 50, 64), (200, 3, 1, 1, 64), 1, (1, 0, 0), 1, "224,128,0,0,1"),
+    ((1, 7, 9, 30, 32), (64, 3, 1, 1, 32), 1, (1, 0, 0), 1, "64,64,0,0,1"),
+    ((600, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, 1, "160,128,0,0,1"),
+    ((3, 4, 7, 9, 64), (256, 1, 1, 1, 64), 1, 0, 1, "256,128,0,0,1"),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[str(i) for i in range(len(PAIR_CASES))])
+def test_cta_pair_kernel(pkg, case):
+    xs, ws, st, pa, di, spec = case
+    old = os.environ.get("CONV3D_PAIR")
+    os.environ["CONV3D_PAIR"] = "1"
+    try:
+        with forced_tile(spec):
+            _run_and_check(pkg, xs, ws, st, pa, di, seed=90 + PAIR_CASES.index(case),
+                           split_k=False, what=f"pair {case}")
+    finally:
+        if old is None:
+            os.environ.pop("CONV3D_PAIR", None)
+        else:
+            os.environ["CONV3D_PAIR"] = old
