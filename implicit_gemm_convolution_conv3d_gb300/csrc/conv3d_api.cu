@@ -287,13 +287,16 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
     // tile defaults
     int BN = pick_bn(g.K);
     int BK = (P->amode == AM_GEMM_GATHER) ? 128 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? rg * elt : g.C * elt);
-    int stages = 0, group_m = 8, splits = 0;
+    // raster group 1: a unit's row block meets every column tile before the
+    // next row block starts (best on the measured workloads)
+    int stages = 0, group_m = 1, splits = 0, pair_pref = -1;
     if (const TileEntry* e = lookup_tile(P->fp8, P->cls, g, P->M)) {
         if (e->BN) BN = e->BN;
         if (e->BK) BK = e->BK;
         if (e->stages) stages = e->stages;
         if (e->group_m) group_m = e->group_m;
         if (e->splits) splits = e->splits;
+        pair_pref = e->pair;
     }
     force_tile(&BN, &BK, &stages, &group_m, &splits);
     if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128) ||
@@ -356,6 +359,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
                                  ? g.N * g.Do * ((g.H * g.W + 2 * kBM - 1) / (2 * kBM))
                                  : (P->M + 2 * kBM - 1) / (2 * kBM);
         int want = pm * P->n_tiles >= 2LL * num_sms ? 1 : 0;
+        if (pair_pref >= 0) want = pair_pref;
         if (const char* e = std::getenv("CONV3D_PAIR")) want = (e[0] == '1') ? 1 : 0;
         if (want) {
             P->pair = 1;

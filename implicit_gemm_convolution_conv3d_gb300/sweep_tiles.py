@@ -28,16 +28,19 @@ import implicit_gemm_convolution_conv3d_gb300 as pkg  # noqa: E402
 CLASS_CODE = {"generic": 0, "temporal": 1, "point_gemm": 2}
 
 
-def candidates(quick: bool, K: int, k_row_bytes: int):
+def candidates(quick: bool, K: int, k_row_bytes: int, default_bn: int):
     bns = [bn for bn in (256, 224, 192, 160, 128, 96, 64, 32) if bn <= max(32, ((K + 31) // 32) * 32)]
     bks = [bk for bk in (128, 64, 32) if bk <= max(32, k_row_bytes)]
-    groups = [1, 4, 8, 16, 32] if not quick else [8, 16]
-    for bn, bk, grp in itertools.product(bns, bks, groups):
-        yield bn, bk, 0, grp, 1
+    groups = [1, 2, 4, 8, 16, 32]
+    if quick:   # default tile width and k-step, every raster group and pair choice
+        bns, bks = [default_bn], [128 if k_row_bytes >= 128 else bks[0]]
+    for bn, bk, grp, pair in itertools.product(bns, bks, groups, (0, 1)):
+        yield bn, bk, 0, grp, 1, pair
 
 
-def time_case(x, w, wl, scale_x, scale_w, spec, flush, reps):
+def time_case(x, w, wl, scale_x, scale_w, spec, flush, reps, pair):
     os.environ["CONV3D_FORCE_TILE"] = spec
+    os.environ["CONV3D_PAIR"] = str(pair)
     try:
         plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
                                  1 if x.dtype == torch.float8_e4m3fn else 0)
@@ -88,24 +91,26 @@ def main():
                                  1 if wl.dtype == "fp8" else 0)
         row_bytes = C * elt if base["class"] != "point_gemm" else T * R * S * C * elt
         results = []
-        for bn, bk, st, grp, spl in candidates(args.quick, K, row_bytes):
+        for bn, bk, st, grp, spl, pair in candidates(args.quick, K, row_bytes, base["tile_n"]):
             spec = f"{bn},{bk},{st},{grp},{spl}"
-            ms, plan = time_case(x, w, wl, sx, sw, spec, flush, args.reps)
+            ms, plan = time_case(x, w, wl, sx, sw, spec, flush, args.reps, pair)
             if ms is None:
                 continue
             tf = 2.0 * cw_flops(wl) / (ms * 1e-3) / 1e12
-            results.append((ms, spec, plan))
-            print(f"{name:26s} {spec:18s} {ms:9.4f} ms {tf:8.1f} TFLOPS stages={plan['stages']}",
-                  flush=True)
+            results.append((ms, spec, plan, pair))
+            print(f"{name:26s} {spec:18s} pair={pair} {ms:9.4f} ms {tf:8.1f} TFLOPS "
+                  f"stages={plan['stages']}", flush=True)
         os.environ.pop("CONV3D_FORCE_TILE", None)
+        os.environ.pop("CONV3D_PAIR", None)
         results.sort(key=lambda r: r[0])
-        best_ms, best_spec, best_plan = results[0]
+        best_ms, best_spec, best_plan, best_pair = results[0]
         bn, bk, _, grp, spl = (int(v) for v in best_spec.split(","))
         M = best_plan_rows(wl)
         rows.append(f"    {{{1 if wl.dtype == 'fp8' else 0}, {CLASS_CODE[best_plan['class']]}, "
                     f"{C}, {K}, {T * R * S}, {M}, {M}, {bn}, {bk}, {best_plan['stages']}, {grp}, "
-                    f"{spl}}},   // {name}: {best_ms:.3f} ms")
-        report[name] = {"best_ms": best_ms, "best": best_spec, "all": [(r[0], r[1]) for r in results]}
+                    f"{spl}, {best_pair}}},   // {name}: {best_ms:.3f} ms")
+        report[name] = {"best_ms": best_ms, "best": best_spec, "pair": best_pair,
+                        "all": [(r[0], r[1], r[3]) for r in results]}
         del x, w
         torch.cuda.empty_cache()
     print("\n".join(rows))
