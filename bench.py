@@ -292,6 +292,12 @@ def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
 
 # ---------------------------------------------------------------- CPU oracle arm
 
+def replica_throughput(world: int, flop_per_step: float, ms_max: float) -> float:
+    """Whole-job TFLOPS of `world` independent replicas, each doing
+    flop_per_step per step, timed by the slowest rank's mean step (ms)."""
+    return world * flop_per_step / (ms_max * 1e-3) / 1e12
+
+
 def cpu_oracle_rate(wl: cw.Workload, x_host, w_host, target_s: float = 10.0):
     """fp64 oracle TFLOPS on a bounded sample of output elements, sized for
     about target_s seconds of work on all host cores."""
@@ -331,7 +337,8 @@ def reference_arm(args):
     if wl.dtype == "fp8":
         raise SystemExit("the reference arm times bf16 workloads")
     xb, wb = host_inputs(wl)
-    per_step_s = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step_s = args.ref_seconds if args.ref_seconds > 0 else \
+        max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_oracle_rate(wl, xb, wb, target_s=min(per_step_s, 5.0))
     vals = []
@@ -380,8 +387,8 @@ def main_arm(args):
     ms = statistics.mean(res["ms"])
     ms_max = max_over_ranks(dist, ms, device)
     e2e_ms = max_over_ranks(dist, statistics.mean(res["e2e"]["ms"]), device)
-    value = world * res["flop"] / (ms_max * 1e-3) / 1e12
-    e2e_value = world * res["flop"] / (e2e_ms * 1e-3) / 1e12
+    value = replica_throughput(world, res["flop"], ms_max)
+    e2e_value = replica_throughput(world, res["flop"], e2e_ms)
 
     secondary = {}
     if not args.no_secondary:
@@ -444,6 +451,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(cw.BY_NAME))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=0.0,
+                    help="reference arm: seconds of oracle work per step (0: auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
