@@ -171,6 +171,7 @@ struct Plan {
     uint32_t tmem_cols;
     uint32_t epi_bytes;      // TMA-store epilogue staging (0: direct stores)
     int pair;                // CTA-pair kernel: 256-row units on clusters of two CTAs
+    int msub;                // row sub-tiles per unit sharing each B stage
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
@@ -289,7 +290,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
     int BK = (P->amode == AM_GEMM_GATHER) ? 128 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? rg * elt : g.C * elt);
     // raster group 1: a unit's row block meets every column tile before the
     // next row block starts (best on the measured workloads)
-    int stages = 0, group_m = 1, splits = 0, pair_pref = -1;
+    int stages = 0, group_m = 1, splits = 0, pair_pref = -1, msub_pref = 0;
     if (const TileEntry* e = lookup_tile(P->fp8, P->cls, g, P->M)) {
         if (e->BN) BN = e->BN;
         if (e->BK) BK = e->BK;
@@ -297,6 +298,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
         if (e->group_m) group_m = e->group_m;
         if (e->splits) splits = e->splits;
         pair_pref = e->pair;
+        msub_pref = e->msub;
     }
     force_tile(&BN, &BK, &stages, &group_m, &splits);
     if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128) ||
@@ -366,6 +368,23 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
             set_m_tiles(2 * kBM);
         }
     }
+    // Two row sub-tiles per unit share every B stage (two accumulators in
+    // TMEM, no epilogue overlap): halves the B bytes per flop, for long
+    // reductions where the exposed epilogue is a small share of the unit.
+    P->msub = 1;
+    if (P->amode != AM_GEMM_GATHER && splits == 1 && 2 * BN <= 256 + 256) {
+        const int rows = (2 * kBM) << P->pair;
+        const long long mt = P->cls == CONV_CLASS_TEMPORAL
+                                 ? g.N * g.Do * ((g.H * g.W + rows - 1) / rows)
+                                 : (P->M + rows - 1) / rows;
+        int want = (P->k_steps >= 384 && mt * P->n_tiles >= 2LL * (num_sms >> P->pair)) ? 2 : 1;
+        if (msub_pref > 0) want = msub_pref;
+        if (const char* e = std::getenv("CONV3D_MSUB")) want = (e[0] == '2') ? 2 : 1;
+        if (want == 2) {
+            P->msub = 2;
+            set_m_tiles(rows);
+        }
+    }
 
     // bf16 output leaves through TMA stores when its rows are 16-byte aligned;
     // split-K partials are written directly
@@ -373,7 +392,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
     P->epi_bytes = (splits == 1 && g.K % 8 == 0 && P->cls != CONV_CLASS_POINT_GEMM)
                        ? kEpiStageBytes : 0u;
     // pipeline depth from the shared-memory budget (a pair CTA holds half of B)
-    const size_t stage_bytes = static_cast<size_t>(kBM + (BN >> P->pair)) * BK;
+    const size_t stage_bytes = static_cast<size_t>(P->msub * kBM + (BN >> P->pair)) * BK;
     const size_t fixed = 1024 + 256 + P->epi_bytes;
     const int max_stages = static_cast<int>((smem_optin - fixed) / stage_bytes);
     if (stages == 0) stages = std::min(8, max_stages);
@@ -645,7 +664,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.BN = P.BN;
     k.BK = P.BK;
     k.stages = P.stages;
-    k.a_stage_bytes = static_cast<uint32_t>(kBM * P.BK);
+    k.a_stage_bytes = static_cast<uint32_t>(P.msub * kBM * P.BK);
     k.b_stage_bytes = static_cast<uint32_t>((P.BN >> P.pair) * P.BK);
     k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
     k.idesc = make_idesc(P.fp8, P.BN, kBM << P.pair);
@@ -654,6 +673,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.tmem_cols = P.tmem_cols;
     k.epi_bytes = P.epi_bytes;
     k.pair = P.pair;
+    k.msub = P.msub;
     k.ga = static_cast<const unsigned char*>(x);
     k.gb = static_cast<const unsigned char*>(w);
     k.g_row_bytes = P.g_row_bytes;
@@ -667,9 +687,9 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
                      "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
-                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d\n",
+                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d msub=%d\n",
                      P.cls, P.amode, P.fp8, P.M, k.K, P.BN, P.BK, P.stages, P.splits, P.k_steps,
-                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair);
+                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair, P.msub);
     }
     cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");

@@ -239,7 +239,7 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
 // commit the stage back to the producer; per tile, commit the accumulator to
 // the epilogue.  Shared-memory descriptors are built once and advanced by
 // adding encoded byte offsets (address field = bytes >> 4).
-template <int KMMA, int FP8, int PAIR>
+template <int KMMA, int FP8, int PAIR, int MSUB>
 __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uint32_t full0,
                                            uint32_t empty0, uint32_t tfull0, uint32_t tempty0,
                                            uint32_t tmem_base, uint32_t* misc,
@@ -248,17 +248,21 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
     const uint64_t adesc0 = make_smem_desc(tiles, p.sbo, p.layout);
     const uint64_t bdesc0 = make_smem_desc(tiles + p.a_stage_bytes, p.sbo, p.layout);
     const uint32_t stage_step = p.stage_bytes >> 4;
+    // msub row sub-tiles share each B stage; the TMEM holds 2/msub unit
+    // accumulators (double-buffered when msub == 1)
+    constexpr int nacc = 2 / MSUB;
+    const uint32_t sub_step = (static_cast<uint32_t>(kBM) * p.BK) >> 4;   // A sub-tile, encoded
     int stage = 0, acc_iter = 0;
     uint32_t phase = 0, consumed = 0;
     for (int u = static_cast<int>(blockIdx.x) >> PAIR; u < total_units; u += gridDim.x >> PAIR) {
         const Unit t = decode_unit(u, p);
         const int ks0 = t.split * p.steps_per_split;
         const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
-        const int acc = acc_iter & 1;
-        const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
+        const int acc = acc_iter % nacc;
+        const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
         if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns)) return;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MSUB * p.BN);
         uint32_t accum = 0u;
         for (int ks = ks0; ks < ks1; ++ks) {
             if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) return;
@@ -268,16 +272,21 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
             const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
 #pragma unroll
             for (int k = 0; k < KMMA; ++k) {
-                if (PAIR) {
-                    if (FP8)
-                        tc_mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                    else
-                        tc_mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                } else {
-                    if (FP8)
-                        tc_mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                    else
-                        tc_mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+#pragma unroll
+                for (int sub = 0; sub < MSUB; ++sub) {
+                    const uint32_t d = d_tmem + static_cast<uint32_t>(sub * p.BN);
+                    const uint64_t a = ad + sub * sub_step + 2 * k;
+                    if (PAIR) {
+                        if (FP8)
+                            tc_mma_f8_pair(d, a, bd + 2 * k, p.idesc, accum);
+                        else
+                            tc_mma_f16_pair(d, a, bd + 2 * k, p.idesc, accum);
+                    } else {
+                        if (FP8)
+                            tc_mma_f8(d, a, bd + 2 * k, p.idesc, accum);
+                        else
+                            tc_mma_f16(d, a, bd + 2 * k, p.idesc, accum);
+                    }
                 }
                 accum = 1u;
             }
@@ -296,6 +305,138 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
         else
             tc_commit(tfull0 + 8 * acc);
         ++acc_iter;
+    }
+}
+
+// The TMA producer (one thread): per k-step, wait for a free stage, arm its
+// full barrier with the stage's bytes (both CTAs' in a pair) and issue the A
+// box of each of the MSUB row sub-tiles and the B box.
+template <int AMODE, int FP8, int PAIR, int MSUB>
+__device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                             const KParams& p, uint32_t tiles, uint32_t full0,
+                                             uint32_t empty0, uint32_t* misc,
+                                             volatile uint32_t* abort_flag, uint32_t rank) {
+    constexpr int kTileM = kBM << PAIR;
+    constexpr int kElt = FP8 ? 1 : 2;
+    const int bke = p.BK / kElt;
+    const int total_units = p.m_tiles * p.n_tiles * p.splits;
+    const int unit0 = static_cast<int>(blockIdx.x) >> PAIR;
+    const int ustride = static_cast<int>(gridDim.x) >> PAIR;
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok_run = true;
+    for (int u = unit0; u < total_units && ok_run; u += ustride) {
+        const Unit t = decode_unit(u, p);
+        const int ks0 = t.split * p.steps_per_split;
+        const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+        // this CTA's B rows: all BN columns, or its half of them in a pair
+        const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (p.BN >> PAIR);
+        // A coordinates of each row sub-tile (128 rows of this CTA)
+        int aw[2] = {0, 0}, ah[2] = {0, 0}, ad[2] = {0, 0}, an[2] = {0, 0}, am0[2] = {0, 0};
+        for (int sub = 0; sub < MSUB; ++sub) {
+            const int first = sub * kTileM + kBM * static_cast<int>(rank);
+            if (AMODE == AM_IM2COL) {
+                const long long m0 =
+                    static_cast<long long>(t.m_tile) * kTileM * MSUB + first;
+                const int ow = static_cast<int>(m0 % p.Wo);
+                const long long q1 = m0 / p.Wo;
+                const int oh = static_cast<int>(q1 % p.Ho);
+                const long long q2 = q1 / p.Ho;
+                const int od = static_cast<int>(q2 % p.Do);
+                an[sub] = static_cast<int>(q2 / p.Do);
+                aw[sub] = ow * p.sw - p.pw;
+                ah[sub] = oh * p.sh - p.ph;
+                ad[sub] = od * p.sd - p.pd;
+            } else if (AMODE == AM_TEMPORAL) {
+                const int plane = t.m_tile / p.hw_tiles;
+                const int hwb = t.m_tile - plane * p.hw_tiles;
+                const int od = plane % p.Do;
+                an[sub] = plane / p.Do;
+                ad[sub] = od * p.sd - p.pd;
+                ah[sub] = hwb * kTileM * MSUB + first;   // first H*W row
+            } else {
+                am0[sub] = t.m_tile * kTileM * MSUB + first;
+            }
+        }
+        // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
+        // position is decoded once per unit and then stepped incrementally.
+        int tap = ks0 % p.taps;
+        int c0 = (ks0 / p.taps) * bke;
+        int fs = tap % p.S, fr = (tap / p.S) % p.R, ft = tap / (p.S * p.R);
+        int k0 = ks0 * bke;   // GEMM modes: first reduction element of the k-step
+        for (int ks = ks0; ks < ks1; ++ks) {
+            if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
+                ok_run = false;
+                break;
+            }
+            uint32_t fb = full0 + 8 * stage;
+            if (PAIR) {
+                // the leader's full barrier counts both CTAs' bytes
+                if (rank == 0) mbar_arrive_expect_tx(fb, 2u * p.stage_bytes);
+                fb = mapa_shared(fb, 0);
+            } else {
+                mbar_arrive_expect_tx(fb, p.stage_bytes);
+            }
+            const uint32_t adst0 = tiles + stage * p.stage_bytes;
+            const uint32_t bdst = adst0 + p.a_stage_bytes;
+            if (AMODE == AM_GEMM_TMA) {
+                for (int sub = 0; sub < MSUB; ++sub) {
+                    const uint32_t adst = adst0 + sub * kBM * p.BK;
+                    if (PAIR)
+                        tma_load_2d_pair(adst, &tmA, fb, k0, am0[sub]);
+                    else
+                        tma_load_2d(adst, &tmA, fb, k0, am0[sub]);
+                }
+                if (PAIR)
+                    tma_load_2d_pair(bdst, &tmB, fb, k0, n0);
+                else
+                    tma_load_2d(bdst, &tmB, fb, k0, n0);
+                k0 += bke;
+            } else {
+                const uint16_t ow = static_cast<uint16_t>(fs * p.dw);
+                const uint16_t oh = static_cast<uint16_t>(fr * p.dh);
+                const uint16_t od = static_cast<uint16_t>(ft * p.dd);
+                for (int sub = 0; sub < MSUB; ++sub) {
+                    const uint32_t adst = adst0 + sub * kBM * p.BK;
+                    if (PAIR) {
+                        if (AMODE == AM_IM2COL)
+                            tma_load_im2col_5d_pair(adst, &tmA, fb, c0, aw[sub], ah[sub],
+                                                    ad[sub], an[sub], ow, oh, od);
+                        else
+                            tma_load_4d_pair(adst, &tmA, fb, c0, ah[sub], ad[sub] + ft * p.dd,
+                                             an[sub]);
+                    } else {
+                        if (AMODE == AM_IM2COL)
+                            tma_load_im2col_5d(adst, &tmA, fb, c0, aw[sub], ah[sub], ad[sub],
+                                               an[sub], ow, oh, od);
+                        else
+                            tma_load_4d(adst, &tmA, fb, c0, ah[sub], ad[sub] + ft * p.dd,
+                                        an[sub]);
+                    }
+                }
+                if (PAIR)
+                    tma_load_3d_pair(bdst, &tmB, fb, c0, tap, n0);
+                else
+                    tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
+                ++tap;
+                if (++fs == p.S) {
+                    fs = 0;
+                    if (++fr == p.R) {
+                        fr = 0;
+                        if (++ft == p.T) {
+                            ft = 0;
+                            tap = 0;
+                            c0 += bke;
+                        }
+                    }
+                }
+            }
+            misc[2] = ++issued;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
     }
 }
 
@@ -331,7 +472,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA within the pair
     const int unit0 = static_cast<int>(blockIdx.x) >> PAIR;
     const int ustride = static_cast<int>(gridDim.x) >> PAIR;
-    constexpr int kTileM = kBM << PAIR;                     // rows of a work unit
+    constexpr int kTileM = kBM << PAIR;   // rows of a row sub-tile (a unit has msub of them)
     constexpr bool kGather = (AMODE == AM_GEMM_GATHER);
     constexpr int kElt = FP8 ? 1 : 2;
     const int bke = p.BK / kElt;   // elements of one row per k-step
@@ -390,117 +531,28 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         }
         // ------------------------------------------------------ TMA producer
         if (!kGather && lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, issued = 0;
-            bool ok_run = true;
-            for (int u = unit0; u < total_units && ok_run; u += ustride) {
-                const Unit t = decode_unit(u, p);
-                const int ks0 = t.split * p.steps_per_split;
-                const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
-                // this CTA's B rows: all BN columns, or its half of them in a pair
-                const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (p.BN >> PAIR);
-                int aw = 0, ah = 0, ad = 0, an = 0, am0 = 0;
-                if (AMODE == AM_IM2COL) {
-                    const long long m0 = static_cast<long long>(t.m_tile) * kTileM + kBM * rank;
-                    const int ow = static_cast<int>(m0 % p.Wo);
-                    const long long q1 = m0 / p.Wo;
-                    const int oh = static_cast<int>(q1 % p.Ho);
-                    const long long q2 = q1 / p.Ho;
-                    const int od = static_cast<int>(q2 % p.Do);
-                    an = static_cast<int>(q2 / p.Do);
-                    aw = ow * p.sw - p.pw;
-                    ah = oh * p.sh - p.ph;
-                    ad = od * p.sd - p.pd;
-                } else if (AMODE == AM_TEMPORAL) {
-                    const int plane = t.m_tile / p.hw_tiles;
-                    const int hwb = t.m_tile - plane * p.hw_tiles;
-                    const int od = plane % p.Do;
-                    an = plane / p.Do;
-                    ad = od * p.sd - p.pd;
-                    ah = hwb * kTileM + kBM * static_cast<int>(rank);   // first H*W row
-                } else {
-                    am0 = t.m_tile * kTileM + kBM * static_cast<int>(rank);
-                }
-                // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
-                // position is decoded once per unit and then stepped incrementally.
-                int tap = ks0 % p.taps;
-                int c0 = (ks0 / p.taps) * bke;
-                int fs = tap % p.S, fr = (tap / p.S) % p.R, ft = tap / (p.S * p.R);
-                int k0 = ks0 * bke;   // GEMM modes: first reduction element of the k-step
-                for (int ks = ks0; ks < ks1; ++ks) {
-                    if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
-                        ok_run = false;
-                        break;
-                    }
-                    uint32_t fb = full0 + 8 * stage;
-                    if (PAIR) {
-                        // the leader's full barrier counts both CTAs' bytes
-                        if (rank == 0) mbar_arrive_expect_tx(fb, 2u * p.stage_bytes);
-                        fb = mapa_shared(fb, 0);
-                    } else {
-                        mbar_arrive_expect_tx(fb, p.stage_bytes);
-                    }
-                    const uint32_t adst = tiles + stage * p.stage_bytes;
-                    const uint32_t bdst = adst + p.a_stage_bytes;
-                    if (AMODE == AM_GEMM_TMA) {
-                        if (PAIR) {
-                            tma_load_2d_pair(adst, &tmA, fb, k0, am0);
-                            tma_load_2d_pair(bdst, &tmB, fb, k0, n0);
-                        } else {
-                            tma_load_2d(adst, &tmA, fb, k0, am0);
-                            tma_load_2d(bdst, &tmB, fb, k0, n0);
-                        }
-                        k0 += bke;
-                    } else {
-                        const uint16_t ow = static_cast<uint16_t>(fs * p.dw);
-                        const uint16_t oh = static_cast<uint16_t>(fr * p.dh);
-                        const uint16_t od = static_cast<uint16_t>(ft * p.dd);
-                        if (PAIR) {
-                            if (AMODE == AM_IM2COL)
-                                tma_load_im2col_5d_pair(adst, &tmA, fb, c0, aw, ah, ad, an, ow, oh, od);
-                            else
-                                tma_load_4d_pair(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
-                            tma_load_3d_pair(bdst, &tmB, fb, c0, tap, n0);
-                        } else {
-                            if (AMODE == AM_IM2COL)
-                                tma_load_im2col_5d(adst, &tmA, fb, c0, aw, ah, ad, an, ow, oh, od);
-                            else
-                                tma_load_4d(adst, &tmA, fb, c0, ah, ad + ft * p.dd, an);
-                            tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
-                        }
-                        ++tap;
-                        if (++fs == p.S) {
-                            fs = 0;
-                            if (++fr == p.R) {
-                                fr = 0;
-                                if (++ft == p.T) {
-                                    ft = 0;
-                                    tap = 0;
-                                    c0 += bke;
-                                }
-                            }
-                        }
-                    }
-                    misc[2] = ++issued;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
+            if (p.msub == 2)
+                tma_producer<AMODE, FP8, PAIR, 2>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag,
+                                                  rank);
+            else
+                tma_producer<AMODE, FP8, PAIR, 1>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag,
+                                                  rank);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
-            if (p.BK == 128)
-                mma_issuer<4, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                         abort_flag);
-            else if (p.BK == 64)
-                mma_issuer<2, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                         abort_flag);
-            else
-                mma_issuer<1, FP8, PAIR>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc,
-                                         abort_flag);
+#define C3D_MMA(KM, MS) \
+    mma_issuer<KM, FP8, PAIR, MS>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc, abort_flag)
+            if (p.msub == 2) {
+                if (p.BK == 128) C3D_MMA(4, 2);
+                else if (p.BK == 64) C3D_MMA(2, 2);
+                else C3D_MMA(1, 2);
+            } else {
+                if (p.BK == 128) C3D_MMA(4, 1);
+                else if (p.BK == 64) C3D_MMA(2, 1);
+                else C3D_MMA(1, 1);
+            }
+#undef C3D_MMA
         }
     } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------ epilogue
@@ -512,44 +564,46 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         const bool vec_out = (p.K % 8) == 0;
         const bool vec_ws = (p.K % 4) == 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const int nacc = 2 / p.msub;
+        const int unit_rows = kTileM * p.msub;
         int acc_iter = 0, epi_iter = 0;
         // the MMA issuer waits on the pair leader's accumulator-free barrier
         const uint32_t tempty_dst0 = PAIR ? mapa_shared(tempty0, 0) : tempty0;
-        const int row_in_unit = kBM * static_cast<int>(rank) + row;
+        const uint32_t bufs = epi0 + static_cast<uint32_t>(warp - 2) * 2u * kEpiChunkBytes;
         for (int u = unit0; u < total_units; u += ustride) {
             const Unit t = decode_unit(u, p);
-            const int acc = acc_iter & 1;
-            const uint32_t acc_phase = static_cast<uint32_t>(acc_iter >> 1) & 1u;
+            const int acc = acc_iter % nacc;
+            const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
             if (!wait_bar(tfull0 + 8 * acc, acc_phase, abort_flag, p.status, p.wait_ns)) break;
             tc_fence_after();
-            long long m;
-            bool valid;
+            int plane = 0, unit_row0;   // temporal: plane and first H*W row of the unit
             if (AMODE == AM_TEMPORAL) {
-                const int plane = t.m_tile / p.hw_tiles;
-                const int hw = (t.m_tile - plane * p.hw_tiles) * kTileM + row_in_unit;
-                valid = hw < p.HW;
-                m = static_cast<long long>(plane) * p.HW + hw;
+                plane = t.m_tile / p.hw_tiles;
+                unit_row0 = (t.m_tile - plane * p.hw_tiles) * unit_rows;
             } else {
-                m = static_cast<long long>(t.m_tile) * kTileM + row_in_unit;
-                valid = m < p.M;
+                unit_row0 = t.m_tile * unit_rows;
             }
-            const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>(acc * p.BN);
-            if (p.epi_bytes) {
-                // TMA-store epilogue: the warp's 32 rows leave in 32x32 chunks
-                // staged in shared memory (64-byte swizzle, two buffers).
-                int row0, plane = 0;
-                bool any;
+            for (int sub = 0; sub < p.msub; ++sub) {
+                // this thread's row of the unit, and the warp's first row
+                const int wrow0 = unit_row0 + sub * kTileM + kBM * static_cast<int>(rank) + q * 32;
+                const int r = wrow0 + lane;
+                long long m;
+                bool valid, any;
                 if (AMODE == AM_TEMPORAL) {
-                    plane = t.m_tile / p.hw_tiles;
-                    row0 = (t.m_tile - plane * p.hw_tiles) * kTileM + row_in_unit - lane;
-                    any = row0 < p.HW;
+                    valid = r < p.HW;
+                    any = wrow0 < p.HW;
+                    m = static_cast<long long>(plane) * p.HW + r;
                 } else {
-                    row0 = t.m_tile * kTileM + row_in_unit - lane;
-                    any = row0 < p.M;
+                    valid = r < p.M;
+                    any = wrow0 < p.M;
+                    m = r;
                 }
-                if (any) {
-                    const uint32_t bufs = epi0 + static_cast<uint32_t>(warp - 2) * 2u * kEpiChunkBytes;
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                    static_cast<uint32_t>((acc * p.msub + sub) * p.BN);
+                if (p.epi_bytes) {
+                    // TMA-store epilogue: the warp's 32 rows leave in 32x32 chunks
+                    // staged in shared memory (64-byte swizzle, two buffers)
+                    if (!any) continue;
                     for (int j = 0; j < p.BN / 32; ++j) {
                         const int n0 = t.n_tile * p.BN + 32 * j;
                         if (n0 >= p.K) break;
@@ -574,36 +628,27 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                         __syncwarp();
                         if (lane == 0) {
                             if (AMODE == AM_TEMPORAL)
-                                tma_store_3d(&tmC, buf, n0, row0, plane);
+                                tma_store_3d(&tmC, buf, n0, wrow0, plane);
                             else
-                                tma_store_2d(&tmC, buf, n0, row0);
+                                tma_store_2d(&tmC, buf, n0, wrow0);
                             bulk_commit();
                         }
                     }
+                    continue;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (PAIR)
-                        mbar_arrive_cluster(tempty_dst0 + 8 * acc);
-                    else
-                        mbar_arrive(tempty0 + 8 * acc);
-                }
-                ++acc_iter;
-                continue;
-            }
-            for (int j = 0; j < p.BN / 32; ++j) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tb + 32 * j, v);
-                tmem_ld_wait();
-                const int n0 = t.n_tile * p.BN + 32 * j;
-                if (valid && n0 < p.K) {
-                    const int cnt = min(32, p.K - n0);
-                    if (p.splits == 1) {
-                        store_row_bf16(out + m * p.K + n0, v, scale, cnt, vec_out);
-                    } else {
-                        float* dst = p.ws + (static_cast<long long>(t.split) * p.M + m) * p.K + n0;
-                        store_row_f32(dst, v, cnt, vec_ws);
+                for (int j = 0; j < p.BN / 32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tb + 32 * j, v);
+                    tmem_ld_wait();
+                    const int n0 = t.n_tile * p.BN + 32 * j;
+                    if (valid && n0 < p.K) {
+                        const int cnt = min(32, p.K - n0);
+                        if (p.splits == 1) {
+                            store_row_bf16(out + m * p.K + n0, v, scale, cnt, vec_out);
+                        } else {
+                            float* dst = p.ws + (static_cast<long long>(t.split) * p.M + m) * p.K + n0;
+                            store_row_f32(dst, v, cnt, vec_ws);
+                        }
                     }
                 }
             }

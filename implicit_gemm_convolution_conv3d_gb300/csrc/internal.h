@@ -50,6 +50,7 @@ struct KParams {
     uint32_t tmem_cols; // allocated TMEM columns (power of two >= 2*BN)
     uint32_t epi_bytes; // shared staging of the TMA-store epilogue (0: direct stores)
     int pair;           // 1: CTA-pair kernel (cluster of 2, 256-row units)
+    int msub;           // row sub-tiles per unit sharing each B stage (1 or 2)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;
     const unsigned char* gb;

@@ -13,15 +13,16 @@ struct TileEntry {
     long long m_lo, m_hi;
     int BN, BK, stages, group_m, splits;
     int pair;           // CTA-pair kernel: -1 default rule, 0 off, 1 on
+    int msub;           // row sub-tiles sharing each B stage: 0 default rule, 1 or 2
 };
 
 static const TileEntry kTileTable[] = {
-    // fp8 cls C     K     TRS  m_lo     m_hi       BN   BK  st  grp split pair
-    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, -1},   // sentinel (never matches: C = 0)
+    // fp8 cls C     K     TRS  m_lo     m_hi       BN   BK  st  grp split pair msub
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, -1, 0},   // sentinel (never matches: C = 0)
     // measured on GB300 (sweep_tiles.py --quick, 5 reps, L2 flushed):
-    {0, 0, 2048, 2048, 27, 100000, 1LL << 40, 256, 128, 0, 1, 0, 1},   // video 3x3x3: 26.72 ms
-    {1, 0, 1024, 1024, 9, 100000, 1LL << 40, 256, 128, 0, 2, 0, 1},    // fp8 1x3x3: 9.68 ms
-    {0, 1, 640, 640, 3, 100000, 1LL << 40, 224, 128, 0, 1, 0, 1},      // temporal 3x1x1: 5.56 ms
+    {0, 0, 2048, 2048, 27, 100000, 1LL << 40, 256, 128, 0, 1, 0, 1, 0},   // video 3x3x3: 26.72 ms
+    {1, 0, 1024, 1024, 9, 100000, 1LL << 40, 256, 128, 0, 2, 0, 1, 0},    // fp8 1x3x3: 9.68 ms
+    {0, 1, 640, 640, 3, 100000, 1LL << 40, 224, 128, 0, 1, 0, 1, 0},      // temporal 3x1x1: 5.56 ms
 };
 
 }  // namespace c3d

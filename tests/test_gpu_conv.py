@@ -255,3 +255,36 @@ def test_cta_pair_kernel(pkg, case):
             os.environ.pop("CONV3D_PAIR", None)
         else:
             os.environ["CONV3D_PAIR"] = old
+
+
+@contextlib.contextmanager
+def env_vars(**kv):
+    old = {k: os.environ.get(k) for k in kv}
+    os.environ.update({k: str(v) for k, v in kv.items()})
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+# Two row sub-tiles per unit sharing each B stage, with and without CTA pairs.
+MSUB_CASES = [
+    ((2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1, "128,128,0,0,1"),
+    ((2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1, "256,128,0,0,1"),
+    ((1, 6, 10, 12, 32), (96, 3, 3, 3, 32), (1, 2, 1), (1, 1, 0), (2, 1, 1), "96,64,0,0,1"),
+    ((1, 5, 10, 70, 64), (200, 3, 1, 1, 64), 1, (1, 0, 0), 1, "224,128,0,0,1"),
+    ((900, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, 1, "160,128,0,0,1"),
+]
+
+
+@pytest.mark.parametrize("case", MSUB_CASES, ids=[str(i) for i in range(len(MSUB_CASES))])
+@pytest.mark.parametrize("pair", [0, 1])
+def test_two_row_subtiles(pkg, case, pair):
+    xs, ws, st, pa, di, spec = case
+    with env_vars(CONV3D_MSUB=2, CONV3D_PAIR=pair), forced_tile(spec):
+        _run_and_check(pkg, xs, ws, st, pa, di, seed=120 + MSUB_CASES.index(case),
+                       split_k=False, what=f"msub2 pair={pair} {case}")
