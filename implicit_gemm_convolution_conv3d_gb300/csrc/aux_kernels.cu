@@ -284,7 +284,64 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const __nv_bfloat16* __
     }
 }
 
+// ----------------------------------------------------------------- row repack
+// dst[r, 0:src_row_bytes) = src[r, :], dst[r, src_row_bytes:dst_row_bytes) = 0,
+// for two matrices in one launch (the point-output GEMM's A and B operands).
+// Gives operands whose rows are not 16-byte aligned a copy the TMA can tile.
+// Rows move in W-byte words (W = 8 when both pitches allow, else 4); the
+// grid strides over 32-word spans of all rows of both matrices, so every
+// warp keeps several rows' loads in flight.
+template <typename Word>
+__global__ void __launch_bounds__(256) row_repack_kernel(const Word* __restrict__ src0,
+                                                         Word* __restrict__ dst0, long long rows0,
+                                                         const Word* __restrict__ src1,
+                                                         Word* __restrict__ dst1, long long rows1,
+                                                         long long src_words, long long dst_words) {
+    const long long spans_per_row = (dst_words + 31) / 32;
+    const long long total = (rows0 + rows1) * spans_per_row;
+    const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (long long i = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         i < total; i += stride) {
+        long long r = i / spans_per_row;
+        const long long w = (i - r * spans_per_row) * 32 + lane;
+        const Word* src = src0;
+        Word* dst = dst0;
+        if (r >= rows0) {
+            r -= rows0;
+            src = src1;
+            dst = dst1;
+        }
+        if (w < dst_words) dst[r * dst_words + w] = w < src_words ? __ldg(src + r * src_words + w) : Word(0);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, const void* src1,
+                              void* dst1, long long rows1, long long src_row_bytes,
+                              long long dst_row_bytes, int num_sms, cudaStream_t stream) {
+    if (src_row_bytes % 4 || dst_row_bytes % 4 || dst_row_bytes < src_row_bytes)
+        return cudaErrorInvalidValue;
+    const int wb = (src_row_bytes % 8 == 0 && dst_row_bytes % 8 == 0) ? 8 : 4;
+    const long long dst_words = dst_row_bytes / wb;
+    const long long spans = (rows0 + rows1) * ((dst_words + 31) / 32);
+    long long blocks = (spans + 7) / 8;
+    const long long cap = static_cast<long long>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (wb == 8)
+        row_repack_kernel<unsigned long long><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const unsigned long long*>(src0), static_cast<unsigned long long*>(dst0),
+            rows0, static_cast<const unsigned long long*>(src1),
+            static_cast<unsigned long long*>(dst1), rows1, src_row_bytes / 8, dst_words);
+    else
+        row_repack_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint32_t*>(src0), static_cast<uint32_t*>(dst0), rows0,
+            static_cast<const uint32_t*>(src1), static_cast<uint32_t*>(dst1), rows1,
+            src_row_bytes / 4, dst_words);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
                                  const float* scale_x, const float* scale_w, int num_sms,

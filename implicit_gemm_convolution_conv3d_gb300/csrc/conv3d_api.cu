@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -165,7 +166,11 @@ struct Plan {
     int BN, BK, stages, splits, group_m;
     long long M;
     int m_tiles, n_tiles, k_steps, taps, steps_per_split, hw_tiles, HW;
-    long long g_row_bytes;   // GEMM classes: bytes of one A / B row
+    long long g_row_bytes;   // GEMM classes: bytes of one A / B row as the caller laid it out
+    long long tma_row_bytes; // GEMM classes: row pitch the TMA maps read (padded copy or caller's)
+    int repack;              // 1: A and B are first copied to 16-byte aligned rows in workspace
+    size_t repack_bytes;     // workspace bytes of those copies (A rows, then B rows)
+    size_t splitk_off;       // workspace offset of the split-K partials
     int grid;
     size_t smem;
     uint32_t tmem_cols;
@@ -175,18 +180,13 @@ struct Plan {
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
+// Bytes per k-step row: each k-step has a fixed issue cost, so the widest
+// step whose padded reduction stays within 25% of the tightest padding.
 int pick_bk(long long row_bytes) {
-    // bytes per k-step row: the choice that pads the channel / reduction run least
-    int best = 128;
-    long long best_pad = ((row_bytes + 127) / 128) * 128;
-    for (int bk : {64, 32}) {
-        const long long pad = ((row_bytes + bk - 1) / bk) * bk;
-        if (pad < best_pad) {
-            best = bk;
-            best_pad = pad;
-        }
-    }
-    return best;
+    long long tight = ((row_bytes + 31) / 32) * 32;
+    for (int bk : {128, 64})
+        if (((row_bytes + bk - 1) / bk) * bk * 4 <= tight * 5) return bk;
+    return 32;
 }
 
 // Tile columns: a tcgen05.mma of M=128 costs about the same issue time for
@@ -223,7 +223,10 @@ void force_tile(int* bn, int* bk, int* st, int* grp, int* spl) {
     if (v[4] > 0) *spl = v[4];
 }
 
-int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_split, Plan* P) {
+// ws_avail: workspace bytes the call can use (SIZE_MAX: plan the preferred
+// layout and report its size).  Split-K partials and the aligned operand
+// copies of the point-output GEMM are used only when they fit.
+int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_avail, Plan* P) {
     if (dtype != CONV_DTYPE_BF16 && dtype != CONV_DTYPE_FP8_E4M3) {
         set_error("unknown dtype");
         return CONV_ERR_INVALID;
@@ -242,11 +245,26 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
         P->M = point_output ? g.N : g.N * g.D * g.H * g.W;
         rg = point_output ? g.T * g.R * g.S * g.C : g.C;
         P->g_row_bytes = rg * elt;
-        if (P->g_row_bytes % 16 == 0)
+        P->tma_row_bytes = P->g_row_bytes;
+        if (P->g_row_bytes % 16 == 0) {
             P->amode = AM_GEMM_TMA;
-        else if (P->g_row_bytes % 4 == 0)
-            P->amode = AM_GEMM_GATHER;
-        else {
+        } else if (P->g_row_bytes % 4 == 0) {
+            // rows the TMA cannot address: copy both operands to 16-byte
+            // aligned, zero-padded rows when the workspace allows it (a
+            // short copy kernel, then TMA tiles), else gather with cp.async
+            const long long pitch = (P->g_row_bytes + 15) / 16 * 16;
+            const size_t a_bytes = static_cast<size_t>((P->M * pitch + 255) / 256 * 256);
+            const size_t b_bytes = static_cast<size_t>((g.K * pitch + 255) / 256 * 256);
+            const char* e = std::getenv("CONV3D_REPACK");
+            if (ws_avail >= a_bytes + b_bytes && !(e && e[0] == '0')) {
+                P->amode = AM_GEMM_TMA;
+                P->repack = 1;
+                P->repack_bytes = a_bytes + b_bytes;
+                P->tma_row_bytes = pitch;
+            } else {
+                P->amode = AM_GEMM_GATHER;
+            }
+        } else {
             set_error("point-output GEMM needs T*R*S*C*elem_bytes %% 4 == 0");
             return CONV_ERR_UNSUPPORTED;
         }
@@ -287,7 +305,9 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
 
     // tile defaults
     int BN = pick_bn(g.K);
-    int BK = (P->amode == AM_GEMM_GATHER) ? 128 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? rg * elt : g.C * elt);
+    int BK = (P->amode == AM_GEMM_GATHER)
+                 ? 128
+                 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? P->tma_row_bytes : g.C * elt);
     // raster group 1: a unit's row block meets every column tile before the
     // next row block starts (best on the measured workloads)
     int stages = 0, group_m = 1, splits = 0, pair_pref = -1, msub_pref = 0;
@@ -312,7 +332,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
 
     if (P->cls == CONV_CLASS_POINT_GEMM) {
         P->taps = 1;
-        P->k_steps = static_cast<int>((rg * elt + BK - 1) / BK);
+        P->k_steps = static_cast<int>((P->tma_row_bytes + BK - 1) / BK);
     } else {
         P->taps = static_cast<int>(g.T * g.R * g.S);
         const long long chunks = (g.C * elt + BK - 1) / BK;
@@ -340,11 +360,14 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, bool allow_s
     splits = std::max(1, std::min(splits, P->k_steps));
     P->steps_per_split = (P->k_steps + splits - 1) / splits;
     splits = (P->k_steps + P->steps_per_split - 1) / P->steps_per_split;
-    P->ws_bytes = splits > 1 ? static_cast<size_t>(splits) * P->M * g.K * sizeof(float) : 0;
-    if (splits > 1 && !allow_split) {
+    const size_t splitk_bytes =
+        splits > 1 ? static_cast<size_t>(splits) * P->M * g.K * sizeof(float) : 0;
+    P->splitk_off = P->repack_bytes;
+    if (splits > 1 && ws_avail < P->repack_bytes + splitk_bytes) {
         splits = 1;
         P->steps_per_split = P->k_steps;
     }
+    P->ws_bytes = P->repack_bytes + (splits > 1 ? splitk_bytes : 0);
     P->splits = splits;
     if (tiles * splits > 0x7FFFFFFFll) {
         set_error("too many work units");
@@ -470,9 +493,9 @@ int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtens
         return CONV_OK;
     }
     if (P.amode == AM_GEMM_TMA) {
-        const cuuint64_t rg = static_cast<cuuint64_t>(P.g_row_bytes) / elt;
+        const cuuint64_t rg = static_cast<cuuint64_t>(P.tma_row_bytes) / elt;
         const cuuint64_t adims[2] = {rg, static_cast<cuuint64_t>(P.M)};
-        const cuuint64_t astr[1] = {static_cast<cuuint64_t>(P.g_row_bytes)};
+        const cuuint64_t astr[1] = {static_cast<cuuint64_t>(P.tma_row_bytes)};
         const cuuint32_t abox[2] = {bke, static_cast<cuuint32_t>(kBM)};
         int rc = encode_tiled(tmA, P.fp8, 2, x, adims, astr, abox, P.BK);
         if (rc) return rc;
@@ -538,6 +561,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
+                              const int stride[3], const int pad[3], const int dil[3], int dtype) {
+    Geo g;
+    DeviceInfo* d = nullptr;
+    if (make_geo(x_dims, w_dims, stride, pad, dil, &g) || device_info(&d)) return 0;
+    Plan P;
+    if (make_plan(g, dtype, d->num_sms, d->smem_optin, SIZE_MAX, &P)) return 0;
+    return P.ws_bytes - P.repack_bytes;
+}
+
 void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof t_last_error, "%s", msg); }
 
 int* device_status_ptr() {
@@ -599,7 +632,7 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
         smem = d->smem_optin;
     }
     Plan P;
-    if ((rc = make_plan(g, dtype, sms, smem, true, &P))) return rc;
+    if ((rc = make_plan(g, dtype, sms, smem, SIZE_MAX, &P))) return rc;
     if (cls) *cls = P.cls;
     if (tile_n) *tile_n = P.BN;
     if (k_bytes) *k_bytes = P.BK;
@@ -634,12 +667,24 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
         return CONV_ERR_CUDA;
     }
     Plan P;
-    if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, true, &P))) return rc;
-    if (P.splits > 1 && (workspace == nullptr || workspace_bytes < P.ws_bytes)) {
-        if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, false, &P))) return rc;
+    if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace ? workspace_bytes : 0,
+                        &P)))
+        return rc;
+    const void* xa = x;
+    const void* wa = w;
+    if (P.repack) {
+        // aligned, zero-padded copies of the GEMM operands at the head of the workspace
+        unsigned char* wsb = static_cast<unsigned char*>(workspace);
+        void* xc = wsb;
+        void* wc = wsb + (P.M * P.tma_row_bytes + 255) / 256 * 256;
+        cudaError_t e = launch_row_repack(x, xc, P.M, w, wc, g.K, P.g_row_bytes, P.tma_row_bytes,
+                                          dev->num_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "row repack launch");
+        xa = xc;
+        wa = wc;
     }
     CUtensorMap tmA, tmB, tmC;
-    if ((rc = build_maps(g, P, x, w, &tmA, &tmB))) return rc;
+    if ((rc = build_maps(g, P, xa, wa, &tmA, &tmB))) return rc;
     if ((rc = build_out_map(g, P, out, &tmC))) return rc;
 
     KParams k;
@@ -678,7 +723,9 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.gb = static_cast<const unsigned char*>(w);
     k.g_row_bytes = P.g_row_bytes;
     k.out = out;
-    k.ws = P.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    k.ws = P.splits > 1
+               ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + P.splitk_off)
+               : nullptr;
     k.scale_x = scale_x;
     k.scale_w = scale_w;
     k.status = dev->status;

@@ -65,10 +65,12 @@ extern "C" int conv_fwd_noalloc(const void* x, const int64_t x_dims[5], const vo
                                 const int64_t w_dims[5], const int stride[3], const int pad[3],
                                 const int dil[3], int dtype, const float* scale_x,
                                 const float* scale_w, void* out, cudaStream_t stream) {
-    size_t need = 0;
     int rc = conv_fwd_plan(x_dims, w_dims, stride, pad, dil, dtype, 0, nullptr, nullptr, nullptr,
-                           nullptr, nullptr, nullptr, &need);
+                           nullptr, nullptr, nullptr, nullptr);
     if (rc != CONV_OK) return rc;
+    // only the split-K partials must fit; workspace uses that do not fit
+    // (aligned operand copies) are skipped by conv_fwd itself
+    const size_t need = c3d::splitk_workspace_bytes(x_dims, w_dims, stride, pad, dil, dtype);
     if (need > c3d::kNoallocScratchBytes) {
         char msg[160];
         std::snprintf(msg, sizeof msg,

@@ -74,6 +74,16 @@ cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int s
                                  const float* scale_x, const float* scale_w, int num_sms,
                                  cudaStream_t stream);
 
+// Row repack of two matrices with equal row pitches: copy rows of
+// src_row_bytes into rows of dst_row_bytes, zero-filling each row's tail.
+cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, const void* src1,
+                              void* dst1, long long rows1, long long src_row_bytes,
+                              long long dst_row_bytes, int num_sms, cudaStream_t stream);
+
+// Bytes of split-K partials the plan for this problem uses (0 without split-K).
+size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
+                              const int stride[3], const int pad[3], const int dil[3], int dtype);
+
 // Pack kernels.
 cudaError_t launch_amax_bf16(const void* in, long long n, unsigned int* amax_bits, int num_sms,
                              cudaStream_t stream);

@@ -23,6 +23,7 @@ static const TileEntry kTileTable[] = {
     {0, 0, 2048, 2048, 27, 100000, 1LL << 40, 256, 128, 0, 1, 0, 1, 0},   // video 3x3x3: 26.72 ms
     {1, 0, 1024, 1024, 9, 100000, 1LL << 40, 256, 128, 0, 2, 0, 1, 0},    // fp8 1x3x3: 9.68 ms
     {0, 1, 640, 640, 3, 100000, 1LL << 40, 224, 128, 0, 1, 0, 1, 0},      // temporal 3x1x1: 5.56 ms
+    {0, 2, 3, 1280, 196, 4096, 1LL << 40, 224, 128, 0, 1, 0, 1, 0},      // patch 14x14: 0.040 ms
 };
 
 }  // namespace c3d
