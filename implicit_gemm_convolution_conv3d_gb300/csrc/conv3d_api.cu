@@ -321,7 +321,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         msub_pref = e->msub;
     }
     force_tile(&BN, &BK, &stages, &group_m, &splits);
-    if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128) ||
+    if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128 || BK == 256) ||
         (P->amode == AM_GEMM_GATHER && BK != 128) || group_m < 1) {
         set_error("invalid tile override");
         return CONV_ERR_INVALID;
@@ -441,12 +441,16 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
 }
 
 // ------------------------------------------------------------ tensor maps
+// A 256-byte k-step is two 128-byte boxes per operand, each in the 128-byte
+// swizzle; narrower k-steps are one box whose row width sets the swizzle.
 CUtensorMapSwizzle swizzle_for(int bk) {
-    return bk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+    return bk >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                      : (bk == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-uint32_t desc_layout_for(int bk) { return bk == 128 ? 2u : (bk == 64 ? 4u : 6u); }
+uint32_t desc_layout_for(int bk) { return bk >= 128 ? 2u : (bk == 64 ? 4u : 6u); }
+
+int box_bytes(int bk) { return bk < 128 ? bk : 128; }
 
 int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuint64_t* dims,
                  const cuuint64_t* strides, const cuuint32_t* box, int bk) {
@@ -486,7 +490,8 @@ int build_out_map(const Geo& g, const Plan& P, void* out, CUtensorMap* tmC) {
 int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtensorMap* tmA,
                CUtensorMap* tmB) {
     const cuuint64_t elt = static_cast<cuuint64_t>(P.elt);
-    const cuuint32_t bke = static_cast<cuuint32_t>(P.BK / P.elt);
+    // elements of one box row (a 256-byte k-step loads two boxes)
+    const cuuint32_t bke = static_cast<cuuint32_t>(box_bytes(P.BK) / P.elt);
     if (P.amode == AM_GEMM_GATHER) {
         std::memset(tmA, 0, sizeof *tmA);
         std::memset(tmB, 0, sizeof *tmB);
@@ -714,7 +719,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
     k.idesc = make_idesc(P.fp8, P.BN, kBM << P.pair);
     k.layout = desc_layout_for(P.BK);
-    k.sbo = static_cast<uint32_t>(8 * P.BK);
+    k.sbo = static_cast<uint32_t>(8 * box_bytes(P.BK));
     k.tmem_cols = P.tmem_cols;
     k.epi_bytes = P.epi_bytes;
     k.pair = P.pair;

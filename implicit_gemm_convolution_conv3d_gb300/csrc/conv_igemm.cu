@@ -238,7 +238,9 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
 // tcgen05.mma over its 32-byte K slices into the tile's TMEM accumulator, and
 // commit the stage back to the producer; per tile, commit the accumulator to
 // the epilogue.  Shared-memory descriptors are built once and advanced by
-// adding encoded byte offsets (address field = bytes >> 4).
+// adding encoded byte offsets (address field = bytes >> 4).  A 256-byte
+// k-step (KMMA = 8) holds each operand as two 128-byte-swizzled boxes, one
+// after the other; slices 4..7 read the second box.
 template <int KMMA, int FP8, int PAIR, int MSUB>
 __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uint32_t full0,
                                            uint32_t empty0, uint32_t tfull0, uint32_t tempty0,
@@ -252,6 +254,8 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
     // accumulators (double-buffered when msub == 1)
     constexpr int nacc = 2 / MSUB;
     const uint32_t sub_step = (static_cast<uint32_t>(kBM) * p.BK) >> 4;   // A sub-tile, encoded
+    const uint32_t abox_step = (static_cast<uint32_t>(kBM) * 128u) >> 4;
+    const uint32_t bbox_step = (static_cast<uint32_t>(p.BN >> PAIR) * 128u) >> 4;
     int stage = 0, acc_iter = 0;
     uint32_t phase = 0, consumed = 0;
     for (int u = static_cast<int>(blockIdx.x) >> PAIR; u < total_units; u += gridDim.x >> PAIR) {
@@ -272,20 +276,22 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
             const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
 #pragma unroll
             for (int k = 0; k < KMMA; ++k) {
+                const int box = k >> 2, kin = k & 3;   // 128-byte box, 32-byte slice in it
+                const uint64_t b = bd + box * bbox_step + 2 * kin;
 #pragma unroll
                 for (int sub = 0; sub < MSUB; ++sub) {
                     const uint32_t d = d_tmem + static_cast<uint32_t>(sub * p.BN);
-                    const uint64_t a = ad + sub * sub_step + 2 * k;
+                    const uint64_t a = ad + sub * sub_step + box * abox_step + 2 * kin;
                     if (PAIR) {
                         if (FP8)
-                            tc_mma_f8_pair(d, a, bd + 2 * k, p.idesc, accum);
+                            tc_mma_f8_pair(d, a, b, p.idesc, accum);
                         else
-                            tc_mma_f16_pair(d, a, bd + 2 * k, p.idesc, accum);
+                            tc_mma_f16_pair(d, a, b, p.idesc, accum);
                     } else {
                         if (FP8)
-                            tc_mma_f8(d, a, bd + 2 * k, p.idesc, accum);
+                            tc_mma_f8(d, a, b, p.idesc, accum);
                         else
-                            tc_mma_f16(d, a, bd + 2 * k, p.idesc, accum);
+                            tc_mma_f16(d, a, b, p.idesc, accum);
                     }
                 }
                 accum = 1u;
@@ -310,8 +316,9 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
 
 // The TMA producer (one thread): per k-step, wait for a free stage, arm its
 // full barrier with the stage's bytes (both CTAs' in a pair) and issue the A
-// box of each of the MSUB row sub-tiles and the B box.
-template <int AMODE, int FP8, int PAIR, int MSUB>
+// boxes of each of the MSUB row sub-tiles and the B boxes: NB boxes of
+// 128-byte rows per operand for a 256-byte k-step, else one.
+template <int AMODE, int FP8, int PAIR, int MSUB, int NB>
 __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              const KParams& p, uint32_t tiles, uint32_t full0,
                                              uint32_t empty0, uint32_t* misc,
@@ -319,6 +326,9 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
     constexpr int kTileM = kBM << PAIR;
     constexpr int kElt = FP8 ? 1 : 2;
     const int bke = p.BK / kElt;
+    const int box_e = bke / NB;                                    // elements per box row
+    const uint32_t abox = static_cast<uint32_t>(kBM) * (p.BK / NB);            // A box bytes
+    const uint32_t bbox = static_cast<uint32_t>(p.BN >> PAIR) * (p.BK / NB);   // B box bytes
     const int total_units = p.m_tiles * p.n_tiles * p.splits;
     const int unit0 = static_cast<int>(blockIdx.x) >> PAIR;
     const int ustride = static_cast<int>(gridDim.x) >> PAIR;
@@ -380,44 +390,52 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
             const uint32_t adst0 = tiles + stage * p.stage_bytes;
             const uint32_t bdst = adst0 + p.a_stage_bytes;
             if (AMODE == AM_GEMM_TMA) {
-                for (int sub = 0; sub < MSUB; ++sub) {
-                    const uint32_t adst = adst0 + sub * kBM * p.BK;
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const int kj = k0 + j * box_e;
+                    for (int sub = 0; sub < MSUB; ++sub) {
+                        const uint32_t adst = adst0 + (sub * NB + j) * abox;
+                        if (PAIR)
+                            tma_load_2d_pair(adst, &tmA, fb, kj, am0[sub]);
+                        else
+                            tma_load_2d(adst, &tmA, fb, kj, am0[sub]);
+                    }
                     if (PAIR)
-                        tma_load_2d_pair(adst, &tmA, fb, k0, am0[sub]);
+                        tma_load_2d_pair(bdst + j * bbox, &tmB, fb, kj, n0);
                     else
-                        tma_load_2d(adst, &tmA, fb, k0, am0[sub]);
+                        tma_load_2d(bdst + j * bbox, &tmB, fb, kj, n0);
                 }
-                if (PAIR)
-                    tma_load_2d_pair(bdst, &tmB, fb, k0, n0);
-                else
-                    tma_load_2d(bdst, &tmB, fb, k0, n0);
                 k0 += bke;
             } else {
                 const uint16_t ow = static_cast<uint16_t>(fs * p.dw);
                 const uint16_t oh = static_cast<uint16_t>(fr * p.dh);
                 const uint16_t od = static_cast<uint16_t>(ft * p.dd);
-                for (int sub = 0; sub < MSUB; ++sub) {
-                    const uint32_t adst = adst0 + sub * kBM * p.BK;
-                    if (PAIR) {
-                        if (AMODE == AM_IM2COL)
-                            tma_load_im2col_5d_pair(adst, &tmA, fb, c0, aw[sub], ah[sub],
-                                                    ad[sub], an[sub], ow, oh, od);
-                        else
-                            tma_load_4d_pair(adst, &tmA, fb, c0, ah[sub], ad[sub] + ft * p.dd,
-                                             an[sub]);
-                    } else {
-                        if (AMODE == AM_IM2COL)
-                            tma_load_im2col_5d(adst, &tmA, fb, c0, aw[sub], ah[sub], ad[sub],
-                                               an[sub], ow, oh, od);
-                        else
-                            tma_load_4d(adst, &tmA, fb, c0, ah[sub], ad[sub] + ft * p.dd,
-                                        an[sub]);
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const int cj = c0 + j * box_e;   // channels past C read as zeros
+                    for (int sub = 0; sub < MSUB; ++sub) {
+                        const uint32_t adst = adst0 + (sub * NB + j) * abox;
+                        if (PAIR) {
+                            if (AMODE == AM_IM2COL)
+                                tma_load_im2col_5d_pair(adst, &tmA, fb, cj, aw[sub], ah[sub],
+                                                        ad[sub], an[sub], ow, oh, od);
+                            else
+                                tma_load_4d_pair(adst, &tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
+                                                 an[sub]);
+                        } else {
+                            if (AMODE == AM_IM2COL)
+                                tma_load_im2col_5d(adst, &tmA, fb, cj, aw[sub], ah[sub], ad[sub],
+                                                   an[sub], ow, oh, od);
+                            else
+                                tma_load_4d(adst, &tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
+                                            an[sub]);
+                        }
                     }
+                    if (PAIR)
+                        tma_load_3d_pair(bdst + j * bbox, &tmB, fb, cj, tap, n0);
+                    else
+                        tma_load_3d(bdst + j * bbox, &tmB, fb, cj, tap, n0);
                 }
-                if (PAIR)
-                    tma_load_3d_pair(bdst, &tmB, fb, c0, tap, n0);
-                else
-                    tma_load_3d(bdst, &tmB, fb, c0, tap, n0);
                 ++tap;
                 if (++fs == p.S) {
                     fs = 0;
@@ -531,12 +549,16 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         }
         // ------------------------------------------------------ TMA producer
         if (!kGather && lane == 0) {
-            if (p.msub == 2)
-                tma_producer<AMODE, FP8, PAIR, 2>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag,
-                                                  rank);
-            else
-                tma_producer<AMODE, FP8, PAIR, 1>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag,
-                                                  rank);
+#define C3D_PROD(MS, NBX) \
+    tma_producer<AMODE, FP8, PAIR, MS, NBX>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag, rank)
+            if (p.msub == 2) {
+                if (p.BK == 256) C3D_PROD(2, 2);
+                else C3D_PROD(2, 1);
+            } else {
+                if (p.BK == 256) C3D_PROD(1, 2);
+                else C3D_PROD(1, 1);
+            }
+#undef C3D_PROD
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -544,11 +566,13 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
 #define C3D_MMA(KM, MS) \
     mma_issuer<KM, FP8, PAIR, MS>(p, tiles, full0, empty0, tfull0, tempty0, tmem_base, misc, abort_flag)
             if (p.msub == 2) {
-                if (p.BK == 128) C3D_MMA(4, 2);
+                if (p.BK == 256) C3D_MMA(8, 2);
+                else if (p.BK == 128) C3D_MMA(4, 2);
                 else if (p.BK == 64) C3D_MMA(2, 2);
                 else C3D_MMA(1, 2);
             } else {
-                if (p.BK == 128) C3D_MMA(4, 1);
+                if (p.BK == 256) C3D_MMA(8, 1);
+                else if (p.BK == 128) C3D_MMA(4, 1);
                 else if (p.BK == 64) C3D_MMA(2, 1);
                 else C3D_MMA(1, 1);
             }

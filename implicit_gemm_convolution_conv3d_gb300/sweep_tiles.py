@@ -1,8 +1,9 @@
 """Measured tile sweep for conv_fwd: fills csrc/tile_table.h.
 
-For each workload, every candidate (BN, BK, stages, raster group, split-K)
-is forced through CONV3D_FORCE_TILE, timed with CUDA events (L2 flushed
-between runs), and the fastest legal one is printed as a tile-table row.
+For each workload, every candidate (BN, BK, stages, raster group, split-K,
+CTA pair, row sub-tiles) is forced through CONV3D_FORCE_TILE / CONV3D_PAIR /
+CONV3D_MSUB, timed with CUDA events (L2 flushed between runs), and the
+fastest legal one is printed as a tile-table row.
 Candidates whose plan is rejected are skipped.  Run on the GPU:
 
     python -m implicit_gemm_convolution_conv3d_gb300.sweep_tiles [--workloads a,b] [--quick]
@@ -30,17 +31,18 @@ CLASS_CODE = {"generic": 0, "temporal": 1, "point_gemm": 2}
 
 def candidates(quick: bool, K: int, k_row_bytes: int, default_bn: int):
     bns = [bn for bn in (256, 224, 192, 160, 128, 96, 64, 32) if bn <= max(32, ((K + 31) // 32) * 32)]
-    bks = [bk for bk in (128, 64, 32) if bk <= max(32, k_row_bytes)]
+    bks = [bk for bk in (256, 128, 64, 32) if bk <= max(32, k_row_bytes) or (bk == 256 and k_row_bytes > 128)]
     groups = [1, 2, 4, 8, 16, 32]
-    if quick:   # default tile width and k-step, every raster group and pair choice
-        bns, bks = [default_bn], [128 if k_row_bytes >= 128 else bks[0]]
-    for bn, bk, grp, pair in itertools.product(bns, bks, groups, (0, 1)):
-        yield bn, bk, 0, grp, 1, pair
+    if quick:   # default tile width, the two widest k-steps, small raster groups
+        bns, bks, groups = [default_bn], bks[:2], [1, 2, 4, 8]
+    for bn, bk, grp, pair, msub in itertools.product(bns, bks, groups, (0, 1), (1, 2)):
+        yield bn, bk, 0, grp, 1, pair, msub
 
 
-def time_case(x, w, wl, scale_x, scale_w, spec, flush, reps, pair):
+def time_case(x, w, wl, scale_x, scale_w, spec, flush, reps, pair, msub):
     os.environ["CONV3D_FORCE_TILE"] = spec
     os.environ["CONV3D_PAIR"] = str(pair)
+    os.environ["CONV3D_MSUB"] = str(msub)
     try:
         plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
                                  1 if x.dtype == torch.float8_e4m3fn else 0)
@@ -91,26 +93,27 @@ def main():
                                  1 if wl.dtype == "fp8" else 0)
         row_bytes = C * elt if base["class"] != "point_gemm" else T * R * S * C * elt
         results = []
-        for bn, bk, st, grp, spl, pair in candidates(args.quick, K, row_bytes, base["tile_n"]):
+        for bn, bk, st, grp, spl, pair, msub in candidates(args.quick, K, row_bytes,
+                                                           base["tile_n"]):
             spec = f"{bn},{bk},{st},{grp},{spl}"
-            ms, plan = time_case(x, w, wl, sx, sw, spec, flush, args.reps, pair)
+            ms, plan = time_case(x, w, wl, sx, sw, spec, flush, args.reps, pair, msub)
             if ms is None:
                 continue
             tf = 2.0 * cw_flops(wl) / (ms * 1e-3) / 1e12
-            results.append((ms, spec, plan, pair))
-            print(f"{name:26s} {spec:18s} pair={pair} {ms:9.4f} ms {tf:8.1f} TFLOPS "
+            results.append((ms, spec, plan, pair, msub))
+            print(f"{name:26s} {spec:18s} pair={pair} msub={msub} {ms:9.4f} ms {tf:8.1f} TFLOPS "
                   f"stages={plan['stages']}", flush=True)
-        os.environ.pop("CONV3D_FORCE_TILE", None)
-        os.environ.pop("CONV3D_PAIR", None)
+        for k in ("CONV3D_FORCE_TILE", "CONV3D_PAIR", "CONV3D_MSUB"):
+            os.environ.pop(k, None)
         results.sort(key=lambda r: r[0])
-        best_ms, best_spec, best_plan, best_pair = results[0]
+        best_ms, best_spec, best_plan, best_pair, best_msub = results[0]
         bn, bk, _, grp, spl = (int(v) for v in best_spec.split(","))
         M = best_plan_rows(wl)
         rows.append(f"    {{{1 if wl.dtype == 'fp8' else 0}, {CLASS_CODE[best_plan['class']]}, "
                     f"{C}, {K}, {T * R * S}, {M}, {M}, {bn}, {bk}, {best_plan['stages']}, {grp}, "
-                    f"{spl}, {best_pair}}},   // {name}: {best_ms:.3f} ms")
+                    f"{spl}, {best_pair}, {best_msub}}},   // {name}: {best_ms:.3f} ms")
         report[name] = {"best_ms": best_ms, "best": best_spec, "pair": best_pair,
-                        "all": [(r[0], r[1], r[3]) for r in results]}
+                        "msub": best_msub, "all": [(r[0], r[1], r[3], r[4]) for r in results]}
         del x, w
         torch.cuda.empty_cache()
     print("\n".join(rows))

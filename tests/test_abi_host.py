@@ -71,9 +71,9 @@ def test_plan_classifies_the_workloads(pkg):
     p = pkg.conv_fwd_plan((1, 15, 120, 120, 2048), (2048, 3, 3, 3, 2048), 1, 1, 1, 0, sms)
     assert p["class"] == "generic" and p["splits"] == 1 and p["ctas"] == sms
     p = pkg.conv_fwd_plan((1, 120, 160, 90, 1024), (1024, 1, 3, 3, 1024), 1, (0, 1, 1), 1, 1, sms)
-    assert p["class"] == "generic" and p["k_bytes"] == 128
+    assert p["class"] == "generic" and p["k_bytes"] == 256   # tile-table row: 256-byte k-steps
     p = pkg.conv_fwd_plan((1, 240, 160, 90, 640), (640, 3, 1, 1, 640), 1, (1, 0, 0), 1, 0, sms)
-    assert p["class"] == "temporal"
+    assert p["class"] == "temporal" and p["k_bytes"] == 256
     # pointwise 1x1x1 conv is a plain GEMM too
     p = pkg.conv_fwd_plan((2, 3, 4, 5, 64), (32, 1, 1, 1, 64), 1, 0, 1, 0, sms)
     assert p["class"] == "point_gemm"
@@ -108,10 +108,28 @@ def test_plan_tiles_are_legal(pkg):
                 assert dt == 1 and C % 16 != 0 and e.status == pkg.CONV_ERR_UNSUPPORTED
                 continue
             assert p["tile_n"] % 32 == 0 and 32 <= p["tile_n"] <= 256
-            assert p["k_bytes"] in (32, 64, 128)
+            assert p["k_bytes"] in (32, 64, 128, 256)
             assert 2 <= p["stages"] <= 8
             assert (p["tile_n"] * p["k_bytes"] + 128 * p["k_bytes"]) * p["stages"] + 1280 <= 232448
             assert 1 <= p["ctas"] <= 148
+
+
+def test_forced_wide_k_step_plans(pkg, monkeypatch):
+    """256-byte k-steps: accepted for every TMA operand mode, the reduction is
+    cut into ceil(row bytes / 256) chunks, and the pipeline fits in shared
+    memory; other k-step widths are rejected as invalid overrides."""
+    sms = 148
+    monkeypatch.setenv("CONV3D_FORCE_TILE", "128,256,0,1,1")
+    for xs, ws, st, pa, cls in [((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, "generic"),
+                                ((1, 5, 10, 50, 200), (200, 3, 1, 1, 200), 1, (1, 0, 0), "temporal"),
+                                ((600, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, "point_gemm")]:
+        p = pkg.conv_fwd_plan(xs, ws, st, pa, 1, 0, sms)
+        assert p["class"] == cls and p["k_bytes"] == 256 and p["stages"] >= 2
+        assert (128 * 256 + 128 * 256) * p["stages"] + 1280 <= 232448
+    monkeypatch.setenv("CONV3D_FORCE_TILE", "128,512,0,1,1")
+    with pytest.raises(pkg.ConvError) as e:
+        pkg.conv_fwd_plan((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, 1, 0, sms)
+    assert e.value.status == pkg.CONV_ERR_INVALID
 
 
 def test_invalid_and_unsupported_arguments(pkg):

@@ -288,3 +288,33 @@ def test_two_row_subtiles(pkg, case, pair):
     with env_vars(CONV3D_MSUB=2, CONV3D_PAIR=pair), forced_tile(spec):
         _run_and_check(pkg, xs, ws, st, pa, di, seed=120 + MSUB_CASES.index(case),
                        split_k=False, what=f"msub2 pair={pair} {case}")
+
+
+# 256-byte k-steps (two 128-byte swizzle boxes per operand and stage) with
+# reduction rows that end inside the first box, inside the second, or on a
+# k-step boundary, for every TMA operand mode, alone, paired and with two
+# row sub-tiles; the last case adds split-K.
+WIDE_K_CASES = [
+    ((2, 5, 9, 11, 136), (272, 3, 3, 3, 136), 1, 1, 1),                  # 272 B rows
+    ((1, 6, 10, 12, 256), (96, 3, 3, 3, 256), (1, 2, 1), (1, 1, 0), (2, 1, 1)),  # 512 B
+    ((1, 4, 7, 9, 40), (64, 3, 3, 3, 40), 1, 1, 1),                      # 80 B: one box part-filled
+    ((1, 5, 10, 50, 200), (200, 3, 1, 1, 200), 1, (1, 0, 0), 1),         # temporal, 400 B
+    ((1, 7, 9, 30, 64), (64, 3, 1, 1, 64), 1, (1, 0, 0), 1),             # temporal, 128 B
+    ((600, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, 1),           # point GEMM, 512 B
+    ((3, 4, 7, 9, 200), (256, 1, 1, 1, 200), 1, 0, 1),                   # pointwise, 400 B
+    ((300, 1, 14, 14, 3), (200, 1, 14, 14, 3), (1, 14, 14), 0, 1),       # repacked rows, 1184 B
+]
+WIDE_K_PLANS = [(0, 1, "128,256,0,0,1"), (1, 1, "224,256,0,0,1"), (0, 2, "96,256,0,0,1"),
+                (1, 2, "256,256,0,0,1"), (0, 1, "64,256,3,2,3")]
+
+
+@pytest.mark.parametrize("case", WIDE_K_CASES, ids=[str(i) for i in range(len(WIDE_K_CASES))])
+@pytest.mark.parametrize("plan", WIDE_K_PLANS, ids=[p[2] + f"-pair{p[0]}-msub{p[1]}"
+                                                    for p in WIDE_K_PLANS])
+def test_wide_k_steps(pkg, case, plan):
+    xs, ws, st, pa, di = case
+    pair, msub, spec = plan
+    with env_vars(CONV3D_MSUB=msub, CONV3D_PAIR=pair), forced_tile(spec):
+        assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["k_bytes"] == 256
+        _run_and_check(pkg, xs, ws, st, pa, di, seed=140 + WIDE_K_CASES.index(case),
+                       split_k=True, what=f"bk256 pair={pair} msub={msub} {spec} {case}")

@@ -6,6 +6,8 @@ bits.  The codec is exercised exhaustively: every finite bf16 pattern below a
 chosen amax, at several amax values.  The fp8 conv is compared with the
 oracle's conv of the very bytes the GPU pack produced (the fp8-cast conv
 reference), times both scales."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -121,3 +123,33 @@ def test_fp8_conv(pkg, case, split_k):
     ref = oracle.conv3d(bytes8(qx), bytes8(qw), pkg._triple(st), pkg._triple(pa), pkg._triple(di),
                         sx.item(), sw.item())
     assert_close(as_f64(y), ref, f"fp8 {case} split={split_k}")
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[str(i) for i in range(len(FP8_CASES))])
+@pytest.mark.parametrize("plan", [(0, "128,256,0,0,1"), (1, "256,256,0,0,1")],
+                         ids=["single", "pair"])
+def test_fp8_conv_wide_k_steps(pkg, case, plan):
+    """256-byte k-steps (two 128-byte boxes per operand) on the fp8 shapes,
+    whose channel rows end inside the first or second box."""
+    pair, spec = plan
+    xs, ws, st, pa, di, cls = case
+    crs = ws[1] * ws[2] * ws[3] * ws[4]
+    x = cw.randn_bf16(xs, 400 + FP8_CASES.index(case), 1.0, "cuda")
+    w = cw.randn_bf16(ws, 500 + FP8_CASES.index(case), 1.0 / np.sqrt(crs), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    old = {k: os.environ.get(k) for k in ("CONV3D_FORCE_TILE", "CONV3D_PAIR")}
+    os.environ.update({"CONV3D_FORCE_TILE": spec, "CONV3D_PAIR": str(pair)})
+    try:
+        assert pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), st, pa, di, 1)["k_bytes"] == 256
+        y = pkg.conv_fwd(qx, qw, st, pa, di, scale_x=sx, scale_w=sw)
+        torch.cuda.synchronize()
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    assert pkg.conv_get_device_status() == 0
+    ref = oracle.conv3d(bytes8(qx), bytes8(qw), pkg._triple(st), pkg._triple(pa), pkg._triple(di),
+                        sx.item(), sw.item())
+    assert_close(as_f64(y), ref, f"fp8 bk256 pair={pair} {case}")
