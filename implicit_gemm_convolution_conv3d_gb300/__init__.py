@@ -81,6 +81,10 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd_noalloc.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
                                          vp, vp, vp]
         lib.conv_fwd_noalloc.restype = ctypes.c_int
+        lib.conv_fwd_from_host.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int,
+                                           vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                           ctypes.c_int, vp]
+        lib.conv_fwd_from_host.restype = ctypes.c_int
         lib.pack_ncdhw_bf16_to_ndhwc.argtypes = [vp, i64p, vp, vp]
         lib.pack_ncdhw_bf16_to_ndhwc.restype = ctypes.c_int
         lib.pack_fp8_workspace_size.argtypes = []
@@ -238,6 +242,66 @@ def conv_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
                               _ptr(scale_w), out.data_ptr(), _stream_handle(stream))
     _check(rc, "conv_fwd_noalloc")
     return out
+
+
+def conv_fwd_from_host(x_host: torch.Tensor, w_host: torch.Tensor, stride=1, pad=0, dil=1,
+                       scale_x: Optional[torch.Tensor] = None,
+                       scale_w: Optional[torch.Tensor] = None,
+                       out_host: Optional[torch.Tensor] = None,
+                       x_dev: Optional[torch.Tensor] = None, w_dev: Optional[torch.Tensor] = None,
+                       out_dev: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, chunks: int = 0,
+                       stream: Optional[torch.cuda.Stream] = None,
+                       device: Optional[torch.device] = None) -> torch.Tensor:
+    """conv_fwd with x, w and the result in host memory (CPU tensors, pinned
+    for the copies to overlap the convolution): the output rows are computed
+    in slices whose input copies and output copies overlap the other slices'
+    kernels.  Device buffers of the operands' sizes (and a workspace when the
+    plan wants one) are taken from torch's allocator when not given.  Returns
+    ``out_host``; synchronise the stream before reading it."""
+    lib = load_library()
+    if x_host.dim() != 5 or w_host.dim() != 5:
+        raise ValueError("x must be [N,D,H,W,C] and w [K,T,R,S,C]")
+    for t in (x_host, w_host, out_host):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host operands must be contiguous CPU tensors")
+    dtype = _dtype_code(x_host)
+    if _dtype_code(w_host) != dtype:
+        raise TypeError("x and w must have the same dtype")
+    dev = torch.device(device) if device is not None else torch.device(
+        "cuda", torch.cuda.current_device())
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    od = conv_out_dims(tuple(x_host.shape), tuple(w_host.shape), st, pa, di)
+    if out_host is None:
+        out_host = torch.empty(od, dtype=torch.bfloat16, pin_memory=True)
+    elif tuple(out_host.shape) != od or out_host.dtype != torch.bfloat16:
+        raise ValueError(f"out_host must be bf16 {od}")
+    if x_dev is None:
+        x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+    if w_dev is None:
+        w_dev = torch.empty(w_host.shape, dtype=w_host.dtype, device=dev)
+    if out_dev is None:
+        out_dev = torch.empty(od, dtype=torch.bfloat16, device=dev)
+    for dv, h in ((x_dev, x_host), (w_dev, w_host), (out_dev, out_host)):
+        if dv.numel() * dv.element_size() != h.numel() * h.element_size():
+            raise ValueError("device buffers must match the host tensors' sizes")
+    _require_cuda(x_dev, w_dev, out_dev, scale_x, scale_w, workspace)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    else:
+        need = conv_fwd_plan(tuple(x_host.shape), tuple(w_host.shape), st, pa, di,
+                             dtype)["workspace_bytes"]
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            ws_ptr, ws_bytes = workspace.data_ptr(), need
+    rc = lib.conv_fwd_from_host(
+        x_host.data_ptr(), _I64_5(*x_host.shape), w_host.data_ptr(), _I64_5(*w_host.shape),
+        _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x), _ptr(scale_w),
+        out_host.data_ptr(), x_dev.data_ptr(), w_dev.data_ptr(), out_dev.data_ptr(), ws_ptr,
+        ws_bytes, int(chunks), _stream_handle(stream))
+    _check(rc, "conv_fwd_from_host")
+    return out_host
 
 
 def pack_ncdhw_bf16_to_ndhwc(x: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -564,6 +564,193 @@ uint32_t make_idesc(int fp8, int bn, int m) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Kernel parameters of plan P over the whole problem (m-tiles [0, m_tiles)).
+void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void* out,
+                 void* workspace, const float* scale_x, const float* scale_w, int* status,
+                 KParams* kp) {
+    KParams& k = *kp;
+    std::memset(&k, 0, sizeof k);
+    k.N = static_cast<int>(g.N); k.D = static_cast<int>(g.D); k.H = static_cast<int>(g.H);
+    k.W = static_cast<int>(g.W); k.C = static_cast<int>(g.C);
+    k.T = static_cast<int>(g.T); k.R = static_cast<int>(g.R); k.S = static_cast<int>(g.S);
+    k.Do = static_cast<int>(g.Do); k.Ho = static_cast<int>(g.Ho); k.Wo = static_cast<int>(g.Wo);
+    k.sd = g.sd; k.sh = g.sh; k.sw = g.sw; k.pd = g.pd; k.ph = g.ph; k.pw = g.pw;
+    k.dd = g.dd; k.dh = g.dh; k.dw = g.dw;
+    k.M = P.M;
+    k.K = static_cast<int>(g.K);
+    k.HW = P.HW;
+    k.hw_tiles = P.hw_tiles;
+    k.m_tiles = P.m_tiles;
+    k.n_tiles = P.n_tiles;
+    k.splits = P.splits;
+    k.m_tile0 = 0;
+    k.k_steps = P.k_steps;
+    k.steps_per_split = P.steps_per_split;
+    k.taps = P.taps;
+    k.group_m = P.group_m;
+    k.BN = P.BN;
+    k.BK = P.BK;
+    k.stages = P.stages;
+    k.a_stage_bytes = static_cast<uint32_t>(P.msub * kBM * P.BK);
+    k.b_stage_bytes = static_cast<uint32_t>((P.BN >> P.pair) * P.BK);
+    k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
+    k.idesc = make_idesc(P.fp8, P.BN, kBM << P.pair);
+    k.layout = desc_layout_for(P.BK);
+    k.sbo = static_cast<uint32_t>(8 * box_bytes(P.BK));
+    k.tmem_cols = P.tmem_cols;
+    k.epi_bytes = P.epi_bytes;
+    k.pair = P.pair;
+    k.msub = P.msub;
+    k.ga = static_cast<const unsigned char*>(x);
+    k.gb = static_cast<const unsigned char*>(w);
+    k.g_row_bytes = P.g_row_bytes;
+    k.out = out;
+    k.ws = P.splits > 1
+               ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + P.splitk_off)
+               : nullptr;
+    k.scale_x = scale_x;
+    k.scale_w = scale_w;
+    k.status = status;
+    k.wait_ns = g_wait_ns;
+}
+
+// ------------------------------------------------------------ host-operand pipeline
+// Per device: a copy-in and a copy-out stream and the events that order them
+// against the caller's stream.  Created on first use, kept until exit.
+constexpr int kMaxChunks = 32;
+struct Pipe {
+    bool ready;
+    cudaStream_t s_in, s_out;
+    cudaEvent_t start, in_done, out_done;
+    cudaEvent_t ev_in[kMaxChunks], ev_conv[kMaxChunks];
+    std::mutex mu;   // one enqueue at a time per device
+};
+Pipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex;
+
+int pipe_for_device(Pipe** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device ordinal out of range");
+        return CONV_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_pipe_mutex);
+    Pipe& p = g_pipe[dev];
+    if (!p.ready) {
+        if ((e = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreateWithFlags");
+        if ((e = cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking)) != cudaSuccess) {
+            cudaStreamDestroy(p.s_in);
+            return cuda_fail(e, "cudaStreamCreateWithFlags");
+        }
+        cudaEvent_t* evs[3 + 2 * kMaxChunks];
+        int n = 0;
+        evs[n++] = &p.start;
+        evs[n++] = &p.in_done;
+        evs[n++] = &p.out_done;
+        for (int i = 0; i < kMaxChunks; ++i) {
+            evs[n++] = &p.ev_in[i];
+            evs[n++] = &p.ev_conv[i];
+        }
+        for (int i = 0; i < n; ++i) {
+            if ((e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming)) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(*evs[j]);
+                cudaStreamDestroy(p.s_in);
+                cudaStreamDestroy(p.s_out);
+                return cuda_fail(e, "cudaEventCreateWithFlags");
+            }
+        }
+        p.ready = true;
+    }
+    *out = &p;
+    return CONV_OK;
+}
+
+// Output rows [first, last) computed by m-tile mt of plan P.
+long long tile_row_lo(const Plan& P, int mt) {
+    const long long unit_rows = static_cast<long long>(kBM << P.pair) * P.msub;
+    if (P.cls == CONV_CLASS_TEMPORAL) {
+        const long long plane = mt / P.hw_tiles, hwb = mt % P.hw_tiles;
+        return plane * P.HW + hwb * unit_rows;
+    }
+    return mt * unit_rows;
+}
+
+long long tile_row_hi(const Plan& P, int mt) {
+    const long long unit_rows = static_cast<long long>(kBM << P.pair) * P.msub;
+    if (P.cls == CONV_CLASS_TEMPORAL) {
+        const long long plane = mt / P.hw_tiles, hwb = mt % P.hw_tiles;
+        return plane * P.HW + std::min<long long>(P.HW, (hwb + 1) * unit_rows);
+    }
+    return std::min<long long>(P.M, (mt + 1) * unit_rows);
+}
+
+// Bytes of x, as a prefix of whole (n, d) planes, that the output rows below
+// row_hi read: the last output plane (n, od) reaches input depth
+// od*sd - pd + (T-1)*dd at most, and output planes are in (n, d) order.
+long long x_prefix_bytes(const Geo& g, long long row_hi, long long plane_bytes) {
+    const long long q = (row_hi - 1) / (g.Ho * g.Wo);
+    const long long n = q / g.Do, od = q % g.Do;
+    const long long d = std::min<long long>(od * g.sd - g.pd + (g.T - 1) * g.dd, g.D - 1);
+    const long long planes = d < 0 ? n * g.D : n * g.D + d + 1;
+    return planes * plane_bytes;
+}
+
+long long gcd_ll(long long a, long long b) {
+    while (b) {
+        const long long t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Split the m-tiles into chunks; bounds[0..n] (bounds[n] = m_tiles), returns n.
+// requested > 1: that many near-equal chunks.  requested == 0: chunks of
+// whole waves of units (a wave = the units the grid holds at once), so that
+// splitting the launch adds no partial waves: the first and last one block
+// long (short lead-in and tail), the rest shared evenly, at most 8 chunks.
+int plan_chunks(const Plan& P, int requested, int* bounds) {
+    const int MT = P.m_tiles;
+    bounds[0] = 0;
+    if (requested == 1 || MT < 2) {
+        bounds[1] = MT;
+        return 1;
+    }
+    if (requested > 1) {
+        const int n = std::min({requested, MT, kMaxChunks});
+        for (int i = 1; i <= n; ++i)
+            bounds[i] = static_cast<int>(static_cast<long long>(MT) * i / n);
+        return n;
+    }
+    const long long wave = P.grid >> P.pair;
+    const long long j = wave / gcd_ll(wave, P.n_tiles);   // m-tiles per block of whole waves
+    const long long nb = MT / j;
+    if (nb < 2) {
+        bounds[1] = MT;
+        return 1;
+    }
+    const int n = static_cast<int>(std::min<long long>(8, nb));
+    long long blocks[8];
+    blocks[0] = 1;
+    if (n == 2) {
+        blocks[1] = nb - 1;
+    } else {
+        blocks[n - 1] = 1;
+        const long long mid = nb - 2, parts = n - 2;
+        for (int i = 0; i < parts; ++i) blocks[1 + i] = mid / parts + (i < mid % parts ? 1 : 0);
+    }
+    long long acc = 0;
+    for (int i = 0; i < n; ++i) {
+        acc += blocks[i] * j;
+        bounds[i + 1] = static_cast<int>(acc);
+    }
+    bounds[n] = MT;   // the last chunk takes the m-tiles past whole blocks
+    return n;
+}
+
 }  // namespace
 
 size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
@@ -693,48 +880,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if ((rc = build_out_map(g, P, out, &tmC))) return rc;
 
     KParams k;
-    std::memset(&k, 0, sizeof k);
-    k.N = static_cast<int>(g.N); k.D = static_cast<int>(g.D); k.H = static_cast<int>(g.H);
-    k.W = static_cast<int>(g.W); k.C = static_cast<int>(g.C);
-    k.T = static_cast<int>(g.T); k.R = static_cast<int>(g.R); k.S = static_cast<int>(g.S);
-    k.Do = static_cast<int>(g.Do); k.Ho = static_cast<int>(g.Ho); k.Wo = static_cast<int>(g.Wo);
-    k.sd = g.sd; k.sh = g.sh; k.sw = g.sw; k.pd = g.pd; k.ph = g.ph; k.pw = g.pw;
-    k.dd = g.dd; k.dh = g.dh; k.dw = g.dw;
-    k.M = P.M;
-    k.K = static_cast<int>(g.K);
-    k.HW = P.HW;
-    k.hw_tiles = P.hw_tiles;
-    k.m_tiles = P.m_tiles;
-    k.n_tiles = P.n_tiles;
-    k.splits = P.splits;
-    k.k_steps = P.k_steps;
-    k.steps_per_split = P.steps_per_split;
-    k.taps = P.taps;
-    k.group_m = P.group_m;
-    k.BN = P.BN;
-    k.BK = P.BK;
-    k.stages = P.stages;
-    k.a_stage_bytes = static_cast<uint32_t>(P.msub * kBM * P.BK);
-    k.b_stage_bytes = static_cast<uint32_t>((P.BN >> P.pair) * P.BK);
-    k.stage_bytes = k.a_stage_bytes + k.b_stage_bytes;
-    k.idesc = make_idesc(P.fp8, P.BN, kBM << P.pair);
-    k.layout = desc_layout_for(P.BK);
-    k.sbo = static_cast<uint32_t>(8 * box_bytes(P.BK));
-    k.tmem_cols = P.tmem_cols;
-    k.epi_bytes = P.epi_bytes;
-    k.pair = P.pair;
-    k.msub = P.msub;
-    k.ga = static_cast<const unsigned char*>(x);
-    k.gb = static_cast<const unsigned char*>(w);
-    k.g_row_bytes = P.g_row_bytes;
-    k.out = out;
-    k.ws = P.splits > 1
-               ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + P.splitk_off)
-               : nullptr;
-    k.scale_x = scale_x;
-    k.scale_w = scale_w;
-    k.status = dev->status;
-    k.wait_ns = g_wait_ns;
+    fill_params(g, P, x, w, out, workspace, scale_x, scale_w, dev->status, &k);
 
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
@@ -750,6 +896,140 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
                                  stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }
+    return CONV_OK;
+}
+
+int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* w_host,
+                       const int64_t w_dims[5], const int stride[3], const int pad[3],
+                       const int dil[3], int dtype, const float* scale_x, const float* scale_w,
+                       void* out_host, void* x_dev, void* w_dev, void* out_dev, void* workspace,
+                       size_t workspace_bytes, int chunks, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!x_host || !w_host || !out_host || !x_dev || !w_dev || !out_dev) {
+        set_error("null tensor pointer");
+        return CONV_ERR_INVALID;
+    }
+    if (chunks < 0) {
+        set_error("chunks must be >= 0");
+        return CONV_ERR_INVALID;
+    }
+    if (!aligned16(x_dev) || !aligned16(w_dev) || !aligned16(out_dev) ||
+        (workspace && !aligned16(workspace))) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    if (!load_entry_points()) {
+        set_error("cuTensorMapEncode* entry points unavailable");
+        return CONV_ERR_CUDA;
+    }
+    Plan P;
+    if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace ? workspace_bytes : 0,
+                        &P)))
+        return rc;
+    const long long plane_bytes = g.H * g.W * g.C * P.elt;
+    const size_t x_bytes = static_cast<size_t>(g.N * g.D * plane_bytes);
+    const size_t w_bytes = static_cast<size_t>(g.K * g.T * g.R * g.S * g.C * P.elt);
+    const size_t row_bytes = static_cast<size_t>(g.K) * 2;   // one bf16 output row
+    const unsigned char* xh = static_cast<const unsigned char*>(x_host);
+    unsigned char* xd = static_cast<unsigned char*>(x_dev);
+    unsigned char* oh = static_cast<unsigned char*>(out_host);
+    const unsigned char* od = static_cast<const unsigned char*>(out_dev);
+
+    int bounds[kMaxChunks + 1];
+    const bool chunkable = P.cls != CONV_CLASS_POINT_GEMM && P.splits == 1;
+    const int n = chunkable ? plan_chunks(P, chunks, bounds) : 1;
+    cudaError_t e;
+    if (n == 1) {
+        // one launch: copy in, convolve, copy out, all on the caller's stream
+        if ((e = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, stream)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(w_dev, w_host, w_bytes, cudaMemcpyHostToDevice, stream)) !=
+                cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync (host to device)");
+        if ((rc = conv_fwd(x_dev, x_dims, w_dev, w_dims, stride, pad, dil, dtype, scale_x,
+                           scale_w, out_dev, workspace, workspace_bytes, stream)))
+            return rc;
+        if ((e = cudaMemcpyAsync(out_host, out_dev, static_cast<size_t>(P.M) * row_bytes,
+                                 cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync (device to host)");
+        return CONV_OK;
+    }
+
+    CUtensorMap tmA, tmB, tmC;
+    if ((rc = build_maps(g, P, x_dev, w_dev, &tmA, &tmB))) return rc;
+    if ((rc = build_out_map(g, P, out_dev, &tmC))) return rc;
+    KParams k;
+    fill_params(g, P, x_dev, w_dev, out_dev, workspace, scale_x, scale_w, dev->status, &k);
+
+    Pipe* pp = nullptr;
+    if ((rc = pipe_for_device(&pp))) return rc;
+    std::lock_guard<std::mutex> lk(pp->mu);
+    const char* what = nullptr;
+    // the copy streams start after the caller's earlier work
+    if ((e = cudaEventRecord(pp->start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(pp->s_in, pp->start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(pp->s_out, pp->start, 0)) != cudaSuccess)
+        return cuda_fail(e, "stream ordering");
+    if ((e = cudaMemcpyAsync(w_dev, w_host, w_bytes, cudaMemcpyHostToDevice, pp->s_in)) !=
+        cudaSuccess)
+        what = "cudaMemcpyAsync (weights)";
+    size_t x_done = 0;
+    for (int i = 0; i < n && !what; ++i) {
+        const int mt0 = bounds[i], mt1 = bounds[i + 1];
+        const long long row_lo = tile_row_lo(P, mt0), row_hi = tile_row_hi(P, mt1 - 1);
+        const size_t x_need =
+            i == n - 1 ? x_bytes : static_cast<size_t>(x_prefix_bytes(g, row_hi, plane_bytes));
+        if (x_need > x_done) {
+            if ((e = cudaMemcpyAsync(xd + x_done, xh + x_done, x_need - x_done,
+                                     cudaMemcpyHostToDevice, pp->s_in)) != cudaSuccess) {
+                what = "cudaMemcpyAsync (activation)";
+                break;
+            }
+            x_done = x_need;
+        }
+        if ((e = cudaEventRecord(pp->ev_in[i], pp->s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, pp->ev_in[i], 0)) != cudaSuccess) {
+            what = "stream ordering";
+            break;
+        }
+        k.m_tile0 = mt0;
+        k.m_tiles = mt1 - mt0;
+        const long long units = static_cast<long long>(k.m_tiles) * P.n_tiles;
+        const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
+                                : static_cast<int>(std::min<long long>(units, P.grid));
+        if (std::getenv("CONV3D_LOG"))
+            std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) rows [%lld, %lld) "
+                         "x prefix %zu B grid %d\n", i, mt0, mt1, row_lo, row_hi, x_done, grid);
+        if ((e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, grid, P.smem, stream)) !=
+            cudaSuccess) {
+            what = "conv kernel launch";
+            break;
+        }
+        if ((e = cudaEventRecord(pp->ev_conv[i], stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(pp->s_out, pp->ev_conv[i], 0)) != cudaSuccess) {
+            what = "stream ordering";
+            break;
+        }
+        if ((e = cudaMemcpyAsync(oh + row_lo * row_bytes, od + row_lo * row_bytes,
+                                 static_cast<size_t>(row_hi - row_lo) * row_bytes,
+                                 cudaMemcpyDeviceToHost, pp->s_out)) != cudaSuccess) {
+            what = "cudaMemcpyAsync (output)";
+            break;
+        }
+    }
+    // the caller's stream continues after both copy streams, also on failure
+    cudaError_t e2;
+    if ((e2 = cudaEventRecord(pp->in_done, pp->s_in)) != cudaSuccess ||
+        (e2 = cudaEventRecord(pp->out_done, pp->s_out)) != cudaSuccess ||
+        (e2 = cudaStreamWaitEvent(stream, pp->in_done, 0)) != cudaSuccess ||
+        (e2 = cudaStreamWaitEvent(stream, pp->out_done, 0)) != cudaSuccess) {
+        if (!what) return cuda_fail(e2, "stream ordering");
+    }
+    if (what) return cuda_fail(e, what);
     return CONV_OK;
 }
 

@@ -40,7 +40,8 @@ struct Unit {
 
 // Work unit -> (m-tile, n-tile, split).  Within a split, tiles are walked in
 // groups of `group_m` m-tiles: down M first, then across N, so that CTAs
-// running at the same time share both A rows and B columns in L2.
+// running at the same time share both A rows and B columns in L2.  A launch
+// covers the m-tiles [m_tile0, m_tile0 + m_tiles).
 __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     const int tiles = p.m_tiles * p.n_tiles;
     Unit r;
@@ -51,7 +52,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     const int first_m = g * p.group_m;
     const int gm = min(p.group_m, p.m_tiles - first_m);
     const int local = t - g * group;
-    r.m_tile = first_m + local % gm;
+    r.m_tile = p.m_tile0 + first_m + local % gm;
     r.n_tile = local / gm;
     return r;
 }
@@ -492,8 +493,6 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     const int ustride = static_cast<int>(gridDim.x) >> PAIR;
     constexpr int kTileM = kBM << PAIR;   // rows of a row sub-tile (a unit has msub of them)
     constexpr bool kGather = (AMODE == AM_GEMM_GATHER);
-    constexpr int kElt = FP8 ? 1 : 2;
-    const int bke = p.BK / kElt;   // elements of one row per k-step
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -542,7 +541,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 const long long n0 = static_cast<long long>(t.n_tile) * p.BN;
                 if (t.n_tile == 0 && t.split == 0)
                     prefetch_rows(p.ga, m0, min(m0 + kBM, p.M), p.g_row_bytes);
-                if (t.m_tile == 0 && t.split == 0)
+                if (t.m_tile == p.m_tile0 && t.split == 0)
                     prefetch_rows(p.gb, n0, min(n0 + p.BN, static_cast<long long>(p.K)),
                                   p.g_row_bytes);
             }
@@ -581,7 +580,6 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;   // TMEM lane quarter this warp may read
-        const int row = q * 32 + lane;
         float scale = 1.0f;
         if (p.scale_x) scale *= *p.scale_x;
         if (p.scale_w) scale *= *p.scale_w;

@@ -35,13 +35,14 @@ struct KParams {
     int HW;             // temporal: H*W rows per (n, d) plane
     int hw_tiles;       // temporal: ceil(HW / 128)
     int m_tiles, n_tiles, splits;
+    int m_tile0;        // first m-tile of this launch (launches over a range of m-tiles)
     int k_steps;        // k-steps of the whole reduction
     int steps_per_split;
     int taps;           // conv: T*R*S
     int group_m;        // raster: consecutive m-tiles per group
     // tile / pipeline shape (runtime)
     int BN;             // tile columns, multiple of 32, <= 256
-    int BK;             // bytes of one row per k-step: 32, 64 or 128
+    int BK;             // bytes of one row per k-step: 32, 64, 128 or 256
     int stages;
     uint32_t a_stage_bytes, b_stage_bytes, stage_bytes;
     uint32_t idesc;     // tcgen05 instruction descriptor

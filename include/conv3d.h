@@ -22,12 +22,14 @@
  *     device pointer must be 16-byte aligned.
  *   - The caller owns and allocates every buffer (inputs, outputs, scales,
  *     workspace).  The library never allocates or frees caller memory.  It
- *     keeps only a per-device status word and per-process host state
- *     (function pointers, device attributes).
+ *     keeps only a per-device status word, per-process host state
+ *     (function pointers, device attributes) and, once conv_fwd_from_host
+ *     has run on a device, two copy streams and a set of events there.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do
  *     not synchronise the host, except conv_get_device_status.
  *   - Every function returns a conv_status; no exception crosses the ABI.
- *     On any non-OK return nothing has been launched.
+ *     On any non-OK return nothing has been launched (conv_fwd_from_host:
+ *     see there).
  *   - Shapes are int64; tensors above 2^31 elements (and 2^32 bytes) are
  *     supported; each single dimension must be below 2^31.
  */
@@ -105,6 +107,40 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
              const int stride[3], const int pad[3], const int dil[3], int dtype,
              const float* scale_x, const float* scale_w, void* out, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
+
+/* conv_fwd with the operands and the result in HOST memory: the same
+ * convolution (same definition and plan as conv_fwd, so the same output
+ * bits), with the host->device copies of x and w and the device->host copy
+ * of out overlapped with the convolution.
+ *   x_host, w_host    host, NDHWC / KTRSC as for conv_fwd (page-locked for
+ *                     the copies to overlap; pageable memory works, serially)
+ *   out_host          host, NDHWC [N,Do,Ho,Wo,K] bf16; fully overwritten
+ *   x_dev, w_dev, out_dev  device buffers of the same sizes (caller-owned,
+ *                     16-byte aligned); on completion they hold copies of
+ *                     x, w and out
+ *   scale_x, scale_w  device pointers or NULL, as for conv_fwd
+ *   workspace, workspace_bytes  as for conv_fwd
+ *   chunks            0: automatic; 1: no overlap; n > 1: n slices (<= 32)
+ * The output rows are cut into slices of whole waves of work units.  Slice
+ * i's input planes ((n, d) planes of x, a growing prefix) are copied on a
+ * library-owned copy-in stream, the kernel for slice i's output rows runs on
+ * `stream` once they have landed, and slice i's output rows go back on a
+ * copy-out stream while slice i+1 computes.  The weights are copied first.
+ * Work queued on `stream` before the call runs before the copies; work
+ * queued after it runs after the last copy: synchronise `stream` before
+ * reading out_host.  Point-output GEMM and split-K plans run unsliced (copy
+ * in, conv_fwd, copy out on `stream`).  The first call on a device creates
+ * the two copy streams and the events with that device current.  Calls on
+ * one device are enqueued one at a time (a lock); their copies share the
+ * copy streams.  If an enqueue step fails after earlier steps were queued,
+ * the call returns the error with `stream` still ordered after whatever was
+ * queued.  The pages of the method have no counterpart: it is the measured
+ * end-to-end path from host operands. */
+int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* w_host,
+                       const int64_t w_dims[5], const int stride[3], const int pad[3],
+                       const int dil[3], int dtype, const float* scale_x, const float* scale_w,
+                       void* out_host, void* x_dev, void* w_dev, void* out_dev, void* workspace,
+                       size_t workspace_bytes, int chunks, cudaStream_t stream);
 
 /* Layout pack: out[n,d,h,w,c] = in[n,c,d,h,w] (bit copy).
  *   in   device, bf16 NCDHW, dims = {N, C, D, H, W}

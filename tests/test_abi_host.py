@@ -34,7 +34,8 @@ def _declared_functions():
 def test_header_declares_the_abi():
     names = _declared_functions()
     for must in ("conv_fwd", "pack_ncdhw_bf16_to_ndhwc", "pack_ncdhw_bf16_to_ndhwc_fp8",
-                 "conv_out_dims", "conv_fwd_plan", "conv_get_device_status"):
+                 "conv_out_dims", "conv_fwd_plan", "conv_get_device_status",
+                 "conv_fwd_from_host"):
         assert must in names
 
 
@@ -153,3 +154,24 @@ def test_invalid_and_unsupported_arguments(pkg):
     lib.conv_status_string.restype = ctypes.c_char_p
     for s in range(5):
         assert lib.conv_status_string(s).startswith(b"CONV_")
+
+
+def test_from_host_argument_checks(pkg):
+    """conv_fwd_from_host rejects null operands, a negative slice count and
+    misaligned device buffers before touching the device."""
+    lib = ctypes.CDLL(pkg.LIB_PATH)
+    lib.conv_fwd_from_host.restype = ctypes.c_int
+    I5, I3 = ctypes.c_int64 * 5, ctypes.c_int * 3
+    xd, wd, st = I5(1, 4, 8, 8, 16), I5(32, 3, 3, 3, 16), I3(1, 1, 1)
+    host = (ctypes.c_uint8 * 64)()
+    hp = ctypes.cast(host, ctypes.c_void_p)
+    good, odd = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 8)
+
+    def call(x_host, x_dev, chunks):
+        return lib.conv_fwd_from_host(x_host, xd, hp, wd, st, st, st, 0, None, None, hp, x_dev,
+                                      good, good, None, ctypes.c_size_t(0), chunks, None)
+
+    assert call(None, good, 0) == pkg.CONV_ERR_INVALID
+    assert call(hp, None, 0) == pkg.CONV_ERR_INVALID
+    assert call(hp, good, -1) == pkg.CONV_ERR_INVALID
+    assert call(hp, odd, 0) == pkg.CONV_ERR_INVALID
