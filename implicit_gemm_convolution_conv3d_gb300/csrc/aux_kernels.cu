@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace c3d {
 
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restri
                                                    const unsigned int* amax_bits,
                                                    float* scale_out, long long c_tiles,
                                                    long long s_tiles) {
+    griddep_launch_dependents();   // the conv reading this output waits for completion
     __shared__ __align__(16) unsigned short tile[kPackC * kPitch];
     const long long b = blockIdx.x;
     const long long st = b % s_tiles;
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const __nv_bfloat16* __
                                                          const unsigned int* amax_bits,
                                                          float* scale_out, long long c_tiles,
                                                          long long s_tiles, long long tiles) {
+    griddep_launch_dependents();   // the conv reading this output waits for completion
     float scale = 1.0f;
     if (FP8) {
         scale = fp8_scale_of(amax_bits);
@@ -286,33 +289,64 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const __nv_bfloat16* __
 
 // ----------------------------------------------------------------- row repack
 // dst[r, 0:src_row_bytes) = src[r, :], dst[r, src_row_bytes:dst_row_bytes) = 0,
-// for two matrices in one launch (the point-output GEMM's A and B operands).
+// for two matrices in one launch (the point-output GEMM's A and B operands),
+// matrix 1's rows optionally shifted right by shift1 words (zeros in front).
 // Gives operands whose rows are not 16-byte aligned a copy the TMA can tile.
-// Rows move in W-byte words (W = 8 when both pitches allow, else 4); the
-// grid strides over 32-word spans of all rows of both matrices, so every
-// warp keeps several rows' loads in flight.
+// Rows move in W-byte words (W = 8 when both pitches allow, else 4).  Each
+// warp copies two rows at a time in spans of 256 words: all loads of both
+// rows' span are issued before any store, so a lane keeps up to 16 loads in
+// flight.  The kernel lets a dependent launch start early (the GEMM it feeds
+// waits for this grid's completion before reading).
 template <typename Word>
 __global__ void __launch_bounds__(256) row_repack_kernel(const Word* __restrict__ src0,
                                                          Word* __restrict__ dst0, long long rows0,
                                                          const Word* __restrict__ src1,
                                                          Word* __restrict__ dst1, long long rows1,
-                                                         long long src_words, long long dst_words) {
-    const long long spans_per_row = (dst_words + 31) / 32;
-    const long long total = (rows0 + rows1) * spans_per_row;
-    const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+                                                         long long src_words, long long dst_words,
+                                                         long long shift1) {
+    griddep_launch_dependents();
+    constexpr int kPer = 8;   // words per lane per row and span
     const int lane = threadIdx.x & 31;
-    for (long long i = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         i < total; i += stride) {
-        long long r = i / spans_per_row;
-        const long long w = (i - r * spans_per_row) * 32 + lane;
-        const Word* src = src0;
-        Word* dst = dst0;
-        if (r >= rows0) {
-            r -= rows0;
-            src = src1;
-            dst = dst1;
+    const long long total = rows0 + rows1;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long warp = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (long long r0 = 2 * warp; r0 < total; r0 += 2 * nwarps) {
+        const Word* src[2];
+        Word* dst[2];
+        bool live[2];
+        long long sh[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            long long r = r0 + h;
+            live[h] = r < total;
+            if (r >= rows0) {
+                r -= rows0;
+                src[h] = src1 + r * src_words;
+                dst[h] = dst1 + r * dst_words;
+                sh[h] = shift1;
+            } else {
+                src[h] = src0 + r * src_words;
+                dst[h] = dst0 + r * dst_words;
+                sh[h] = 0;
+            }
         }
-        if (w < dst_words) dst[r * dst_words + w] = w < src_words ? __ldg(src + r * src_words + w) : Word(0);
+        for (long long base = 0; base < dst_words; base += 32 * kPer) {
+            Word v[2][kPer];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const long long w = base + lane + 32 * i - sh[h];   // source word
+                    v[h][i] = (live[h] && w >= 0 && w < src_words) ? __ldg(src[h] + w) : Word(0);
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const long long w = base + lane + 32 * i;
+                    if (live[h] && w < dst_words) dst[h][w] = v[h][i];
+                }
+        }
     }
 }
 
@@ -320,26 +354,31 @@ __global__ void __launch_bounds__(256) row_repack_kernel(const Word* __restrict_
 
 cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, const void* src1,
                               void* dst1, long long rows1, long long src_row_bytes,
-                              long long dst_row_bytes, int num_sms, cudaStream_t stream) {
-    if (src_row_bytes % 4 || dst_row_bytes % 4 || dst_row_bytes < src_row_bytes)
+                              long long dst_row_bytes, long long dst1_shift_bytes, int num_sms,
+                              cudaStream_t stream) {
+    if (src_row_bytes % 4 || dst_row_bytes % 4 || dst1_shift_bytes % 4 || dst1_shift_bytes < 0 ||
+        dst_row_bytes < src_row_bytes + dst1_shift_bytes)
         return cudaErrorInvalidValue;
-    const int wb = (src_row_bytes % 8 == 0 && dst_row_bytes % 8 == 0) ? 8 : 4;
+    const int wb =
+        (src_row_bytes % 8 == 0 && dst_row_bytes % 8 == 0 && dst1_shift_bytes % 8 == 0) ? 8 : 4;
     const long long dst_words = dst_row_bytes / wb;
-    const long long spans = (rows0 + rows1) * ((dst_words + 31) / 32);
-    long long blocks = (spans + 7) / 8;
-    const long long cap = static_cast<long long>(num_sms) * 16;
+    // two rows per warp, 8 warps per block; at most 4 blocks per SM so that
+    // the dependent GEMM's CTAs find room as soon as they are launched
+    long long blocks = (rows0 + rows1 + 15) / 16;
+    const long long cap = static_cast<long long>(num_sms) * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (wb == 8)
         row_repack_kernel<unsigned long long><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const unsigned long long*>(src0), static_cast<unsigned long long*>(dst0),
             rows0, static_cast<const unsigned long long*>(src1),
-            static_cast<unsigned long long*>(dst1), rows1, src_row_bytes / 8, dst_words);
+            static_cast<unsigned long long*>(dst1), rows1, src_row_bytes / 8, dst_words,
+            dst1_shift_bytes / 8);
     else
         row_repack_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const uint32_t*>(src0), static_cast<uint32_t*>(dst0), rows0,
             static_cast<const uint32_t*>(src1), static_cast<uint32_t*>(dst1), rows1,
-            src_row_bytes / 4, dst_words);
+            src_row_bytes / 4, dst_words, dst1_shift_bytes / 4);
     return cudaGetLastError();
 }
 

@@ -170,6 +170,9 @@ struct Plan {
     long long tma_row_bytes; // GEMM classes: row pitch the TMA maps read (padded copy or caller's)
     int repack;              // 1: A and B are first copied to 16-byte aligned rows in workspace
     size_t repack_bytes;     // workspace bytes of those copies (A rows, then B rows)
+    int phases;              // 2: A rows alternate 16-byte aligned / 8 bytes past (two-phase GEMM)
+    int mt_phase0;           // m-tiles of phase 0 (all m-tiles when phases == 1)
+    long long rows0, rows1;  // GEMM rows of phase 0 / phase 1
     size_t splitk_off;       // workspace offset of the split-K partials
     int grid;
     size_t smem;
@@ -246,8 +249,25 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         rg = point_output ? g.T * g.R * g.S * g.C : g.C;
         P->g_row_bytes = rg * elt;
         P->tma_row_bytes = P->g_row_bytes;
+        const char* ph = std::getenv("CONV3D_PHASES");
         if (P->g_row_bytes % 16 == 0) {
             P->amode = AM_GEMM_TMA;
+        } else if (P->g_row_bytes % 16 == 8 && P->M >= 2 && !(ph && ph[0] == '1') &&
+                   ws_avail >= 2 * static_cast<size_t>((g.K * (P->g_row_bytes + 8) + 255) / 256 * 256)) {
+            // rows of g_row_bytes = 16q + 8: even rows start 16-byte aligned, odd
+            // rows 8 bytes past a boundary.  Two row phases, each a TMA-tiled
+            // GEMM over the caller's x: phase 0 reads even rows in place, phase 1
+            // odd rows from 8 bytes earlier (the previous row's last 8 bytes)
+            // against a weight copy shifted right by 8 zero bytes, which cancels
+            // them.  Only the weights are copied (twice, to 16-byte rows).
+            P->amode = AM_GEMM_TMA;
+            P->phases = 2;
+            P->repack = 1;
+            P->tma_row_bytes = P->g_row_bytes + 8;
+            P->repack_bytes =
+                2 * static_cast<size_t>((g.K * P->tma_row_bytes + 255) / 256 * 256);
+            P->rows0 = (P->M + 1) / 2;
+            P->rows1 = P->M / 2;
         } else if (P->g_row_bytes % 4 == 0) {
             // rows the TMA cannot address: copy both operands to 16-byte
             // aligned, zero-padded rows when the workspace allows it (a
@@ -338,13 +358,23 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         const long long chunks = (g.C * elt + BK - 1) / BK;
         P->k_steps = static_cast<int>(chunks * P->taps);
     }
+    if (P->phases != 2) {
+        P->phases = 1;
+        P->rows0 = P->M;
+        P->rows1 = 0;
+    }
     auto set_m_tiles = [&](int tile_m) {
         if (P->cls == CONV_CLASS_TEMPORAL) {
             P->HW = static_cast<int>(g.H * g.W);
             P->hw_tiles = (P->HW + tile_m - 1) / tile_m;
             P->m_tiles = static_cast<int>(g.N * g.Do * P->hw_tiles);
+            P->mt_phase0 = P->m_tiles;
+        } else if (P->phases == 2) {
+            P->mt_phase0 = static_cast<int>((P->rows0 + tile_m - 1) / tile_m);
+            P->m_tiles = P->mt_phase0 + static_cast<int>((P->rows1 + tile_m - 1) / tile_m);
         } else {
             P->m_tiles = static_cast<int>((P->M + tile_m - 1) / tile_m);
+            P->mt_phase0 = P->m_tiles;
         }
     };
     set_m_tiles(kBM);
@@ -409,11 +439,16 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         }
     }
 
-    // bf16 output leaves through TMA stores when its rows are 16-byte aligned;
-    // split-K partials are written directly
-    // (the short point-output GEMM tiles keep the lighter direct stores)
-    P->epi_bytes = (splits == 1 && g.K % 8 == 0 && P->cls != CONV_CLASS_POINT_GEMM)
-                       ? kEpiStageBytes : 0u;
+    // bf16 output leaves through TMA stores when its rows are 16-byte aligned
+    // (a warp's 32 rows x 64 bytes per store, where direct stores would send
+    // 32 separate 16-byte pieces per instruction); split-K partials are
+    // written directly
+    P->epi_bytes = (splits == 1 && g.K % 8 == 0) ? kEpiStageBytes : 0u;
+    // CONV3D_EPI=tma / direct overrides the epilogue kind (for sweeps)
+    if (const char* e = std::getenv("CONV3D_EPI")) {
+        if (e[0] == 't' && splits == 1 && g.K % 8 == 0) P->epi_bytes = kEpiStageBytes;
+        if (e[0] == 'd') P->epi_bytes = 0u;
+    }
     // pipeline depth from the shared-memory budget (a pair CTA holds half of B)
     const size_t stage_bytes = static_cast<size_t>(P->msub * kBM + (BN >> P->pair)) * BK;
     const size_t fixed = 1024 + 256 + P->epi_bytes;
@@ -469,8 +504,8 @@ int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuin
 // Output map for the TMA-store epilogue: [M, K] bf16 rows (or, for the
 // temporal class, [N*Do planes, H*W, K] so stores clip at each plane's edge),
 // 32x32 boxes with the 64-byte swizzle the epilogue writes.
-int build_out_map(const Geo& g, const Plan& P, void* out, CUtensorMap* tmC) {
-    std::memset(tmC, 0, sizeof *tmC);
+int build_out_map(const Geo& g, const Plan& P, void* out, TMaps* tm) {
+    std::memset(tm->c, 0, sizeof tm->c);
     if (!P.epi_bytes) return CONV_OK;
     const cuuint64_t row = static_cast<cuuint64_t>(g.K) * 2;
     if (P.amode == AM_TEMPORAL) {
@@ -479,22 +514,52 @@ int build_out_map(const Geo& g, const Plan& P, void* out, CUtensorMap* tmC) {
                                     static_cast<cuuint64_t>(g.N * g.Do)};
         const cuuint64_t str[2] = {row, row * hw};
         const cuuint32_t box[3] = {32, 32, 1};
-        return encode_tiled(tmC, 0, 3, out, dims, str, box, 64);
+        return encode_tiled(&tm->c[0], 0, 3, out, dims, str, box, 64);
     }
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(P.M)};
-    const cuuint64_t str[1] = {row};
-    const cuuint32_t box[2] = {32, 32};
-    return encode_tiled(tmC, 0, 2, out, dims, str, box, 64);
+    // phase j's output rows are rows j, j + phases, ... of out
+    for (int j = 0; j < P.phases; ++j) {
+        const cuuint64_t rows = static_cast<cuuint64_t>(j ? P.rows1 : P.rows0);
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), rows};
+        const cuuint64_t str[1] = {row * static_cast<cuuint64_t>(P.phases)};
+        const cuuint32_t box[2] = {32, 32};
+        int rc = encode_tiled(&tm->c[j], 0, 2, static_cast<unsigned char*>(out) + j * row, dims,
+                              str, box, 64);
+        if (rc) return rc;
+    }
+    return CONV_OK;
 }
 
-int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, CUtensorMap* tmA,
-               CUtensorMap* tmB) {
+int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, TMaps* tm) {
+    CUtensorMap* tmA = &tm->a[0];
+    CUtensorMap* tmB = &tm->b[0];
+    std::memset(tm->a, 0, sizeof tm->a);
+    std::memset(tm->b, 0, sizeof tm->b);
     const cuuint64_t elt = static_cast<cuuint64_t>(P.elt);
     // elements of one box row (a 256-byte k-step loads two boxes)
     const cuuint32_t bke = static_cast<cuuint32_t>(box_bytes(P.BK) / P.elt);
-    if (P.amode == AM_GEMM_GATHER) {
-        std::memset(tmA, 0, sizeof *tmA);
-        std::memset(tmB, 0, sizeof *tmB);
+    if (P.amode == AM_GEMM_GATHER) return CONV_OK;
+    if (P.amode == AM_GEMM_TMA && P.phases == 2) {
+        // x as given: phase j's rows start j*(row - 8) bytes into x, 2*row
+        // bytes apart, (row + 8*j) bytes long; w: the two aligned copies
+        // (plain, and shifted right by 8 zero bytes) in the workspace
+        const cuuint64_t rb = static_cast<cuuint64_t>(P.g_row_bytes);
+        const cuuint64_t pitch = static_cast<cuuint64_t>(P.tma_row_bytes);
+        const unsigned char* xb = static_cast<const unsigned char*>(x);
+        const unsigned char* wb = static_cast<const unsigned char*>(w);
+        const size_t wcopy = static_cast<size_t>((g.K * P.tma_row_bytes + 255) / 256 * 256);
+        for (int j = 0; j < 2; ++j) {
+            const cuuint64_t adims[2] = {(rb + 8 * j) / elt,
+                                         static_cast<cuuint64_t>(j ? P.rows1 : P.rows0)};
+            const cuuint64_t astr[1] = {2 * rb};
+            const cuuint32_t abox[2] = {bke, static_cast<cuuint32_t>(kBM)};
+            int rc = encode_tiled(&tm->a[j], P.fp8, 2, xb + j * (rb - 8), adims, astr, abox, P.BK);
+            if (rc) return rc;
+            const cuuint64_t bdims[2] = {pitch / elt, static_cast<cuuint64_t>(g.K)};
+            const cuuint64_t bstr[1] = {pitch};
+            const cuuint32_t bbox[2] = {bke, static_cast<cuuint32_t>(P.BN >> P.pair)};
+            rc = encode_tiled(&tm->b[j], P.fp8, 2, wb + j * wcopy, bdims, bstr, bbox, P.BK);
+            if (rc) return rc;
+        }
         return CONV_OK;
     }
     if (P.amode == AM_GEMM_TMA) {
@@ -584,6 +649,10 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.n_tiles = P.n_tiles;
     k.splits = P.splits;
     k.m_tile0 = 0;
+    k.phases = P.phases;
+    k.mt_phase0 = P.mt_phase0;
+    k.rows0 = P.rows0;
+    k.rows1 = P.rows1;
     k.k_steps = P.k_steps;
     k.steps_per_split = P.steps_per_split;
     k.taps = P.taps;
@@ -864,20 +933,29 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
         return rc;
     const void* xa = x;
     const void* wa = w;
-    if (P.repack) {
+    if (P.repack && P.phases == 2) {
+        // the two aligned weight copies (plain, shifted by 8 bytes) at the head
+        // of the workspace; x is read in place
+        unsigned char* wsb = static_cast<unsigned char*>(workspace);
+        void* w1 = wsb + (g.K * P.tma_row_bytes + 255) / 256 * 256;
+        cudaError_t e = launch_row_repack(w, wsb, g.K, w, w1, g.K, P.g_row_bytes, P.tma_row_bytes,
+                                          8, dev->num_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "row repack launch");
+        wa = wsb;
+    } else if (P.repack) {
         // aligned, zero-padded copies of the GEMM operands at the head of the workspace
         unsigned char* wsb = static_cast<unsigned char*>(workspace);
         void* xc = wsb;
         void* wc = wsb + (P.M * P.tma_row_bytes + 255) / 256 * 256;
         cudaError_t e = launch_row_repack(x, xc, P.M, w, wc, g.K, P.g_row_bytes, P.tma_row_bytes,
-                                          dev->num_sms, stream);
+                                          0, dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "row repack launch");
         xa = xc;
         wa = wc;
     }
-    CUtensorMap tmA, tmB, tmC;
-    if ((rc = build_maps(g, P, xa, wa, &tmA, &tmB))) return rc;
-    if ((rc = build_out_map(g, P, out, &tmC))) return rc;
+    TMaps tm;
+    if ((rc = build_maps(g, P, xa, wa, &tm))) return rc;
+    if ((rc = build_out_map(g, P, out, &tm))) return rc;
 
     KParams k;
     fill_params(g, P, x, w, out, workspace, scale_x, scale_w, dev->status, &k);
@@ -885,11 +963,13 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
                      "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
-                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d msub=%d\n",
+                     "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d msub=%d "
+                     "phases=%d repack=%d\n",
                      P.cls, P.amode, P.fp8, P.M, k.K, P.BN, P.BK, P.stages, P.splits, P.k_steps,
-                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair, P.msub);
+                     P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair, P.msub,
+                     P.phases, P.repack);
     }
-    cudaError_t e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, P.grid, P.smem, stream);
+    cudaError_t e = launch_igemm(P.amode, P.fp8, &tm, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
         e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, dev->num_sms,
@@ -959,9 +1039,9 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         return CONV_OK;
     }
 
-    CUtensorMap tmA, tmB, tmC;
-    if ((rc = build_maps(g, P, x_dev, w_dev, &tmA, &tmB))) return rc;
-    if ((rc = build_out_map(g, P, out_dev, &tmC))) return rc;
+    TMaps tm;
+    if ((rc = build_maps(g, P, x_dev, w_dev, &tm))) return rc;
+    if ((rc = build_out_map(g, P, out_dev, &tm))) return rc;
     KParams k;
     fill_params(g, P, x_dev, w_dev, out_dev, workspace, scale_x, scale_w, dev->status, &k);
 
@@ -1004,7 +1084,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         if (std::getenv("CONV3D_LOG"))
             std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) rows [%lld, %lld) "
                          "x prefix %zu B grid %d\n", i, mt0, mt1, row_lo, row_hi, x_done, grid);
-        if ((e = launch_igemm(P.amode, P.fp8, &tmA, &tmB, &tmC, k, grid, P.smem, stream)) !=
+        if ((e = launch_igemm(P.amode, P.fp8, &tm, k, grid, P.smem, stream)) !=
             cudaSuccess) {
             what = "conv kernel launch";
             break;

@@ -24,6 +24,8 @@
 // drains its copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -320,8 +322,8 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
 // boxes of each of the MSUB row sub-tiles and the B boxes: NB boxes of
 // 128-byte rows per operand for a 256-byte k-step, else one.
 template <int AMODE, int FP8, int PAIR, int MSUB, int NB>
-__device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                             const KParams& p, uint32_t tiles, uint32_t full0,
+__device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, uint32_t tiles,
+                                             uint32_t full0,
                                              uint32_t empty0, uint32_t* misc,
                                              volatile uint32_t* abort_flag, uint32_t rank) {
     constexpr int kTileM = kBM << PAIR;
@@ -340,6 +342,11 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
         const Unit t = decode_unit(u, p);
         const int ks0 = t.split * p.steps_per_split;
         const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
+        // row phase (two-phase point-output GEMM): its own A / B maps, local m-tile
+        const int rphase = t.m_tile >= p.mt_phase0 ? 1 : 0;
+        const int mt_local = t.m_tile - rphase * p.mt_phase0;
+        const CUtensorMap* tmA = &tm.a[rphase];
+        const CUtensorMap* tmB = &tm.b[rphase];
         // this CTA's B rows: all BN columns, or its half of them in a pair
         const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (p.BN >> PAIR);
         // A coordinates of each row sub-tile (128 rows of this CTA)
@@ -366,7 +373,7 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
                 ad[sub] = od * p.sd - p.pd;
                 ah[sub] = hwb * kTileM * MSUB + first;   // first H*W row
             } else {
-                am0[sub] = t.m_tile * kTileM * MSUB + first;
+                am0[sub] = mt_local * kTileM * MSUB + first;
             }
         }
         // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
@@ -397,14 +404,14 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
                     for (int sub = 0; sub < MSUB; ++sub) {
                         const uint32_t adst = adst0 + (sub * NB + j) * abox;
                         if (PAIR)
-                            tma_load_2d_pair(adst, &tmA, fb, kj, am0[sub]);
+                            tma_load_2d_pair(adst, tmA, fb, kj, am0[sub]);
                         else
-                            tma_load_2d(adst, &tmA, fb, kj, am0[sub]);
+                            tma_load_2d(adst, tmA, fb, kj, am0[sub]);
                     }
                     if (PAIR)
-                        tma_load_2d_pair(bdst + j * bbox, &tmB, fb, kj, n0);
+                        tma_load_2d_pair(bdst + j * bbox, tmB, fb, kj, n0);
                     else
-                        tma_load_2d(bdst + j * bbox, &tmB, fb, kj, n0);
+                        tma_load_2d(bdst + j * bbox, tmB, fb, kj, n0);
                 }
                 k0 += bke;
             } else {
@@ -418,24 +425,24 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
                         const uint32_t adst = adst0 + (sub * NB + j) * abox;
                         if (PAIR) {
                             if (AMODE == AM_IM2COL)
-                                tma_load_im2col_5d_pair(adst, &tmA, fb, cj, aw[sub], ah[sub],
+                                tma_load_im2col_5d_pair(adst, tmA, fb, cj, aw[sub], ah[sub],
                                                         ad[sub], an[sub], ow, oh, od);
                             else
-                                tma_load_4d_pair(adst, &tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
+                                tma_load_4d_pair(adst, tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
                                                  an[sub]);
                         } else {
                             if (AMODE == AM_IM2COL)
-                                tma_load_im2col_5d(adst, &tmA, fb, cj, aw[sub], ah[sub], ad[sub],
+                                tma_load_im2col_5d(adst, tmA, fb, cj, aw[sub], ah[sub], ad[sub],
                                                    an[sub], ow, oh, od);
                             else
-                                tma_load_4d(adst, &tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
+                                tma_load_4d(adst, tmA, fb, cj, ah[sub], ad[sub] + ft * p.dd,
                                             an[sub]);
                         }
                     }
                     if (PAIR)
-                        tma_load_3d_pair(bdst + j * bbox, &tmB, fb, cj, tap, n0);
+                        tma_load_3d_pair(bdst + j * bbox, tmB, fb, cj, tap, n0);
                     else
-                        tma_load_3d(bdst + j * bbox, &tmB, fb, cj, tap, n0);
+                        tma_load_3d(bdst + j * bbox, tmB, fb, cj, tap, n0);
                 }
                 ++tap;
                 if (++fs == p.S) {
@@ -465,9 +472,7 @@ __device__ __forceinline__ void tma_producer(const CUtensorMap& tmA, const CUten
 // each CTA's epilogue drains its own TMEM half).
 template <int AMODE, int FP8, int PAIR>
 __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
-    conv_igemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const KParams p) {
+    conv_igemm_kernel(const __grid_constant__ TMaps tm, const KParams p) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -509,10 +514,13 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         misc[3] = 0u;
         fence_mbar_init();
         if (!kGather) {
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
+            for (int ph = 0; ph < p.phases; ++ph) {
+                prefetch_tmap(&tm.a[ph]);
+                prefetch_tmap(&tm.b[ph]);
+            }
         }
-        if (p.epi_bytes) prefetch_tmap(&tmC);
+        if (p.epi_bytes)
+            for (int ph = 0; ph < p.phases; ++ph) prefetch_tmap(&tm.c[ph]);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -528,6 +536,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
     if (PAIR) cluster_sync();   // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
+    // everything above touches only shared memory, TMEM and the kernel
+    // parameters; global memory is read and written only after the previous
+    // kernel in the stream has completed (programmatic dependent launch)
+    griddep_wait();
 
     if (warp == 0) {
         if (kGather && lane == 0) {
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         // ------------------------------------------------------ TMA producer
         if (!kGather && lane == 0) {
 #define C3D_PROD(MS, NBX) \
-    tma_producer<AMODE, FP8, PAIR, MS, NBX>(tmA, tmB, p, tiles, full0, empty0, misc, abort_flag, rank)
+    tma_producer<AMODE, FP8, PAIR, MS, NBX>(tm, p, tiles, full0, empty0, misc, abort_flag, rank)
             if (p.msub == 2) {
                 if (p.BK == 256) C3D_PROD(2, 2);
                 else C3D_PROD(2, 1);
@@ -599,11 +611,13 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             if (!wait_bar(tfull0 + 8 * acc, acc_phase, abort_flag, p.status, p.wait_ns)) break;
             tc_fence_after();
             int plane = 0, unit_row0;   // temporal: plane and first H*W row of the unit
+            const int rphase = t.m_tile >= p.mt_phase0 ? 1 : 0;   // row phase (GEMM)
+            const long long phase_rows = rphase ? p.rows1 : p.rows0;
             if (AMODE == AM_TEMPORAL) {
                 plane = t.m_tile / p.hw_tiles;
                 unit_row0 = (t.m_tile - plane * p.hw_tiles) * unit_rows;
             } else {
-                unit_row0 = t.m_tile * unit_rows;
+                unit_row0 = (t.m_tile - rphase * p.mt_phase0) * unit_rows;
             }
             for (int sub = 0; sub < p.msub; ++sub) {
                 // this thread's row of the unit, and the warp's first row
@@ -616,9 +630,9 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     any = wrow0 < p.HW;
                     m = static_cast<long long>(plane) * p.HW + r;
                 } else {
-                    valid = r < p.M;
-                    any = wrow0 < p.M;
-                    m = r;
+                    valid = r < phase_rows;
+                    any = wrow0 < phase_rows;
+                    m = static_cast<long long>(r) * p.phases + rphase;   // output row
                 }
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>((acc * p.msub + sub) * p.BN);
@@ -626,12 +640,9 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     // TMA-store epilogue: the warp's 32 rows leave in 32x32 chunks
                     // staged in shared memory (64-byte swizzle, two buffers)
                     if (!any) continue;
-                    for (int j = 0; j < p.BN / 32; ++j) {
+                    // one 32-column chunk: stage in the next buffer, store by TMA
+                    auto store_chunk = [&](const uint32_t (&v)[32], int j) {
                         const int n0 = t.n_tile * p.BN + 32 * j;
-                        if (n0 >= p.K) break;
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(tb + 32 * j, v);
-                        tmem_ld_wait();
                         const uint32_t buf = bufs + static_cast<uint32_t>(epi_iter & 1) * kEpiChunkBytes;
                         ++epi_iter;
                         if (lane == 0) bulk_wait_read<1>();   // this buffer's last store has read it
@@ -650,11 +661,25 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                         __syncwarp();
                         if (lane == 0) {
                             if (AMODE == AM_TEMPORAL)
-                                tma_store_3d(&tmC, buf, n0, wrow0, plane);
+                                tma_store_3d(&tm.c[0], buf, n0, wrow0, plane);
                             else
-                                tma_store_2d(&tmC, buf, n0, wrow0);
+                                tma_store_2d(&tm.c[rphase], buf, n0, wrow0);
                             bulk_commit();
                         }
+                    };
+                    // chunks holding columns below K; the TMEM load of chunk
+                    // j + 1 is in flight while chunk j is converted and stored
+                    const int nch = min(p.BN / 32, (p.K - t.n_tile * p.BN + 31) / 32);
+                    uint32_t va[32], vb[32];
+                    tmem_ld_32x32b_x32(tb, va);
+                    for (int j = 0; j < nch; j += 2) {
+                        tmem_ld_wait();
+                        if (j + 1 < nch) tmem_ld_32x32b_x32(tb + 32 * (j + 1), vb);
+                        store_chunk(va, j);
+                        if (j + 1 >= nch) break;
+                        tmem_ld_wait();
+                        if (j + 2 < nch) tmem_ld_32x32b_x32(tb + 32 * (j + 2), va);
+                        store_chunk(vb, j + 1);
                     }
                     continue;
                 }
@@ -684,7 +709,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             }
             ++acc_iter;
         }
-        if (p.epi_bytes && lane == 0) bulk_wait_all();   // stores done before the CTA leaves
+        // the staging buffers are read out before the CTA leaves; the stores'
+        // global writes complete with the grid (the next kernel in the
+        // stream, or a dependent launch's wait, sees them)
+        if (p.epi_bytes && lane == 0) bulk_wait_read<0>();
     } else if (kGather) {
         // ------------------------------------------------------ row gather
         const int g = threadIdx.x - (2 + kEpiWarps) * 32;
@@ -735,41 +763,48 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
 }
 
 template <int AM, int F8, int PAIR>
-cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
-                       const KParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_one(const TMaps* tm, const KParams& p, int grid, size_t smem,
+                       cudaStream_t stream) {
     auto kern = conv_igemm_kernel<AM, F8, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int threads = (AM == AM_GEMM_GATHER) ? 320 : 192;
-    if (!PAIR) {
-        kern<<<grid, threads, smem, stream>>>(*tmA, *tmB, *tmC, p);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    // the set-up (barriers, TMEM, descriptor prefetch) may overlap the tail
+    // of the previous kernel in the stream; CONV3D_PDL=0 turns this off
+    const char* pdl = std::getenv("CONV3D_PDL");
+    if (!(pdl && pdl[0] == '0')) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (PAIR) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, *tmC, p);
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, *tm, p);
 }
 
 }  // namespace
 
-cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                         const CUtensorMap* tmC, const KParams& p, int grid, size_t smem,
-                         cudaStream_t stream) {
+cudaError_t launch_igemm(int amode, int fp8, const TMaps* tm, const KParams& p, int grid,
+                         size_t smem, cudaStream_t stream) {
     const int key = (amode * 2 + (fp8 ? 1 : 0)) * 2 + (p.pair ? 1 : 0);
     switch (key) {
 #define C3D_CASE(AM, F8, PR) \
-    case (AM * 2 + F8) * 2 + PR: return launch_one<AM, F8, PR>(tmA, tmB, tmC, p, grid, smem, stream);
+    case (AM * 2 + F8) * 2 + PR: return launch_one<AM, F8, PR>(tm, p, grid, smem, stream);
         C3D_CASE(AM_IM2COL, 0, 0)
         C3D_CASE(AM_IM2COL, 1, 0)
         C3D_CASE(AM_IM2COL, 0, 1)

@@ -36,6 +36,11 @@ struct KParams {
     int hw_tiles;       // temporal: ceil(HW / 128)
     int m_tiles, n_tiles, splits;
     int m_tile0;        // first m-tile of this launch (launches over a range of m-tiles)
+    // row phases of the point-output GEMM (1, or 2 when every other A row is
+    // not 16-byte aligned): output row = local row * phases + phase; m-tiles
+    // [0, mt_phase0) are phase 0, the rest phase 1; rows0 / rows1 rows each
+    int phases, mt_phase0;
+    long long rows0, rows1;
     int k_steps;        // k-steps of the whole reduction
     int steps_per_split;
     int taps;           // conv: T*R*S
@@ -65,10 +70,15 @@ struct KParams {
     unsigned long long wait_ns;
 };
 
+// The tensor maps of one launch: A, B and the output for each row phase
+// (index 1 is used only by a two-phase point-output GEMM).
+struct TMaps {
+    CUtensorMap a[2], b[2], c[2];
+};
+
 // Launch the implicit-GEMM kernel (AMODE x dtype) on grid/smem from the plan.
-cudaError_t launch_igemm(int amode, int fp8, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                         const CUtensorMap* tmC, const KParams& p, int grid, size_t smem,
-                         cudaStream_t stream);
+cudaError_t launch_igemm(int amode, int fp8, const TMaps* maps, const KParams& p, int grid,
+                         size_t smem, cudaStream_t stream);
 
 // Deterministic split-K reduction: out = bf16(scale * sum_s ws[s]) in split order.
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
@@ -76,10 +86,12 @@ cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int s
                                  cudaStream_t stream);
 
 // Row repack of two matrices with equal row pitches: copy rows of
-// src_row_bytes into rows of dst_row_bytes, zero-filling each row's tail.
+// src_row_bytes into rows of dst_row_bytes, matrix 1's rows shifted right by
+// dst1_shift_bytes, zero-filling the rest of each destination row.
 cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, const void* src1,
                               void* dst1, long long rows1, long long src_row_bytes,
-                              long long dst_row_bytes, int num_sms, cudaStream_t stream);
+                              long long dst_row_bytes, long long dst1_shift_bytes, int num_sms,
+                              cudaStream_t stream);
 
 // Bytes of split-K partials the plan for this problem uses (0 without split-K).
 size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],

@@ -318,3 +318,51 @@ def test_wide_k_steps(pkg, case, plan):
         assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["k_bytes"] == 256
         _run_and_check(pkg, xs, ws, st, pa, di, seed=140 + WIDE_K_CASES.index(case),
                        split_k=True, what=f"bk256 pair={pair} msub={msub} {spec} {case}")
+
+
+# Point-output GEMM whose rows are 8 bytes past a 16-byte multiple (the 14x14x3
+# patch embedding): two row phases over the caller's x, only the weights
+# copied.  Odd and even image counts, two and three images, K below / not a
+# multiple of 8 (direct-store epilogue), split-K, forced CTA pairs.
+TWO_PHASE = [
+    ((301, 1, 14, 14, 3), (200, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((600, 1, 14, 14, 3), (96, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((2, 1, 14, 14, 3), (40, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((3, 1, 14, 14, 3), (36, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((517, 1, 2, 2, 1), (100, 1, 2, 2, 1), (1, 2, 2), 0, 1),     # 8-byte rows, K % 8 = 4
+    ((260, 1, 2, 2, 5), (72, 1, 2, 2, 5), (1, 2, 2), 0, 1),      # 20 elements = 40-byte rows
+]
+
+
+@pytest.mark.parametrize("case", TWO_PHASE, ids=[str(i) for i in range(len(TWO_PHASE))])
+@pytest.mark.parametrize("split_k", [True, False])
+def test_point_gemm_two_phases(pkg, case, split_k):
+    xs, ws, st, pa, di = case
+    x, w = _inputs(xs, ws, 160 + TWO_PHASE.index(case))
+    rb = ws[1] * ws[2] * ws[3] * ws[4] * 2
+    assert rb % 16 == 8
+    plan = pkg.conv_fwd_plan(xs, ws, st, pa, di)
+    assert plan["class"] == "point_gemm"
+    ws_t = None
+    if not split_k:   # room for the weight copies only: no split-K
+        ws_t = torch.empty(2 * ((ws[0] * (rb + 8) + 255) // 256 * 256), dtype=torch.uint8,
+                           device="cuda")
+    y = pkg.conv_fwd(x, w, st, pa, di, workspace=ws_t)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    ref = oracle_conv(x, w, pkg._triple(st), pkg._triple(pa), pkg._triple(di))
+    assert_close(as_f64(y), ref, f"two-phase {case} split={split_k}")
+    if split_k:
+        # the same problem through the full operand repack (CONV3D_PHASES=1)
+        with env_vars(CONV3D_PHASES=1):
+            y1 = pkg.conv_fwd(x, w, st, pa, di)
+            torch.cuda.synchronize()
+        assert_close(as_f64(y1), ref, f"repack {case}")
+
+
+@pytest.mark.parametrize("pair", [0, 1])
+def test_point_gemm_two_phases_forced_pair(pkg, pair):
+    xs, ws = (1100, 1, 14, 14, 3), (256, 1, 14, 14, 3)
+    with env_vars(CONV3D_PAIR=pair), forced_tile("128,128,0,1,1"):
+        _run_and_check(pkg, xs, ws, (1, 14, 14), 0, 1, seed=170, split_k=True,
+                       what=f"two-phase pair={pair}")

@@ -153,3 +153,19 @@ def test_fp8_conv_wide_k_steps(pkg, case, plan):
     ref = oracle.conv3d(bytes8(qx), bytes8(qw), pkg._triple(st), pkg._triple(pa), pkg._triple(di),
                         sx.item(), sw.item())
     assert_close(as_f64(y), ref, f"fp8 bk256 pair={pair} {case}")
+
+
+def test_fp8_point_gemm_two_phases(pkg):
+    """fp8 point-output GEMM with 24-byte rows (8 past a 16-byte multiple):
+    the two-phase path over the packed activation."""
+    xs, ws = (333, 6, 1, 2, 2), (48, 6, 1, 2, 2)   # NCDHW / KCTRS: 24 elements per row
+    x = cw.randn_bf16(xs, 420, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 520, 1.0 / np.sqrt(24), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    plan = pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), (1, 2, 2), 0, 1, 1)
+    assert plan["class"] == "point_gemm"
+    y = pkg.conv_fwd(qx, qw, (1, 2, 2), 0, 1, scale_x=sx, scale_w=sw)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    ref = oracle.conv3d(bytes8(qx), bytes8(qw), (1, 2, 2), (0, 0, 0), (1, 1, 1), sx.item(), sw.item())
+    assert_close(as_f64(y), ref, "fp8 two-phase")
