@@ -645,6 +645,10 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.K = static_cast<int>(g.K);
     k.HW = P.HW;
     k.hw_tiles = P.hw_tiles;
+    // temporal units of one wave share input planes in L2 when H*W-tile
+    // major; CONV3D_HWMAJOR=0 keeps output row order
+    const char* hm = std::getenv("CONV3D_HWMAJOR");
+    k.hw_major = (P.cls == CONV_CLASS_TEMPORAL && !(hm && hm[0] == '0')) ? 1 : 0;
     k.m_tiles = P.m_tiles;
     k.n_tiles = P.n_tiles;
     k.splits = P.splits;
@@ -1044,6 +1048,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
     if ((rc = build_out_map(g, P, out_dev, &tm))) return rc;
     KParams k;
     fill_params(g, P, x_dev, w_dev, out_dev, workspace, scale_x, scale_w, dev->status, &k);
+    k.hw_major = 0;   // slices are ranges of output rows: m-tiles in row order
 
     Pipe* pp = nullptr;
     if ((rc = pipe_for_device(&pp))) return rc;

@@ -40,6 +40,21 @@ struct Unit {
     int m_tile, n_tile, split;
 };
 
+// Temporal m-tile -> ((n, d) plane, H*W tile).  Plane-major by default (output
+// row order); H*W-tile-major when p.hw_major, so that the units running at
+// once cover one H*W tile of consecutive planes and share their input planes
+// (each is read by T output planes) in L2.
+__device__ __forceinline__ void temporal_tile(int m_tile, const KParams& p, int& plane, int& hwb) {
+    if (p.hw_major) {
+        const int planes = p.N * p.Do;
+        hwb = m_tile / planes;
+        plane = m_tile - hwb * planes;
+    } else {
+        plane = m_tile / p.hw_tiles;
+        hwb = m_tile - plane * p.hw_tiles;
+    }
+}
+
 // Work unit -> (m-tile, n-tile, split).  Within a split, tiles are walked in
 // groups of `group_m` m-tiles: down M first, then across N, so that CTAs
 // running at the same time share both A rows and B columns in L2.  A launch
@@ -366,8 +381,8 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
                 ah[sub] = oh * p.sh - p.ph;
                 ad[sub] = od * p.sd - p.pd;
             } else if (AMODE == AM_TEMPORAL) {
-                const int plane = t.m_tile / p.hw_tiles;
-                const int hwb = t.m_tile - plane * p.hw_tiles;
+                int plane, hwb;
+                temporal_tile(t.m_tile, p, plane, hwb);
                 const int od = plane % p.Do;
                 an[sub] = plane / p.Do;
                 ad[sub] = od * p.sd - p.pd;
@@ -614,8 +629,9 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             const int rphase = t.m_tile >= p.mt_phase0 ? 1 : 0;   // row phase (GEMM)
             const long long phase_rows = rphase ? p.rows1 : p.rows0;
             if (AMODE == AM_TEMPORAL) {
-                plane = t.m_tile / p.hw_tiles;
-                unit_row0 = (t.m_tile - plane * p.hw_tiles) * unit_rows;
+                int hwb;
+                temporal_tile(t.m_tile, p, plane, hwb);
+                unit_row0 = hwb * unit_rows;
             } else {
                 unit_row0 = (t.m_tile - rphase * p.mt_phase0) * unit_rows;
             }

@@ -33,7 +33,8 @@ struct KParams {
     long long M;        // output rows
     int K;              // output columns (filters)
     int HW;             // temporal: H*W rows per (n, d) plane
-    int hw_tiles;       // temporal: ceil(HW / 128)
+    int hw_tiles;       // temporal: ceil(HW / rows per m-tile)
+    int hw_major;       // temporal: m-tiles ordered H*W tile major (see temporal_tile)
     int m_tiles, n_tiles, splits;
     int m_tile0;        // first m-tile of this launch (launches over a range of m-tiles)
     // row phases of the point-output GEMM (1, or 2 when every other A row is
