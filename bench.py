@@ -216,12 +216,13 @@ def prepare(pkg, wl: cw.Workload, device):
     return {"x": x, "w": w, "sx": None, "sw": None}
 
 
-def conv_step(pkg, wl, ops, out, ws):
+def conv_step(pkg, wl, ops, out, ws, bias=None):
     return lambda: pkg.conv_fwd(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil, scale_x=ops["sx"],
-                                scale_w=ops["sw"], out=out, workspace=ws)
+                                scale_w=ops["sw"], out=out, workspace=ws, bias=bias)
 
 
-def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True):
+def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias=False):
+    """with_bias: the same step through conv_fwd_bias (a per-filter fp32 bias)."""
     ops = prepare(pkg, wl, device)
     x, w = ops["x"], ops["w"]
     plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
@@ -229,7 +230,11 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True):
     od = pkg.conv_out_dims(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil)
     out = torch.empty(od, dtype=torch.bfloat16, device=device)
     ws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=device)
-    step = conv_step(pkg, wl, ops, out, ws)
+    bias = None
+    if with_bias:
+        g = torch.Generator(device="cpu").manual_seed(wl.w_seed + 500)
+        bias = torch.randn(w.shape[0], generator=g).float().to(device)
+    step = conv_step(pkg, wl, ops, out, ws, bias)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -399,11 +404,14 @@ def main_arm(args):
 
     secondary = {}
     if not args.no_secondary:
-        for name in [n for n in ("fp8_conv3d_1x3x3", "temporal_3x1x1_bf16_big", "patch_embed_bf16",
-                                 "tiny_conv3d_bf16") if n != wl.name]:
+        names = [n for n in ("fp8_conv3d_1x3x3", "temporal_3x1x1_bf16_big", "patch_embed_bf16",
+                             "tiny_conv3d_bf16") if n != wl.name]
+        # the bias epilogue on the headline and on the epilogue-heavy patch embedding
+        names += [wl.name + "+bias", "patch_embed_bf16+bias"]
+        for name in names:
             try:
-                r = run_workload(pkg, cw.BY_NAME[name], device, args.steps, args.warmup, flush,
-                                 with_e2e=False)
+                r = run_workload(pkg, cw.BY_NAME[name.split("+")[0]], device, args.steps,
+                                 args.warmup, flush, with_e2e=False, with_bias=name.endswith("+bias"))
                 m = statistics.mean(r["ms"])
                 ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m, "plan": r["plan"]}
                 if "ms_with_pack" in r:

@@ -78,6 +78,9 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp, vp,
                                  vp, ctypes.c_size_t, vp]
         lib.conv_fwd.restype = ctypes.c_int
+        lib.conv_fwd_bias.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp,
+                                      vp, vp, vp, ctypes.c_size_t, vp]
+        lib.conv_fwd_bias.restype = ctypes.c_int
         lib.conv_fwd_noalloc.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
                                          vp, vp, vp]
         lib.conv_fwd_noalloc.restype = ctypes.c_int
@@ -185,11 +188,13 @@ def conv_get_device_status() -> int:
 def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
              scale_x: Optional[torch.Tensor] = None, scale_w: Optional[torch.Tensor] = None,
              out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-             stream: Optional[torch.cuda.Stream] = None, split_k: bool = True) -> torch.Tensor:
+             stream: Optional[torch.cuda.Stream] = None, split_k: bool = True,
+             bias: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Forward conv: x NDHWC [N,D,H,W,C], w KTRSC [K,T,R,S,C] (both bf16, or
     both float8_e4m3fn with fp32 device scales) -> out NDHWC [N,Do,Ho,Wo,K]
-    bf16.  A split-K workspace is taken from torch's allocator when the plan
-    wants one and none is given (``split_k=False`` runs without)."""
+    bf16, plus ``bias`` (fp32 [K], through conv_fwd_bias) when given.  A
+    split-K workspace is taken from torch's allocator when the plan wants one
+    and none is given (``split_k=False`` runs without)."""
     lib = load_library()
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x must be [N,D,H,W,C] and w [K,T,R,S,C]")
@@ -199,7 +204,9 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
     for s in (scale_x, scale_w):
         if s is not None and (s.dtype != torch.float32 or s.numel() < 1):
             raise TypeError("scales must be float32 device tensors")
-    _require_cuda(x, w, scale_x, scale_w, out, workspace)
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (w.shape[0],)):
+        raise TypeError("bias must be a float32 device tensor of shape [K]")
+    _require_cuda(x, w, scale_x, scale_w, out, workspace, bias)
     st, pa, di = _triple(stride), _triple(pad), _triple(dil)
     od = conv_out_dims(tuple(x.shape), tuple(w.shape), st, pa, di)
     if out is None:
@@ -214,10 +221,17 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
             ws_ptr, ws_bytes = workspace.data_ptr(), need
-    rc = lib.conv_fwd(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
-                      _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x), _ptr(scale_w),
-                      out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
-    _check(rc, "conv_fwd")
+    if bias is None:
+        rc = lib.conv_fwd(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                          _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
+                          _ptr(scale_w), out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
+        _check(rc, "conv_fwd")
+    else:
+        rc = lib.conv_fwd_bias(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                               _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
+                               _ptr(scale_w), bias.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes,
+                               _stream_handle(stream))
+        _check(rc, "conv_fwd_bias")
     return out
 
 

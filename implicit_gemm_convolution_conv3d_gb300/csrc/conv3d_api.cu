@@ -631,8 +631,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Kernel parameters of plan P over the whole problem (m-tiles [0, m_tiles)).
 void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void* out,
-                 void* workspace, const float* scale_x, const float* scale_w, int* status,
-                 KParams* kp) {
+                 void* workspace, const float* scale_x, const float* scale_w, const float* bias,
+                 int* status, KParams* kp) {
     KParams& k = *kp;
     std::memset(&k, 0, sizeof k);
     k.N = static_cast<int>(g.N); k.D = static_cast<int>(g.D); k.H = static_cast<int>(g.H);
@@ -683,6 +683,7 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
                : nullptr;
     k.scale_x = scale_x;
     k.scale_w = scale_w;
+    k.bias = bias;
     k.status = status;
     k.wait_ns = g_wait_ns;
 }
@@ -912,6 +913,14 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
              const int stride[3], const int pad[3], const int dil[3], int dtype,
              const float* scale_x, const float* scale_w, void* out, void* workspace,
              size_t workspace_bytes, cudaStream_t stream) {
+    return conv_fwd_bias(x, x_dims, w, w_dims, stride, pad, dil, dtype, scale_x, scale_w, nullptr,
+                         out, workspace, workspace_bytes, stream);
+}
+
+int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+                  const int stride[3], const int pad[3], const int dil[3], int dtype,
+                  const float* scale_x, const float* scale_w, const float* bias, void* out,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Geo g;
     int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
     if (rc) return rc;
@@ -921,7 +930,8 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     }
     if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (workspace && !aligned16(workspace)) ||
         (scale_x && (reinterpret_cast<uintptr_t>(scale_x) & 3u)) ||
-        (scale_w && (reinterpret_cast<uintptr_t>(scale_w) & 3u))) {
+        (scale_w && (reinterpret_cast<uintptr_t>(scale_w) & 3u)) ||
+        (bias && (reinterpret_cast<uintptr_t>(bias) & 3u))) {
         set_error("device pointers must be 16-byte aligned");
         return CONV_ERR_INVALID;
     }
@@ -962,7 +972,7 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     if ((rc = build_out_map(g, P, out, &tm))) return rc;
 
     KParams k;
-    fill_params(g, P, x, w, out, workspace, scale_x, scale_w, dev->status, &k);
+    fill_params(g, P, x, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
 
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
@@ -976,8 +986,8 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
     cudaError_t e = launch_igemm(P.amode, P.fp8, &tm, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
-        e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, dev->num_sms,
-                                 stream);
+        e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K,
+                                 dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }
     return CONV_OK;
@@ -1047,7 +1057,8 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
     if ((rc = build_maps(g, P, x_dev, w_dev, &tm))) return rc;
     if ((rc = build_out_map(g, P, out_dev, &tm))) return rc;
     KParams k;
-    fill_params(g, P, x_dev, w_dev, out_dev, workspace, scale_x, scale_w, dev->status, &k);
+    fill_params(g, P, x_dev, w_dev, out_dev, workspace, scale_x, scale_w, nullptr, dev->status,
+                &k);
     k.hw_major = 0;   // slices are ranges of output rows: m-tiles in row order
 
     Pipe* pp = nullptr;

@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdlib>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -120,24 +121,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Store 32 accumulator columns of one output row (bf16).
+// Store 32 accumulator columns of one output row (bf16): v * scale + bias
+// (bias: the 32 columns' entries, or NULL).
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
-                                               float scale, int count, bool vec_ok) {
+                                               float scale, const float* bias, int count,
+                                               bool vec_ok) {
+    auto val = [&](int i) {
+        return __uint_as_float(v[i]) * scale + (bias ? __ldg(bias + i) : 0.0f);
+    };
     if (count == 32 && vec_ok) {
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * scale, __uint_as_float(v[8 * i + 1]) * scale);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * scale, __uint_as_float(v[8 * i + 3]) * scale);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * scale, __uint_as_float(v[8 * i + 5]) * scale);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * scale, __uint_as_float(v[8 * i + 7]) * scale);
+            o.x = pack_bf16x2(val(8 * i + 0), val(8 * i + 1));
+            o.y = pack_bf16x2(val(8 * i + 2), val(8 * i + 3));
+            o.z = pack_bf16x2(val(8 * i + 4), val(8 * i + 5));
+            o.w = pack_bf16x2(val(8 * i + 6), val(8 * i + 7));
             d4[i] = o;
         }
     } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            if (i < count) dst[i] = __float2bfloat16_rn(__uint_as_float(v[i]) * scale);
+            if (i < count) dst[i] = __float2bfloat16_rn(val(i));
     }
 }
 
@@ -623,6 +629,14 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
             const Unit t = decode_unit(u, p);
             const int acc = acc_iter % nacc;
             const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
+            // this lane's bias entry of each 32-column chunk of the unit
+            // (loaded while the accumulator is still being computed)
+            float bl[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int col = t.n_tile * p.BN + 32 * j + lane;
+                bl[j] = (p.bias && 32 * j < p.BN && col < p.K) ? __ldg(p.bias + col) : 0.0f;
+            }
             if (!wait_bar(tfull0 + 8 * acc, acc_phase, abort_flag, p.status, p.wait_ns)) break;
             tc_fence_after();
             int plane = 0, unit_row0;   // temporal: plane and first H*W row of the unit
@@ -657,8 +671,14 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     // staged in shared memory (64-byte swizzle, two buffers)
                     if (!any) continue;
                     // one 32-column chunk: stage in the next buffer, store by TMA
-                    auto store_chunk = [&](const uint32_t (&v)[32], int j) {
+                    // (with_bias: column i's bias is lane i's entry bj)
+                    auto store_chunk = [&](const uint32_t (&v)[32], int j, float bj, auto with_bias) {
+                        constexpr bool kBias = decltype(with_bias)::value;
                         const int n0 = t.n_tile * p.BN + 32 * j;
+                        auto val = [&](int i) {
+                            const float b = kBias ? __shfl_sync(0xffffffffu, bj, i) : 0.0f;
+                            return __uint_as_float(v[i]) * scale + b;
+                        };
                         const uint32_t buf = bufs + static_cast<uint32_t>(epi_iter & 1) * kEpiChunkBytes;
                         ++epi_iter;
                         if (lane == 0) bulk_wait_read<1>();   // this buffer's last store has read it
@@ -667,10 +687,10 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                         const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * c + 0]) * scale, __uint_as_float(v[8 * c + 1]) * scale);
-                            const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * c + 2]) * scale, __uint_as_float(v[8 * c + 3]) * scale);
-                            const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * c + 4]) * scale, __uint_as_float(v[8 * c + 5]) * scale);
-                            const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * c + 6]) * scale, __uint_as_float(v[8 * c + 7]) * scale);
+                            const uint32_t w0 = pack_bf16x2(val(8 * c + 0), val(8 * c + 1));
+                            const uint32_t w1 = pack_bf16x2(val(8 * c + 2), val(8 * c + 3));
+                            const uint32_t w2 = pack_bf16x2(val(8 * c + 4), val(8 * c + 5));
+                            const uint32_t w3 = pack_bf16x2(val(8 * c + 6), val(8 * c + 7));
                             st_shared_v4(rowaddr + ((static_cast<uint32_t>(c) ^ sw) << 4), w0, w1, w2, w3);
                         }
                         fence_proxy_async_smem();
@@ -687,15 +707,23 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     // j + 1 is in flight while chunk j is converted and stored
                     const int nch = min(p.BN / 32, (p.K - t.n_tile * p.BN + 31) / 32);
                     uint32_t va[32], vb[32];
+                    auto chunk = [&](const uint32_t (&v)[32], int j, float bj) {
+                        if (p.bias)
+                            store_chunk(v, j, bj, std::integral_constant<bool, true>());
+                        else
+                            store_chunk(v, j, bj, std::integral_constant<bool, false>());
+                    };
                     tmem_ld_32x32b_x32(tb, va);
-                    for (int j = 0; j < nch; j += 2) {
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {   // at most 8 chunks (BN <= 256)
+                        if (j >= nch) break;
                         tmem_ld_wait();
                         if (j + 1 < nch) tmem_ld_32x32b_x32(tb + 32 * (j + 1), vb);
-                        store_chunk(va, j);
+                        chunk(va, j, bl[j]);
                         if (j + 1 >= nch) break;
                         tmem_ld_wait();
                         if (j + 2 < nch) tmem_ld_32x32b_x32(tb + 32 * (j + 2), va);
-                        store_chunk(vb, j + 1);
+                        chunk(vb, j + 1, bl[j + 1]);
                     }
                     continue;
                 }
@@ -707,7 +735,8 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     if (valid && n0 < p.K) {
                         const int cnt = min(32, p.K - n0);
                         if (p.splits == 1) {
-                            store_row_bf16(out + m * p.K + n0, v, scale, cnt, vec_out);
+                            store_row_bf16(out + m * p.K + n0, v, scale,
+                                           p.bias ? p.bias + n0 : nullptr, cnt, vec_out);
                         } else {
                             float* dst = p.ws + (static_cast<long long>(t.split) * p.M + m) * p.K + n0;
                             store_row_f32(dst, v, cnt, vec_ws);

@@ -67,6 +67,7 @@ struct KParams {
     float* ws;          // split-K partials [splits, M, K]
     const float* scale_x;
     const float* scale_w;
+    const float* bias;  // fp32 [K] added after the scales, or NULL
     int* status;        // device status word
     unsigned long long wait_ns;
 };
@@ -81,10 +82,11 @@ struct TMaps {
 cudaError_t launch_igemm(int amode, int fp8, const TMaps* maps, const KParams& p, int grid,
                          size_t smem, cudaStream_t stream);
 
-// Deterministic split-K reduction: out = bf16(scale * sum_s ws[s]) in split order.
+// Deterministic split-K reduction: out = bf16(scale * sum_s ws[s] + bias[k]) in
+// split order (bias may be NULL; k = column of the [M, K] output).
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
-                                 const float* scale_x, const float* scale_w, int num_sms,
-                                 cudaStream_t stream);
+                                 const float* scale_x, const float* scale_w, const float* bias,
+                                 long long K, int num_sms, cudaStream_t stream);
 
 // Row repack of two matrices with equal row pitches: copy rows of
 // src_row_bytes into rows of dst_row_bytes, matrix 1's rows shifted right by

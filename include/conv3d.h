@@ -108,6 +108,19 @@ int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_
              const float* scale_x, const float* scale_w, void* out, void* workspace,
              size_t workspace_bytes, cudaStream_t stream);
 
+/* conv_fwd plus a per-filter bias:
+ *   out[n,od,oh,ow,k] = bf16_rn( scale_x * scale_w * (the conv_fwd sum) + bias[k] )
+ *   bias   device, fp32 [K], 4-byte aligned; NULL gives conv_fwd exactly
+ * Every other argument, the plan and the error behaviour are conv_fwd's (with
+ * split-K the bias is added once, in the reduction).  Defined by: FlyDSL PR
+ * #860, PR summary, which lists bias among the fp8 conv's test cases; the
+ * page gives neither the bias type nor where it enters, so it is taken as an
+ * fp32 vector added after the dequantisation scales, before the rounding. */
+int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+                  const int stride[3], const int pad[3], const int dil[3], int dtype,
+                  const float* scale_x, const float* scale_w, const float* bias, void* out,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* conv_fwd with the operands and the result in HOST memory: the same
  * convolution (same definition and plan as conv_fwd, so the same output
  * bits), with the host->device copies of x and w and the device->host copy

@@ -191,9 +191,11 @@ def out_dims(x_shape, w_shape, stride, pad, dil):
 
 
 def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1, 1, 1),
-           scale_x: float = 1.0, scale_w: float = 1.0) -> np.ndarray:
+           scale_x: float = 1.0, scale_w: float = 1.0, bias=None) -> np.ndarray:
     """Full fp64 forward conv.  x [N,D,H,W,C], w [K,T,R,S,C]; both bf16 bits
-    (uint16), e4m3 bytes (uint8) or float64.  Returns fp64 [N,Do,Ho,Wo,K]."""
+    (uint16), e4m3 bytes (uint8) or float64.  Returns fp64 [N,Do,Ho,Wo,K]:
+    scale_x * scale_w * (the sum), plus bias[k] (a per-filter vector, FlyDSL
+    PR #860's fp8 conv tests include a bias case) when given."""
     x = np.ascontiguousarray(x)
     w = np.ascontiguousarray(w)
     elem = _elem_of(x)
@@ -206,13 +208,16 @@ def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1
                                    elem, float(scale_x), float(scale_w), out.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_conv3d_fwd: bad shapes")
+    if bias is not None:
+        out += np.asarray(bias, dtype=np.float64).reshape(-1)
     return out
 
 
 def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1),
                   pad=(0, 0, 0), dil=(1, 1, 1), scale_x: float = 1.0,
-                  scale_w: float = 1.0) -> np.ndarray:
-    """fp64 conv evaluated at flat NDHWC output indices ``idx`` (int64)."""
+                  scale_w: float = 1.0, bias=None) -> np.ndarray:
+    """fp64 conv evaluated at flat NDHWC output indices ``idx`` (int64), plus
+    bias[k] of each index's filter k when given."""
     x = np.ascontiguousarray(x)
     w = np.ascontiguousarray(w)
     elem = _elem_of(x)
@@ -226,6 +231,8 @@ def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1
         idx.ctypes.data_as(_I64P), idx.size, vals.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_conv3d_fwd_points: bad shapes or index out of range")
+    if bias is not None:
+        vals += np.asarray(bias, dtype=np.float64).reshape(-1)[idx % w.shape[0]]
     return vals
 
 

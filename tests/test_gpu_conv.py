@@ -366,3 +366,41 @@ def test_point_gemm_two_phases_forced_pair(pkg, pair):
     with env_vars(CONV3D_PAIR=pair), forced_tile("128,128,0,1,1"):
         _run_and_check(pkg, xs, ws, (1, 14, 14), 0, 1, seed=170, split_k=True,
                        what=f"two-phase pair={pair}")
+
+
+# Per-filter fp32 bias through conv_fwd_bias: every dispatch class, ragged K
+# (direct-store tail), with and without split-K (the bias then enters once,
+# in the reduction).
+BIAS_CASES = [
+    ((2, 5, 9, 11, 64), (272, 3, 3, 3, 64), 1, 1, 1),
+    ((1, 5, 10, 20, 64), (200, 3, 1, 1, 64), 1, (1, 0, 0), 1),
+    ((300, 1, 14, 14, 3), (200, 1, 14, 14, 3), (1, 14, 14), 0, 1),
+    ((37, 1, 3, 3, 6), (40, 1, 3, 3, 6), (1, 3, 3), 0, 1),
+    ((1, 4, 8, 8, 16), (36, 3, 3, 3, 16), 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("case", BIAS_CASES, ids=[str(i) for i in range(len(BIAS_CASES))])
+@pytest.mark.parametrize("split_k", [True, False])
+def test_bias(pkg, case, split_k):
+    xs, ws, st, pa, di = case
+    x, w = _inputs(xs, ws, 180 + BIAS_CASES.index(case))
+    g = torch.Generator(device="cpu").manual_seed(190 + BIAS_CASES.index(case))
+    b = (torch.randn(ws[0], generator=g) * 0.5).float()
+    y = pkg.conv_fwd(x, w, st, pa, di, split_k=split_k, bias=b.cuda())
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    st3, pa3, di3 = pkg._triple(st), pkg._triple(pa), pkg._triple(di)
+    ref = oracle.conv3d(bits16(x), bits16(w), st3, pa3, di3, bias=b.double().numpy())
+    assert_close(as_f64(y), ref, f"bias {case} split={split_k}")
+
+
+def test_bias_zero_weights_is_exact(pkg):
+    """Zero weights: every output is bf16_rn(bias[k]) exactly."""
+    x = cw.randn_bf16((1, 4, 6, 6, 32), 195, 1.0, "cuda")
+    w = torch.zeros((48, 3, 3, 3, 32), dtype=torch.bfloat16, device="cuda")
+    b = torch.linspace(-3.0, 3.0, 48, dtype=torch.float32, device="cuda")
+    for split_k in (True, False):
+        y = pkg.conv_fwd(x, w, 1, 1, 1, split_k=split_k, bias=b)
+        torch.cuda.synchronize()
+        assert torch.equal(y.float(), b.to(torch.bfloat16).float().expand_as(y))

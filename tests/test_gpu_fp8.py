@@ -169,3 +169,20 @@ def test_fp8_point_gemm_two_phases(pkg):
     assert pkg.conv_get_device_status() == 0
     ref = oracle.conv3d(bytes8(qx), bytes8(qw), (1, 2, 2), (0, 0, 0), (1, 1, 1), sx.item(), sw.item())
     assert_close(as_f64(y), ref, "fp8 two-phase")
+
+
+def test_fp8_conv_with_bias(pkg):
+    """The fp8 conv with both scales and a bias (FlyDSL PR #860's bias test
+    case): bias added after the dequantisation scales."""
+    xs, ws = (1, 64, 4, 9, 11), (96, 64, 1, 3, 3)
+    x = cw.randn_bf16(xs, 430, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 530, 1.0 / np.sqrt(576), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    b = torch.linspace(-1.0, 2.0, 96, dtype=torch.float32, device="cuda")
+    for split_k in (True, False):
+        y = pkg.conv_fwd(qx, qw, 1, (0, 1, 1), 1, scale_x=sx, scale_w=sw, split_k=split_k, bias=b)
+        torch.cuda.synchronize()
+        assert pkg.conv_get_device_status() == 0
+        ref = oracle.conv3d(bytes8(qx), bytes8(qw), (1, 1, 1), (0, 1, 1), (1, 1, 1), sx.item(),
+                            sw.item(), bias=b.double().cpu().numpy())
+        assert_close(as_f64(y), ref, f"fp8 bias split={split_k}")

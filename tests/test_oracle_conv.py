@@ -238,3 +238,21 @@ def test_out_extent_matches_torch_shape_rule():
         w = torch.zeros((1, 1, f))
         ref = F.conv1d(x, w, stride=s, padding=p, dilation=d).shape[-1]
         assert oracle.out_extent(inp, f, s, p, d) == ref
+
+
+def test_bias_special_cases():
+    """A per-filter bias (FlyDSL PR #860 lists a bias case among the fp8 conv
+    tests): with zero weights, or a zero input, every output of filter k is
+    exactly bias[k]; the sampled evaluation adds the same entry."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 3, 5, 4, 6))
+    w = rng.standard_normal((7, 3, 2, 2, 6))
+    b = rng.standard_normal(7)
+    out0 = oracle.conv3d(x, np.zeros_like(w), (1, 2, 1), (1, 0, 1), (1, 1, 2), bias=b)
+    assert np.array_equal(out0, np.broadcast_to(b, out0.shape))
+    outz = oracle.conv3d(np.zeros_like(x), w, (1, 2, 1), (1, 0, 1), (1, 1, 2), 0.5, 3.0, bias=b)
+    assert np.array_equal(outz, np.broadcast_to(b, outz.shape))
+    full = oracle.conv3d(x, w, (1, 2, 1), (1, 0, 1), (1, 1, 2), 0.5, 3.0, bias=b)
+    idx = rng.integers(0, full.size, size=50)
+    pts = oracle.conv3d_points(x, w, idx, (1, 2, 1), (1, 0, 1), (1, 1, 2), 0.5, 3.0, bias=b)
+    assert np.array_equal(pts, full.reshape(-1)[idx])
