@@ -91,6 +91,12 @@ def _load():
         lib.oracle_conv3d_fwd_points.restype = ctypes.c_int
         lib.oracle_conv3d_fwd_points.argtypes = conv_args + [_I64P, ctypes.c_int64,
                                                              ctypes.c_void_p]
+        bwd_args = [ctypes.c_void_p, _I64P, ctypes.c_void_p, _I64P, _I32P, _I32P, _I32P,
+                    ctypes.c_int, ctypes.c_void_p]
+        lib.oracle_conv3d_bwd_data.restype = ctypes.c_int
+        lib.oracle_conv3d_bwd_data.argtypes = bwd_args
+        lib.oracle_conv3d_bwd_weight.restype = ctypes.c_int
+        lib.oracle_conv3d_bwd_weight.argtypes = bwd_args
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -234,6 +240,50 @@ def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1
     if bias is not None:
         vals += np.asarray(bias, dtype=np.float64).reshape(-1)[idx % w.shape[0]]
     return vals
+
+
+def conv3d_bwd_data(dy: np.ndarray, w: np.ndarray, x_shape, stride=(1, 1, 1), pad=(0, 0, 0),
+                    dil=(1, 1, 1)) -> np.ndarray:
+    """fp64 gradient of sum(conv3d(x, w) * dy) with respect to x (MIOpen PR
+    #10912, backward data).  dy [N,Do,Ho,Wo,K], w [K,T,R,S,C], both bf16 bits
+    or float64; returns dx [N,D,H,W,C] = x_shape."""
+    dy = np.ascontiguousarray(dy)
+    w = np.ascontiguousarray(w)
+    elem = _elem_of(dy)
+    if _elem_of(w) != elem:
+        raise TypeError("dy and w must have the same element type")
+    od = out_dims(x_shape, w.shape, stride, pad, dil)
+    if tuple(dy.shape) != tuple(od):
+        raise ValueError(f"dy must have the output shape {od}")
+    dx = np.empty(tuple(x_shape), dtype=np.float64)
+    rc = _load().oracle_conv3d_bwd_data(dy.ctypes.data, _dims(x_shape, 5), w.ctypes.data,
+                                        _dims(w.shape, 5), _ints3(stride), _ints3(pad),
+                                        _ints3(dil), elem, dx.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_conv3d_bwd_data: bad shapes")
+    return dx
+
+
+def conv3d_bwd_weight(x: np.ndarray, dy: np.ndarray, w_shape, stride=(1, 1, 1), pad=(0, 0, 0),
+                      dil=(1, 1, 1)) -> np.ndarray:
+    """fp64 gradient of sum(conv3d(x, w) * dy) with respect to w (MIOpen PR
+    #10912, backward weights).  x [N,D,H,W,C], dy [N,Do,Ho,Wo,K], both bf16
+    bits or float64; returns dw [K,T,R,S,C] = w_shape."""
+    x = np.ascontiguousarray(x)
+    dy = np.ascontiguousarray(dy)
+    elem = _elem_of(x)
+    if _elem_of(dy) != elem:
+        raise TypeError("x and dy must have the same element type")
+    od = out_dims(x.shape, w_shape, stride, pad, dil)
+    if tuple(dy.shape) != tuple(od):
+        raise ValueError(f"dy must have the output shape {od}")
+    dw = np.empty(tuple(w_shape), dtype=np.float64)
+    rc = _load().oracle_conv3d_bwd_weight(x.ctypes.data, _dims(x.shape, 5), dy.ctypes.data,
+                                          _dims(w_shape, 5), _ints3(stride), _ints3(pad),
+                                          _ints3(dil), elem, dw.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_conv3d_bwd_weight: bad shapes")
+    return dw
 
 
 def num_threads() -> int:

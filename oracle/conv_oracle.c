@@ -314,6 +314,106 @@ int oracle_conv3d_fwd_points(const void *x, const int64_t xd[5], const void *w,
     return 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* backward passes (MIOpen PR #10912: backward-data and backward-weights  */
+/* of the point-output conv; written here for any geometry)              */
+/* ------------------------------------------------------------------ */
+
+/* Backward data: the gradient of sum(out * dy) with respect to x,
+ *   dx[n,id,ih,iw,c] = sum over (od,oh,ow,t,r,s,k) with
+ *       id = od*sd-pd+t*dd, ih = oh*sh-ph+r*dh, iw = ow*sw-pw+s*dw
+ *   of dy[n,od,oh,ow,k] * w[k,t,r,s,c].
+ * Computed in the scatter form, straight from that sum: every output element
+ * and tap adds its products into the input element it read.  dy is
+ * [N,Do,Ho,Wo,K], dx [N,D,H,W,C] fp64 (overwritten).  One thread per batch
+ * element n (each writes only its own dx[n]). */
+int oracle_conv3d_bwd_data(const void *dy, const int64_t xd[5], const void *w, const int64_t wd[5],
+                           const int stride[3], const int pad[3], const int dil[3], int elem,
+                           double *dx)
+{
+    conv_geom g;
+    int64_t n;
+    if (make_geom(&g, xd, wd, stride, pad, dil) != 0)
+        return -1;
+    memset(dx, 0, (size_t)(g.N * g.D * g.H * g.W * g.C) * sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (n = 0; n < g.N; ++n) {
+        int64_t od, oh, ow, k, t, r, s, c;
+        for (od = 0; od < g.Do; ++od)
+            for (oh = 0; oh < g.Ho; ++oh)
+                for (ow = 0; ow < g.Wo; ++ow)
+                    for (k = 0; k < g.K; ++k) {
+                        double gy = load_elem(dy, (((n * g.Do + od) * g.Ho + oh) * g.Wo + ow) * g.K + k, elem);
+                        for (t = 0; t < g.T; ++t) {
+                            int64_t id = od * g.sd - g.pd + t * g.dd;
+                            if (id < 0 || id >= g.D)
+                                continue;
+                            for (r = 0; r < g.R; ++r) {
+                                int64_t ih = oh * g.sh - g.ph + r * g.dh;
+                                if (ih < 0 || ih >= g.H)
+                                    continue;
+                                for (s = 0; s < g.S; ++s) {
+                                    int64_t iw = ow * g.sw - g.pw + s * g.dw;
+                                    int64_t xrow, wrow;
+                                    if (iw < 0 || iw >= g.W)
+                                        continue;
+                                    xrow = (((n * g.D + id) * g.H + ih) * g.W + iw) * g.C;
+                                    wrow = (((k * g.T + t) * g.R + r) * g.S + s) * g.C;
+                                    for (c = 0; c < g.C; ++c)
+                                        dx[xrow + c] += gy * load_elem(w, wrow + c, elem);
+                                }
+                            }
+                        }
+                    }
+    }
+    return 0;
+}
+
+/* Backward weights: the gradient of sum(out * dy) with respect to w,
+ *   dw[k,t,r,s,c] = sum over (n,od,oh,ow) of dy[n,od,oh,ow,k] *
+ *                   x[n, od*sd-pd+t*dd, oh*sh-ph+r*dh, ow*sw-pw+s*dw, c]
+ * (x = 0 outside the input).  dw is [K,T,R,S,C] fp64 (overwritten).  One
+ * thread per filter k. */
+int oracle_conv3d_bwd_weight(const void *x, const int64_t xd[5], const void *dy,
+                             const int64_t wd[5], const int stride[3], const int pad[3],
+                             const int dil[3], int elem, double *dw)
+{
+    conv_geom g;
+    int64_t k;
+    if (make_geom(&g, xd, wd, stride, pad, dil) != 0)
+        return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (k = 0; k < g.K; ++k) {
+        int64_t t, r, s, c, n, od, oh, ow;
+        for (t = 0; t < g.T; ++t)
+            for (r = 0; r < g.R; ++r)
+                for (s = 0; s < g.S; ++s)
+                    for (c = 0; c < g.C; ++c) {
+                        double acc = 0.0;
+                        for (n = 0; n < g.N; ++n)
+                            for (od = 0; od < g.Do; ++od) {
+                                int64_t id = od * g.sd - g.pd + t * g.dd;
+                                if (id < 0 || id >= g.D)
+                                    continue;
+                                for (oh = 0; oh < g.Ho; ++oh) {
+                                    int64_t ih = oh * g.sh - g.ph + r * g.dh;
+                                    if (ih < 0 || ih >= g.H)
+                                        continue;
+                                    for (ow = 0; ow < g.Wo; ++ow) {
+                                        int64_t iw = ow * g.sw - g.pw + s * g.dw;
+                                        if (iw < 0 || iw >= g.W)
+                                            continue;
+                                        acc += load_elem(dy, (((n * g.Do + od) * g.Ho + oh) * g.Wo + ow) * g.K + k, elem) *
+                                               load_elem(x, (((n * g.D + id) * g.H + ih) * g.W + iw) * g.C + c, elem);
+                                    }
+                                }
+                            }
+                        dw[(((k * g.T + t) * g.R + r) * g.S + s) * g.C + c] = acc;
+                    }
+    }
+    return 0;
+}
+
 /* Number of threads the OpenMP runtime will use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -256,3 +256,68 @@ def test_bias_special_cases():
     idx = rng.integers(0, full.size, size=50)
     pts = oracle.conv3d_points(x, w, idx, (1, 2, 1), (1, 0, 1), (1, 1, 2), 0.5, 3.0, bias=b)
     assert np.array_equal(pts, full.reshape(-1)[idx])
+
+
+# ------------------------------------------------------------ backward passes
+
+def _torch_grads(x, w, dy, stride, pad, dil):
+    """fp64 gradients of sum(conv3d(x, w) * dy) by torch autograd on the CPU
+    (a library routine), in the NDHWC / KTRSC layouts."""
+    xt = torch.from_numpy(np.transpose(x, (0, 4, 1, 2, 3)).copy()).requires_grad_(True)
+    wt = torch.from_numpy(np.transpose(w, (0, 4, 1, 2, 3)).copy()).requires_grad_(True)
+    y = torch.nn.functional.conv3d(xt, wt, stride=stride, padding=pad, dilation=dil)
+    y.backward(torch.from_numpy(np.transpose(dy, (0, 4, 1, 2, 3)).copy()))
+    return (np.transpose(xt.grad.numpy(), (0, 2, 3, 4, 1)),
+            np.transpose(wt.grad.numpy(), (0, 2, 3, 4, 1)))
+
+
+def test_backward_matches_torch_autograd():
+    rng = np.random.default_rng(31)
+    done = 0
+    while done < 40:
+        T, R, S = (int(v) for v in rng.integers(1, 4, size=3))
+        st = tuple(int(v) for v in rng.integers(1, 4, size=3))
+        pa = tuple(int(rng.integers(0, f)) if f > 1 else 0 for f in (T, R, S))
+        di = tuple(int(v) for v in rng.integers(1, 3, size=3))
+        xs = (int(rng.integers(1, 3)), int(rng.integers(1, 6)), int(rng.integers(1, 7)),
+              int(rng.integers(1, 7)), int(rng.integers(1, 5)))
+        ws = (int(rng.integers(1, 6)), T, R, S, xs[4])
+        od = oracle.out_dims(xs, ws, st, pa, di)
+        if min(od) < 1:
+            continue
+        x = rng.standard_normal(xs)
+        w = rng.standard_normal(ws)
+        dy = rng.standard_normal(od)
+        gx, gw = _torch_grads(x, w, dy, st, pa, di)
+        np.testing.assert_allclose(oracle.conv3d_bwd_data(dy, w, xs, st, pa, di), gx,
+                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(oracle.conv3d_bwd_weight(x, dy, ws, st, pa, di), gw,
+                                   rtol=1e-12, atol=1e-12)
+        done += 1
+
+
+def test_backward_adjoint_identity():
+    """<conv(x, w), dy> = <x, dx(dy, w)> = <w, dw(x, dy)>: the three share one
+    trilinear form."""
+    rng = np.random.default_rng(32)
+    xs, ws, st, pa, di = (2, 5, 6, 7, 3), (4, 3, 2, 3, 3), (2, 1, 2), (1, 1, 0), (1, 2, 1)
+    x, w = rng.standard_normal(xs), rng.standard_normal(ws)
+    dy = rng.standard_normal(oracle.out_dims(xs, ws, st, pa, di))
+    fwd = np.sum(oracle.conv3d(x, w, st, pa, di) * dy)
+    assert np.isclose(fwd, np.sum(x * oracle.conv3d_bwd_data(dy, w, xs, st, pa, di)), rtol=1e-12)
+    assert np.isclose(fwd, np.sum(w * oracle.conv3d_bwd_weight(x, dy, ws, st, pa, di)), rtol=1e-12)
+
+
+def test_backward_point_output_is_one_gemm():
+    """Point-output shapes (MIOpen PR #10912): dx = dy @ W and dW = dy^T @ x
+    over the flattened (t, r, s, c) axis, at the patch-embedding geometry."""
+    rng = np.random.default_rng(33)
+    xs, ws, st = (37, 1, 14, 14, 3), (20, 1, 14, 14, 3), (1, 14, 14)
+    x, w = rng.standard_normal(xs), rng.standard_normal(ws)
+    dy = rng.standard_normal((37, 1, 1, 1, 20))
+    dx = oracle.conv3d_bwd_data(dy, w, xs, st)
+    np.testing.assert_allclose(dx.reshape(37, -1), dy.reshape(37, 20) @ w.reshape(20, -1),
+                               rtol=1e-12, atol=1e-12)
+    dw = oracle.conv3d_bwd_weight(x, dy, ws, st)
+    np.testing.assert_allclose(dw.reshape(20, -1), dy.reshape(37, 20).T @ x.reshape(37, -1),
+                               rtol=1e-12, atol=1e-12)
