@@ -380,6 +380,40 @@ def workload_config(wl):
             "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"}
 
 
+def run_backward(pkg, wl, device, steps, warmup, flush):
+    """Point-output backward passes of workload wl (the patch embedding): one
+    conv_bwd_data_point and one conv_bwd_weight_point call per step, each
+    with its operand transposes, GEMM and (for dw) split-K reduction."""
+    x, w = cw.make_inputs(wl, device)
+    N, K = x.shape[0], w.shape[0]
+    g = torch.Generator(device=device).manual_seed(wl.sample_seed + 1)
+    dy = (torch.randn((N, 1, 1, 1, K), generator=g, device=device) / math.sqrt(K)).to(torch.bfloat16)
+    dx, dw = torch.empty_like(x), torch.empty_like(w)
+    res = {}
+    for which, name in ((0, "dgrad"), (1, "wgrad")):
+        need = pkg.conv_bwd_point_workspace_bytes(tuple(x.shape), tuple(w.shape), wl.stride,
+                                                  wl.pad, wl.dil, which)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        if which == 0:
+            fn = lambda: pkg.conv_bwd_data_point(dy, w, tuple(x.shape), wl.stride, wl.pad,  # noqa: E731
+                                                 wl.dil, dx=dx, workspace=ws)
+        else:
+            fn = lambda: pkg.conv_bwd_weight_point(x, dy, tuple(w.shape), wl.stride, wl.pad,  # noqa: E731
+                                                   wl.dil, dw=dw, workspace=ws)
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        if pkg.conv_get_device_status() != 0:
+            raise RuntimeError("device status reports a timeout")
+        res[name] = Timer(steps, flush).run(fn)
+    return res
+
+
+# MI355X figures for the patch embedding's backward passes (MIOpen PR #10912,
+# test plan and review thread): context, not a target on this hardware
+PAGE_BACKWARD_MS = {"dgrad": 0.028, "wgrad": 0.040}
+
+
 # ---------------------------------------------------------------- main arm
 
 def main_arm(args):
@@ -425,6 +459,19 @@ def main_arm(args):
             except Exception as e:  # a secondary workload never hides the headline line
                 secondary[name] = {"error": f"{type(e).__name__}: {e}"}
             torch.cuda.empty_cache()
+        # backward data / weights of the patch embedding
+        try:
+            pe = cw.BY_NAME["patch_embed_bf16"]
+            rb = run_backward(pkg, pe, device, args.steps, args.warmup, flush)
+            for name, t in rb.items():
+                m = statistics.mean(t)
+                secondary["patch_embed_bf16_" + name] = {
+                    "tflops": flops(pe) / (m * 1e-3) / 1e12, "ms": m,
+                    "ms_median": statistics.median(t),
+                    "page_mi355x_ms": PAGE_BACKWARD_MS[name]}
+        except Exception as e:
+            secondary["patch_embed_bf16_backward"] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
 
     if rank != 0:
         return

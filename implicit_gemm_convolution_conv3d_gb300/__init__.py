@@ -81,6 +81,12 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd_bias.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp,
                                       vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_fwd_bias.restype = ctypes.c_int
+        lib.conv_bwd_point_workspace_bytes.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int,
+                                                       ctypes.POINTER(ctypes.c_size_t)]
+        lib.conv_bwd_point_workspace_bytes.restype = ctypes.c_int
+        for fn in (lib.conv_bwd_data_point, lib.conv_bwd_weight_point):
+            fn.argtypes = [vp, vp, i64p, i64p, i32p, i32p, i32p, vp, vp, ctypes.c_size_t, vp]
+            fn.restype = ctypes.c_int
         lib.conv_fwd_noalloc.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
                                          vp, vp, vp]
         lib.conv_fwd_noalloc.restype = ctypes.c_int
@@ -316,6 +322,60 @@ def conv_fwd_from_host(x_host: torch.Tensor, w_host: torch.Tensor, stride=1, pad
         ws_bytes, int(chunks), _stream_handle(stream))
     _check(rc, "conv_fwd_from_host")
     return out_host
+
+
+def conv_bwd_point_workspace_bytes(x_shape, w_shape, stride=1, pad=0, dil=1,
+                                   which: int = 0) -> int:
+    """Preferred workspace of conv_bwd_data_point (which=0) or
+    conv_bwd_weight_point (which=1) on the current device."""
+    lib = load_library()
+    b = ctypes.c_size_t(0)
+    _check(lib.conv_bwd_point_workspace_bytes(
+        _I64_5(*x_shape), _I64_5(*w_shape), _I32_3(*_triple(stride)), _I32_3(*_triple(pad)),
+        _I32_3(*_triple(dil)), int(which), ctypes.byref(b)), "conv_bwd_point_workspace_bytes")
+    return int(b.value)
+
+
+def _bwd_call(name, a, b, x_shape, w_shape, stride, pad, dil, out, workspace, stream, which):
+    lib = load_library()
+    for t in (a, b):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("backward passes take bf16 tensors")
+    _require_cuda(a, b, out, workspace)
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    if workspace is None:
+        need = conv_bwd_point_workspace_bytes(x_shape, w_shape, st, pa, di, which)
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    rc = getattr(lib, name)(a.data_ptr(), b.data_ptr(), _I64_5(*x_shape), _I64_5(*w_shape),
+                            _I32_3(*st), _I32_3(*pa), _I32_3(*di), out.data_ptr(),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream))
+    _check(rc, name)
+    return out
+
+
+def conv_bwd_data_point(dy: torch.Tensor, w: torch.Tensor, x_shape, stride=1, pad=0, dil=1,
+                        dx: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Backward data of a point-output conv: dx (x_shape, bf16) from dy
+    [N,1,1,1,K] and w [K,T,R,S,C]."""
+    if dx is None:
+        dx = torch.empty(tuple(x_shape), dtype=torch.bfloat16, device=dy.device)
+    return _bwd_call("conv_bwd_data_point", dy, w, x_shape, tuple(w.shape), stride, pad, dil,
+                     dx, workspace, stream, 0)
+
+
+def conv_bwd_weight_point(x: torch.Tensor, dy: torch.Tensor, w_shape, stride=1, pad=0, dil=1,
+                          dw: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Backward weights of a point-output conv: dw (w_shape, bf16) from x
+    [N,D,H,W,C] and dy [N,1,1,1,K]."""
+    if dw is None:
+        dw = torch.empty(tuple(w_shape), dtype=torch.bfloat16, device=x.device)
+    return _bwd_call("conv_bwd_weight_point", x, dy, tuple(x.shape), w_shape, stride, pad, dil,
+                     dw, workspace, stream, 1)
 
 
 def pack_ncdhw_bf16_to_ndhwc(x: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -357,7 +357,95 @@ __global__ void __launch_bounds__(256) row_repack_kernel(const Word* __restrict_
     }
 }
 
+// ----------------------------------------------------------------- transpose
+// dst[c, r] = src[r, c] for a dense [R, C] 16-bit matrix, into rows of P >= R
+// elements whose tail [R, P) is zero-filled (the backward passes of the
+// point-output GEMM turn their operands K-major this way).  64x64 tiles
+// through shared memory (2-element pitch padding keeps the transposed reads
+// free of bank conflicts).  With C and P even, every global access moves an
+// element pair (a warp: 128 bytes of a row); otherwise single elements.
+__global__ void __launch_bounds__(256) transpose_pad_pairs_kernel(
+    const unsigned short* __restrict__ src, long long R, long long C,
+    unsigned short* __restrict__ dst, long long P, long long tiles_r, long long tiles_c) {
+    griddep_launch_dependents();
+    __shared__ __align__(4) unsigned short t[64][66];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (long long b = blockIdx.x; b < tiles_r * tiles_c; b += gridDim.x) {
+        const long long r0 = (b % tiles_r) * 64, c0 = (b / tiles_r) * 64;
+        const long long c = c0 + 2 * tx;   // this lane's source column pair
+        for (int i = ty; i < 64; i += 8) {
+            const long long r = r0 + i;
+            uint32_t v = 0;
+            if (r < R && c < C) v = __ldg(reinterpret_cast<const uint32_t*>(src + r * C + c));
+            *reinterpret_cast<uint32_t*>(&t[i][2 * tx]) = v;
+        }
+        __syncthreads();
+        const long long r = r0 + 2 * tx;   // this lane's destination column pair
+        for (int i = ty; i < 64; i += 8) {
+            const long long cc = c0 + i;
+            if (cc < C && r < P) {
+                const uint32_t v = static_cast<uint32_t>(t[2 * tx][i]) |
+                                   (static_cast<uint32_t>(t[2 * tx + 1][i]) << 16);
+                *reinterpret_cast<uint32_t*>(dst + cc * P + r) = v;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(256) transpose_pad_kernel(const unsigned short* __restrict__ src,
+                                                            long long R, long long C,
+                                                            unsigned short* __restrict__ dst,
+                                                            long long P, long long tiles_r,
+                                                            long long tiles_c) {
+    griddep_launch_dependents();
+    __shared__ unsigned short t[64][66];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (long long b = blockIdx.x; b < tiles_r * tiles_c; b += gridDim.x) {
+        const long long r0 = (b % tiles_r) * 64, c0 = (b / tiles_r) * 64;
+        for (int i = ty; i < 64; i += 8) {
+            const long long r = r0 + i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const long long c = c0 + 32 * h + tx;
+                t[i][32 * h + tx] = (r < R && c < C) ? __ldg(src + r * C + c) : 0;
+            }
+        }
+        __syncthreads();
+        for (int i = ty; i < 64; i += 8) {
+            const long long c = c0 + i;
+            if (c < C) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long r = r0 + 32 * h + tx;
+                    if (r < P) dst[c * P + r] = t[32 * h + tx][i];
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_pad(const void* src, long long R, long long C, void* dst,
+                                 long long P, int num_sms, cudaStream_t stream) {
+    if (P < R || R <= 0 || C <= 0) return cudaErrorInvalidValue;
+    const long long tiles_r = (P + 63) / 64, tiles_c = (C + 63) / 64;
+    long long blocks = tiles_r * tiles_c;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (C % 2 == 0 && P % 2 == 0) {
+        transpose_pad_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const unsigned short*>(src), R, C, static_cast<unsigned short*>(dst), P,
+            tiles_r, tiles_c);
+        return cudaGetLastError();
+    }
+    transpose_pad_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const unsigned short*>(src), R, C, static_cast<unsigned short*>(dst), P,
+        tiles_r, tiles_c);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, const void* src1,
                               void* dst1, long long rows1, long long src_row_bytes,

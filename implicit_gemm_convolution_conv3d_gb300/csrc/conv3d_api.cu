@@ -177,7 +177,8 @@ struct Plan {
     int grid;
     size_t smem;
     uint32_t tmem_cols;
-    uint32_t epi_bytes;      // TMA-store epilogue staging (0: direct stores)
+    uint32_t epi_bytes;      // epilogue staging (0: direct stores from registers)
+    int epi_mode;            // 0 direct, 1 TMA tensor stores, 2 staged 8- / 4-byte stores
     int pair;                // CTA-pair kernel: 256-row units on clusters of two CTAs
     int msub;                // row sub-tiles per unit sharing each B stage
     size_t ws_bytes;         // split-K workspace needed by this plan
@@ -443,12 +444,17 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     // (a warp's 32 rows x 64 bytes per store, where direct stores would send
     // 32 separate 16-byte pieces per instruction); split-K partials are
     // written directly
-    P->epi_bytes = (splits == 1 && g.K % 8 == 0) ? kEpiStageBytes : 0u;
-    // CONV3D_EPI=tma / direct overrides the epilogue kind (for sweeps)
+    // bf16 rows of an even K whose pitch is not a multiple of 16 bytes are
+    // staged the same way and leave in 8- or 4-byte pieces, several rows per
+    // instruction, instead of 2-byte stores from each lane's own row
+    P->epi_mode = splits > 1 ? 0 : (g.K % 8 == 0 ? 1 : (g.K % 2 == 0 ? 2 : 0));
+    // CONV3D_EPI=tma / staged / direct overrides the epilogue kind (for sweeps)
     if (const char* e = std::getenv("CONV3D_EPI")) {
-        if (e[0] == 't' && splits == 1 && g.K % 8 == 0) P->epi_bytes = kEpiStageBytes;
-        if (e[0] == 'd') P->epi_bytes = 0u;
+        if (e[0] == 't' && splits == 1 && g.K % 8 == 0) P->epi_mode = 1;
+        if (e[0] == 's' && splits == 1 && g.K % 2 == 0) P->epi_mode = 2;
+        if (e[0] == 'd') P->epi_mode = 0;
     }
+    P->epi_bytes = P->epi_mode ? kEpiStageBytes : 0u;
     // pipeline depth from the shared-memory budget (a pair CTA holds half of B)
     const size_t stage_bytes = static_cast<size_t>(P->msub * kBM + (BN >> P->pair)) * BK;
     const size_t fixed = 1024 + 256 + P->epi_bytes;
@@ -506,7 +512,7 @@ int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuin
 // 32x32 boxes with the 64-byte swizzle the epilogue writes.
 int build_out_map(const Geo& g, const Plan& P, void* out, TMaps* tm) {
     std::memset(tm->c, 0, sizeof tm->c);
-    if (!P.epi_bytes) return CONV_OK;
+    if (P.epi_mode != 1) return CONV_OK;
     const cuuint64_t row = static_cast<cuuint64_t>(g.K) * 2;
     if (P.amode == AM_TEMPORAL) {
         const cuuint64_t hw = static_cast<cuuint64_t>(P.HW);
@@ -672,6 +678,7 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.sbo = static_cast<uint32_t>(8 * box_bytes(P.BK));
     k.tmem_cols = P.tmem_cols;
     k.epi_bytes = P.epi_bytes;
+    k.epi_mode = P.epi_mode;
     k.pair = P.pair;
     k.msub = P.msub;
     k.ga = static_cast<const unsigned char*>(x);
@@ -686,6 +693,43 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.bias = bias;
     k.status = status;
     k.wait_ns = g_wait_ns;
+}
+
+// ------------------------------------------------------------ backward passes
+// Point-output geometry (MIOpen PR #10912): zero padding and the input
+// spatially equal to the filter, so each batch element has one output
+// position (a valid geometry with D == T forces unit dilation or T == 1).
+bool is_point_output(const Geo& g) {
+    return g.pd == 0 && g.ph == 0 && g.pw == 0 && g.D == g.T && g.H == g.R && g.W == g.S;
+}
+
+size_t round256(long long b) { return static_cast<size_t>((b + 255) / 256 * 256); }
+
+// Checks shared by the two backward entry points; fills the GEMM extents
+// N (batch), K (filters) and J = T*R*S*C.
+int bwd_setup(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+              const int pad[3], const int dil[3], const void* a, const void* b, void* out,
+              void* workspace, long long* N, long long* K, long long* J) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!a || !b || !out) {
+        set_error("null tensor pointer");
+        return CONV_ERR_INVALID;
+    }
+    if (!aligned16(a) || !aligned16(b) || !aligned16(out) || (workspace && !aligned16(workspace))) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    if (!is_point_output(g)) {
+        set_error("backward passes cover point-output shapes only (input spatially equal to "
+                  "the filter, zero padding)");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    *N = g.N;
+    *K = g.K;
+    *J = g.T * g.R * g.S * g.C;
+    return CONV_OK;
 }
 
 // ------------------------------------------------------------ host-operand pipeline
@@ -1190,6 +1234,91 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
     e = launch_pack(in, dims[0], dims[1], S, out, 1, amax, scale_out, dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return CONV_OK;
+}
+
+int conv_bwd_point_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
+                                   const int stride[3], const int pad[3], const int dil[3],
+                                   int which, size_t* bytes) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!bytes || (which != 0 && which != 1)) {
+        set_error("bytes must be non-NULL and which 0 (data) or 1 (weights)");
+        return CONV_ERR_INVALID;
+    }
+    if (!is_point_output(g)) {
+        set_error("backward passes cover point-output shapes only");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    const long long N = g.N, K = g.K, J = g.T * g.R * g.S * g.C;
+    const int one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+    size_t inner = 0, head;
+    if (which == 0) {
+        const int64_t xi[5] = {N, 1, 1, 1, K}, wi[5] = {J, 1, 1, 1, K};
+        head = round256(J * K * 2);
+        rc = conv_fwd_plan(xi, wi, one, zero, one, CONV_DTYPE_BF16, 0, nullptr, nullptr, nullptr,
+                           nullptr, nullptr, nullptr, &inner);
+    } else {
+        const long long Np = (N + 7) / 8 * 8;
+        const int64_t xi[5] = {K, 1, 1, 1, Np}, wi[5] = {J, 1, 1, 1, Np};
+        head = round256(K * Np * 2) + round256(J * Np * 2);
+        rc = conv_fwd_plan(xi, wi, one, zero, one, CONV_DTYPE_BF16, 0, nullptr, nullptr, nullptr,
+                           nullptr, nullptr, nullptr, &inner);
+    }
+    if (rc) return rc;
+    *bytes = head + inner;
+    return CONV_OK;
+}
+
+int conv_bwd_data_point(const void* dy, const void* w, const int64_t x_dims[5],
+                        const int64_t w_dims[5], const int stride[3], const int pad[3],
+                        const int dil[3], void* dx, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+    long long N, K, J;
+    int rc = bwd_setup(x_dims, w_dims, stride, pad, dil, dy, w, dx, workspace, &N, &K, &J);
+    if (rc) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    const size_t head = round256(J * K * 2);
+    if (!workspace || workspace_bytes < head) {
+        set_error("workspace smaller than the transposed weights (see conv_bwd_point_workspace_bytes)");
+        return CONV_ERR_INVALID;
+    }
+    // w [K, J] -> w^T [J, K]: the GEMM dx[N, J] = dy[N, K] w[K, J] then has
+    // both operands K-major, and is the pointwise forward conv of dy by w^T
+    cudaError_t e = launch_transpose_pad(w, K, J, workspace, K, dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+    const int64_t xi[5] = {N, 1, 1, 1, K}, wi[5] = {J, 1, 1, 1, K};
+    const int one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+    return conv_fwd(dy, xi, workspace, wi, one, zero, one, CONV_DTYPE_BF16, nullptr, nullptr, dx,
+                    static_cast<unsigned char*>(workspace) + head, workspace_bytes - head, stream);
+}
+
+int conv_bwd_weight_point(const void* x, const void* dy, const int64_t x_dims[5],
+                          const int64_t w_dims[5], const int stride[3], const int pad[3],
+                          const int dil[3], void* dw, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+    long long N, K, J;
+    int rc = bwd_setup(x_dims, w_dims, stride, pad, dil, x, dy, dw, workspace, &N, &K, &J);
+    if (rc) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    // the reduction runs over the batch: dy^T [K, Np] and x^T [J, Np], rows
+    // zero-padded to Np (a multiple of 8 elements, 16 bytes)
+    const long long Np = (N + 7) / 8 * 8;
+    const size_t dyt = round256(K * Np * 2), head = dyt + round256(J * Np * 2);
+    if (!workspace || workspace_bytes < head) {
+        set_error("workspace smaller than the transposed operands (see conv_bwd_point_workspace_bytes)");
+        return CONV_ERR_INVALID;
+    }
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    cudaError_t e = launch_transpose_pad(dy, N, K, wsb, Np, dev->num_sms, stream);
+    if (e == cudaSuccess) e = launch_transpose_pad(x, N, J, wsb + dyt, Np, dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+    const int64_t xi[5] = {K, 1, 1, 1, Np}, wi[5] = {J, 1, 1, 1, Np};
+    const int one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+    return conv_fwd(wsb, xi, wsb + dyt, wi, one, zero, one, CONV_DTYPE_BF16, nullptr, nullptr, dw,
+                    wsb + head, workspace_bytes - head, stream);
 }
 
 int conv_get_device_status(int* device_status) {

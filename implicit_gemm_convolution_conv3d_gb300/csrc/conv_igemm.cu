@@ -109,6 +109,12 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+    uint2 r;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 prefetch_tmap(&tm.b[ph]);
             }
         }
-        if (p.epi_bytes)
+        if (p.epi_mode == 1)
             for (int ph = 0; ph < p.phases; ++ph) prefetch_tmap(&tm.c[ph]);
     }
     if (warp == 1) {
@@ -681,7 +687,9 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                         };
                         const uint32_t buf = bufs + static_cast<uint32_t>(epi_iter & 1) * kEpiChunkBytes;
                         ++epi_iter;
-                        if (lane == 0) bulk_wait_read<1>();   // this buffer's last store has read it
+                        // this buffer's last TMA store has read it (staged
+                        // stores read it back synchronously)
+                        if (p.epi_mode == 1 && lane == 0) bulk_wait_read<1>();
                         __syncwarp();
                         const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 64u;
                         const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
@@ -693,14 +701,51 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                             const uint32_t w3 = pack_bf16x2(val(8 * c + 6), val(8 * c + 7));
                             st_shared_v4(rowaddr + ((static_cast<uint32_t>(c) ^ sw) << 4), w0, w1, w2, w3);
                         }
-                        fence_proxy_async_smem();
+                        if (p.epi_mode == 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (AMODE == AM_TEMPORAL)
+                                    tma_store_3d(&tm.c[0], buf, n0, wrow0, plane);
+                                else
+                                    tma_store_2d(&tm.c[rphase], buf, n0, wrow0);
+                                bulk_commit();
+                            }
+                            return;
+                        }
+                        // staged stores (rows whose byte pitch is not a
+                        // multiple of 16): read the chunk back in row order
+                        // and write 8-byte pieces, 4 rows of 64 bytes per
+                        // instruction (K % 4 == 0), else 4-byte pieces, 2 rows
                         __syncwarp();
-                        if (lane == 0) {
-                            if (AMODE == AM_TEMPORAL)
-                                tma_store_3d(&tm.c[0], buf, n0, wrow0, plane);
-                            else
-                                tma_store_2d(&tm.c[rphase], buf, n0, wrow0);
-                            bulk_commit();
+                        const bool wide = (p.K & 3) == 0;
+                        const int rows_per = wide ? 4 : 2, lanes_per = 32 / rows_per;
+                        const int piece = lane % lanes_per;             // 8- or 4-byte piece
+                        for (int rr = lane / lanes_per; rr < 32; rr += rows_per) {
+                            const int lr = wrow0 + rr;                  // row within the phase / plane
+                            long long orow;
+                            bool ok;
+                            if (AMODE == AM_TEMPORAL) {
+                                ok = lr < p.HW;
+                                orow = static_cast<long long>(plane) * p.HW + lr;
+                            } else {
+                                ok = lr < phase_rows;
+                                orow = static_cast<long long>(lr) * p.phases + rphase;
+                            }
+                            const int col = n0 + (wide ? 4 : 2) * piece;
+                            if (!ok || col >= p.K) continue;
+                            const int byte = (wide ? 8 : 4) * piece;     // within the 64-byte row
+                            const uint32_t a = buf + static_cast<uint32_t>(rr) * 64u +
+                                               ((static_cast<uint32_t>((byte >> 4) ^ ((rr >> 1) & 3)) << 4) |
+                                                static_cast<uint32_t>(byte & 15));
+                            __nv_bfloat16* dst = out + orow * p.K + col;
+                            if (wide) {
+                                *reinterpret_cast<uint2*>(dst) = ld_shared_v2(a);
+                            } else {
+                                uint32_t v1;
+                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v1) : "r"(a) : "memory");
+                                *reinterpret_cast<uint32_t*>(dst) = v1;
+                            }
                         }
                     };
                     // chunks holding columns below K; the TMEM load of chunk
@@ -757,7 +802,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
         // the staging buffers are read out before the CTA leaves; the stores'
         // global writes complete with the grid (the next kernel in the
         // stream, or a dependent launch's wait, sees them)
-        if (p.epi_bytes && lane == 0) bulk_wait_read<0>();
+        if (p.epi_mode == 1 && lane == 0) bulk_wait_read<0>();
     } else if (kGather) {
         // ------------------------------------------------------ row gather
         const int g = threadIdx.x - (2 + kEpiWarps) * 32;

@@ -55,7 +55,8 @@ struct KParams {
     uint32_t layout;    // smem descriptor swizzle code
     uint32_t sbo;       // smem descriptor stride byte offset (8 rows)
     uint32_t tmem_cols; // allocated TMEM columns (power of two >= 2*BN)
-    uint32_t epi_bytes; // shared staging of the TMA-store epilogue (0: direct stores)
+    uint32_t epi_bytes; // shared staging of the epilogue (0: direct stores from registers)
+    int epi_mode;       // 0 direct stores, 1 TMA tensor stores, 2 staged 8- / 4-byte stores
     int pair;           // 1: CTA-pair kernel (cluster of 2, 256-row units)
     int msub;           // row sub-tiles per unit sharing each B stage (1 or 2)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
@@ -95,6 +96,11 @@ cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, con
                               void* dst1, long long rows1, long long src_row_bytes,
                               long long dst_row_bytes, long long dst1_shift_bytes, int num_sms,
                               cudaStream_t stream);
+
+// 16-bit transpose: dst[c, r] = src[r, c] for src [R, C] dense, dst rows of
+// P >= R elements with [R, P) zero-filled.
+cudaError_t launch_transpose_pad(const void* src, long long R, long long C, void* dst,
+                                 long long P, int num_sms, cudaStream_t stream);
 
 // Bytes of split-K partials the plan for this problem uses (0 without split-K).
 size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],

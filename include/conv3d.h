@@ -155,6 +155,36 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
                        void* out_host, void* x_dev, void* w_dev, void* out_dev, void* workspace,
                        size_t workspace_bytes, int chunks, cudaStream_t stream);
 
+/* Backward passes of the point-output conv (MIOpen PR #10912 "Use a single
+ * GEMM for point-output conv in all three directions": backward data and
+ * backward weights of patch-embedding shapes, each one GEMM).  Shapes: zero
+ * padding and x spatially equal to w's filter (D == T, H == R, W == S), so
+ * the output is [N,1,1,1,K]; anything else returns CONV_ERR_UNSUPPORTED.
+ * bf16 operands, fp32 accumulation, bf16 results; J = T*R*S*C.
+ *   conv_bwd_data_point:   dx[n, j] = sum_k dy[n, k] * w[k, j]
+ *       dy device [N,1,1,1,K]; w device KTRSC; dx device NDHWC (x's shape)
+ *   conv_bwd_weight_point: dw[k, j] = sum_n dy[n, k] * x[n, j]
+ *       x device NDHWC; dy device [N,1,1,1,K]; dw device KTRSC (w's shape)
+ * x_dims / w_dims / stride / pad / dil describe the forward conv.  Both
+ * transpose their operands K-major into `workspace` (dx: w^T [J, K]; dw:
+ * dy^T [K, N'] and x^T [J, N'], N' = N rounded up to 8, zero-padded) and run
+ * the pointwise forward GEMM on them (split-K over the batch for dw when the
+ * rest of the workspace holds the partials).  A workspace smaller than the
+ * transposes returns CONV_ERR_INVALID; conv_bwd_point_workspace_bytes
+ * (which = 0 data, 1 weights) gives the preferred size.  Outputs are fully
+ * overwritten; asynchronous on `stream`. */
+int conv_bwd_point_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
+                                   const int stride[3], const int pad[3], const int dil[3],
+                                   int which, size_t* bytes);
+int conv_bwd_data_point(const void* dy, const void* w, const int64_t x_dims[5],
+                        const int64_t w_dims[5], const int stride[3], const int pad[3],
+                        const int dil[3], void* dx, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+int conv_bwd_weight_point(const void* x, const void* dy, const int64_t x_dims[5],
+                          const int64_t w_dims[5], const int stride[3], const int pad[3],
+                          const int dil[3], void* dw, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
 /* Layout pack: out[n,d,h,w,c] = in[n,c,d,h,w] (bit copy).
  *   in   device, bf16 NCDHW, dims = {N, C, D, H, W}
  *   out  device, bf16 NDHWC [N,D,H,W,C]

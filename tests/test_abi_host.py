@@ -175,3 +175,22 @@ def test_from_host_argument_checks(pkg):
     assert call(hp, None, 0) == pkg.CONV_ERR_INVALID
     assert call(hp, good, -1) == pkg.CONV_ERR_INVALID
     assert call(hp, odd, 0) == pkg.CONV_ERR_INVALID
+
+
+def test_backward_argument_checks(pkg):
+    """The point-output backward entry points reject null operands, misaligned
+    buffers and non-point-output shapes before touching the device."""
+    lib = ctypes.CDLL(pkg.LIB_PATH)
+    I5, I3 = ctypes.c_int64 * 5, ctypes.c_int * 3
+    pt_x, pt_w, st = I5(4, 1, 4, 4, 8), I5(8, 1, 4, 4, 8), I3(1, 4, 4)
+    zero, one = I3(0, 0, 0), I3(1, 1, 1)
+    a, b = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
+    for fn in (lib.conv_bwd_data_point, lib.conv_bwd_weight_point):
+        fn.restype = ctypes.c_int
+        assert fn(None, b, pt_x, pt_w, st, zero, one, a, a, ctypes.c_size_t(0), None) == \
+            pkg.CONV_ERR_INVALID
+        assert fn(a, b, pt_x, pt_w, st, zero, one, ctypes.c_void_p((1 << 20) + 4), a,
+                  ctypes.c_size_t(0), None) == pkg.CONV_ERR_INVALID
+        # a 3x3 filter over an 8x8 input has many output positions
+        assert fn(a, b, I5(2, 1, 8, 8, 16), I5(32, 1, 3, 3, 16), one, zero, one, a, a,
+                  ctypes.c_size_t(1 << 20), None) == pkg.CONV_ERR_UNSUPPORTED
