@@ -439,7 +439,8 @@ def main_arm(args):
     secondary = {}
     if not args.no_secondary:
         names = [n for n in ("fp8_conv3d_1x3x3", "temporal_3x1x1_bf16_big", "patch_embed_bf16",
-                             "tiny_conv3d_bf16") if n != wl.name]
+                             "tiny_conv3d_bf16", "vit_patch16_bf16", "vit_patch14_bf16")
+                 if n != wl.name]
         # the bias epilogue on the headline and on the epilogue-heavy patch embedding
         names += [wl.name + "+bias", "patch_embed_bf16+bias"]
         for name in names:

@@ -12,7 +12,9 @@ sample indices 3000+i for workload i.  The shapes are those of the
 convolution workloads the method is measured on: a tiny 3x3x3 case, the
 ViT-style 14x14 stride-14 patch embedding, a 2048-channel video conv, the
 1024-channel fp8 1x3x3 conv on an NCDHW bf16 input, and a 640-channel 3x1x1
-temporal conv whose tensors exceed 2^31 elements.
+temporal conv whose tensors exceed 2^31 elements.  Two more cover patch
+embeddings with many patches per image (16x16 and 14x14 patches of 224x224
+RGB images: stride == filter, output 14x14 / 16x16 per image).
 """
 from __future__ import annotations
 
@@ -86,7 +88,16 @@ PROFILE_WORKLOADS = [
              (1, 1, 1), (1, 0, 0)),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
+# Patch embeddings with many patches per image (stride == filter, output
+# spatially larger than 1x1): the gathered-patch GEMM.
+PATCH_WORKLOADS = [
+    Workload("vit_patch16_bf16", 8, (64, 1, 224, 224, 3), (768, 1, 16, 16, 3), (1, 16, 16),
+             (0, 0, 0)),
+    Workload("vit_patch14_bf16", 9, (64, 1, 224, 224, 3), (1024, 1, 14, 14, 3), (1, 14, 14),
+             (0, 0, 0)),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS + PATCH_WORKLOADS}
 
 
 def randn_bf16(shape, seed: int, std: float = 1.0, device="cpu",

@@ -33,7 +33,7 @@ CONV_ERR_TIMEOUT = 4
 CONV_DTYPE_BF16 = 0
 CONV_DTYPE_FP8_E4M3 = 1
 
-CLASS_NAMES = {0: "generic", 1: "temporal", 2: "point_gemm"}
+CLASS_NAMES = {0: "generic", 1: "temporal", 2: "point_gemm", 3: "patch_gemm"}
 
 _I64_5 = ctypes.c_int64 * 5
 _I32_3 = ctypes.c_int * 3

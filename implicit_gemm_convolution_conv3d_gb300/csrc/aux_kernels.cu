@@ -426,7 +426,107 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(const unsigned short
     }
 }
 
+// ----------------------------------------------------------------- patch gather
+// Convolutions whose stride equals the filter (zero padding): the patches do
+// not overlap, and GEMM row m = (n, od, oh, ow) is the patch
+// x[n, od*T .. +T, oh*R .. +R, ow*S .. +S, :]: T*R segments of S*C contiguous
+// elements.  Each row is written to `a` with a pitch of `pitch` words, its
+// tail zeroed; one warp per row.  The lanes walk the row's words 32 apart,
+// stepping their (segment, offset) position without divisions, and keep 8
+// loads in flight before storing.  Counts are in Word units (a Word holds
+// one or more elements; segments and rows are whole Words).
+template <typename Word>
+__device__ __forceinline__ Word zero_word() {
+    Word z;
+    memset(&z, 0, sizeof z);
+    return z;
+}
+
+template <typename Word>
+__global__ void __launch_bounds__(256) patch_gather_kernel(
+    const Word* __restrict__ x, Word* __restrict__ a, long long M, long long D, long long H,
+    long long Wrow, long long seg, int T, int R, int Do, int Ho, int Wo, long long pitch) {
+    griddep_launch_dependents();
+    constexpr int kBatch = 8;
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long row_words = static_cast<long long>(T) * R * seg;
+    const long long wrap = (H - R + 1) * Wrow;   // from segment (t, R-1) to (t+1, 0)
+    for (long long m = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         m < M; m += nwarps) {
+        const long long ow = m % Wo;
+        long long q = m / Wo;
+        const long long oh = q % Ho;
+        q /= Ho;
+        const long long od = q % Do;
+        const long long n = q / Do;
+        Word* dst = a + m * pitch;
+        // this lane's position: segment base pointer and offset within it
+        const Word* sb = x + ((n * D + od * T) * H + oh * R) * Wrow + ow * seg;
+        long long off = lane;
+        int r = 0;
+        auto normalise = [&]() {
+            while (off >= seg) {
+                off -= seg;
+                if (++r == R) {
+                    r = 0;
+                    sb += wrap;
+                } else {
+                    sb += Wrow;
+                }
+            }
+        };
+        normalise();
+        for (long long i = lane; i < row_words; i += 32 * kBatch) {
+            const Word* src[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                src[u] = sb + off;
+                off += 32;
+                normalise();
+            }
+            Word v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                v[u] = (i + 32 * u < row_words) ? __ldg(src[u]) : zero_word<Word>();
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (i + 32 * u < row_words) dst[i + 32 * u] = v[u];
+        }
+        for (long long i = row_words + lane; i < pitch; i += 32) dst[i] = zero_word<Word>();
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
+                                long long W, long long C, int T, int R, int S, int Do, int Ho,
+                                int Wo, void* a, long long pitch_bytes, int num_sms,
+                                cudaStream_t stream) {
+    const long long M = N * Do * Ho * Wo;
+    const long long seg_b = static_cast<long long>(S) * C * elt, row_b = W * C * elt;
+    long long blocks = (M + 7) / 8;
+    const long long cap = static_cast<long long>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (seg_b % 16 == 0 && row_b % 16 == 0 && pitch_bytes % 16 == 0)
+        patch_gather_kernel<uint4><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint4*>(x), static_cast<uint4*>(a), M, D, H, row_b / 16,
+            seg_b / 16, T, R, Do, Ho, Wo, pitch_bytes / 16);
+    else if (seg_b % 4 == 0 && row_b % 4 == 0 && pitch_bytes % 4 == 0)
+        patch_gather_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint32_t*>(x), static_cast<uint32_t*>(a), M, D, H, row_b / 4,
+            seg_b / 4, T, R, Do, Ho, Wo, pitch_bytes / 4);
+    else if (elt == 2)
+        patch_gather_kernel<unsigned short><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const unsigned short*>(x), static_cast<unsigned short*>(a), M, D, H,
+            row_b / 2, seg_b / 2, T, R, Do, Ho, Wo, pitch_bytes / 2);
+    else
+        patch_gather_kernel<unsigned char><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const unsigned char*>(x), static_cast<unsigned char*>(a), M, D, H, row_b,
+            seg_b, T, R, Do, Ho, Wo, pitch_bytes);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_pad(const void* src, long long R, long long C, void* dst,
                                  long long P, int num_sms, cudaStream_t stream) {

@@ -227,6 +227,39 @@ void force_tile(int* bn, int* bk, int* st, int* grp, int* spl) {
     if (v[4] > 0) *spl = v[4];
 }
 
+bool gemm_amode(int amode) { return amode == AM_GEMM_TMA || amode == AM_GEMM_GATHER; }
+
+// Temporal class: T x 1 x 1 filter, unit H/W stride, no H/W padding.
+bool temporal_class(const Geo& g) {
+    return g.R == 1 && g.S == 1 && g.sh == 1 && g.sw == 1 && g.ph == 0 && g.pw == 0;
+}
+
+// im2col descriptor limits for a 5-D tensor: traversal stride <= 8, box
+// corners in [-16, 15], tap offsets below 32.
+bool im2col_fits(const Geo& g) {
+    const int pads[3] = {g.pd, g.ph, g.pw};
+    const int sts[3] = {g.sd, g.sh, g.sw};
+    const long long ext[3] = {g.dd * (g.T - 1), g.dh * (g.R - 1), g.dw * (g.S - 1)};
+    for (int i = 0; i < 3; ++i) {
+        const long long up = pads[i] - ext[i];
+        if (sts[i] > 8 || pads[i] > 16 || up < -16 || up > 15 || ext[i] > 31) return false;
+    }
+    return true;
+}
+
+// Non-overlapping patches (stride == filter, zero padding; dilation can only
+// matter for a filter extent above 1) that neither implicit class can read:
+// channel rows not a multiple of 16 bytes, or strides beyond the im2col box.
+// Patches covering all of x are the point-output class instead.
+bool patch_gather_class(const Geo& g, long long elt) {
+    const bool patches = g.pd == 0 && g.ph == 0 && g.pw == 0 && g.sd == g.T && g.sh == g.R &&
+                         g.sw == g.S && (g.dd == 1 || g.T == 1) && (g.dh == 1 || g.R == 1) &&
+                         (g.dw == 1 || g.S == 1);
+    if (!patches) return false;
+    const bool implicit = (g.C * elt) % 16 == 0 && (temporal_class(g) || im2col_fits(g));
+    return !implicit;
+}
+
 // ws_avail: workspace bytes the call can use (SIZE_MAX: plan the preferred
 // layout and report its size).  Split-K partials and the aligned operand
 // copies of the point-output GEMM are used only when they fit.
@@ -289,6 +322,24 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
             set_error("point-output GEMM needs T*R*S*C*elem_bytes %% 4 == 0");
             return CONV_ERR_UNSUPPORTED;
         }
+    } else if (patch_gather_class(g, elt)) {
+        // stride == filter, output larger than one point, and the implicit
+        // classes cannot read x (channel rows or strides TMA cannot address):
+        // gather the non-overlapping patches into GEMM rows, then one GEMM
+        P->cls = CONV_CLASS_PATCH_GEMM;
+        P->M = g.N * g.Do * g.Ho * g.Wo;
+        rg = g.T * g.R * g.S * g.C;
+        P->g_row_bytes = rg * elt;
+        P->tma_row_bytes = (P->g_row_bytes + 15) / 16 * 16;
+        P->amode = AM_GEMM_TMA;
+        P->repack = 2;
+        P->repack_bytes = static_cast<size_t>((P->M * P->tma_row_bytes + 255) / 256 * 256) +
+                          static_cast<size_t>((g.K * P->tma_row_bytes + 255) / 256 * 256);
+        if (ws_avail < P->repack_bytes) {
+            set_error("the patch gather needs %s%lld bytes of workspace (conv_fwd_plan)", "",
+                      static_cast<long long>(P->repack_bytes));
+            return CONV_ERR_INVALID;
+        }
     } else {
         if ((g.C * elt) % 16 != 0) {
             set_error("implicit GEMM needs C*elem_bytes %% 16 == 0");
@@ -328,7 +379,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     int BN = pick_bn(g.K);
     int BK = (P->amode == AM_GEMM_GATHER)
                  ? 128
-                 : pick_bk(P->cls == CONV_CLASS_POINT_GEMM ? P->tma_row_bytes : g.C * elt);
+                 : pick_bk(gemm_amode(P->amode) ? P->tma_row_bytes : g.C * elt);
     // raster group 1: a unit's row block meets every column tile before the
     // next row block starts (best on the measured workloads)
     int stages = 0, group_m = 1, splits = 0, pair_pref = -1, msub_pref = 0;
@@ -351,7 +402,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     P->BK = BK;
     P->group_m = group_m;
 
-    if (P->cls == CONV_CLASS_POINT_GEMM) {
+    if (gemm_amode(P->amode)) {
         P->taps = 1;
         P->k_steps = static_cast<int>((P->tma_row_bytes + BK - 1) / BK);
     } else {
@@ -991,7 +1042,25 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
         return rc;
     const void* xa = x;
     const void* wa = w;
-    if (P.repack && P.phases == 2) {
+    if (P.repack == 2) {
+        // the patches gathered into GEMM rows, then the weights copied to the
+        // same 16-byte pitch, at the head of the workspace
+        unsigned char* wsb = static_cast<unsigned char*>(workspace);
+        void* wc = wsb + (P.M * P.tma_row_bytes + 255) / 256 * 256;
+        cudaError_t e = launch_patch_gather(
+            x, static_cast<int>(P.elt), g.N, g.D, g.H, g.W, g.C, static_cast<int>(g.T),
+            static_cast<int>(g.R), static_cast<int>(g.S), static_cast<int>(g.Do),
+            static_cast<int>(g.Ho), static_cast<int>(g.Wo), wsb, P.tma_row_bytes, dev->num_sms,
+            stream);
+        // each filter row is one patch of T*R*S*C elements (any byte count)
+        if (e == cudaSuccess)
+            e = launch_patch_gather(w, static_cast<int>(P.elt), g.K, 1, 1, 1,
+                                    g.T * g.R * g.S * g.C, 1, 1, 1, 1, 1, 1, wc,
+                                    P.tma_row_bytes, dev->num_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "patch gather launch");
+        xa = wsb;
+        wa = wc;
+    } else if (P.repack && P.phases == 2) {
         // the two aligned weight copies (plain, shifted by 8 bytes) at the head
         // of the workspace; x is read in place
         unsigned char* wsb = static_cast<unsigned char*>(workspace);
@@ -1078,7 +1147,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
     const unsigned char* od = static_cast<const unsigned char*>(out_dev);
 
     int bounds[kMaxChunks + 1];
-    const bool chunkable = P.cls != CONV_CLASS_POINT_GEMM && P.splits == 1;
+    const bool chunkable = !gemm_amode(P.amode) && P.splits == 1;
     const int n = chunkable ? plan_chunks(P, chunks, bounds) : 1;
     cudaError_t e;
     if (n == 1) {

@@ -97,6 +97,13 @@ cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, con
                               long long dst_row_bytes, long long dst1_shift_bytes, int num_sms,
                               cudaStream_t stream);
 
+// Patch gather of a stride == filter convolution: row (n, od, oh, ow) of `a`
+// (pitch_bytes per row, tail zeroed) is the patch's T*R*S*C elements.
+cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
+                                long long W, long long C, int T, int R, int S, int Do, int Ho,
+                                int Wo, void* a, long long pitch_bytes, int num_sms,
+                                cudaStream_t stream);
+
 // 16-bit transpose: dst[c, r] = src[r, c] for src [R, C] dense, dst rows of
 // P >= R elements with [R, P) zero-filled.
 cudaError_t launch_transpose_pad(const void* src, long long R, long long C, void* dst,

@@ -62,6 +62,8 @@ typedef enum {
     CONV_CLASS_GENERIC = 0,   /* implicit GEMM, A gathered by TMA im2col */
     CONV_CLASS_TEMPORAL = 1,  /* T x 1 x 1 filter, unit H/W stride, no H/W pad: tiled TMA rows */
     CONV_CLASS_POINT_GEMM = 2,/* point-output / pointwise conv: one plain GEMM */
+    CONV_CLASS_PATCH_GEMM = 3,/* stride == filter patches the implicit classes cannot read:
+                                 gathered into GEMM rows in the workspace, then one GEMM */
     CONV_CLASS_NONE = -1
 } conv_class;
 
@@ -100,9 +102,12 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
  *            NULL/0: split-K is then not used); size from conv_fwd_plan
  * Coverage: C*elem_bytes % 16 == 0 for the implicit-GEMM classes; the
  * point-output class needs T*R*S*C*elem_bytes % 4 == 0; strides <= 8 and
- * pads <= 15 for the im2col class.  Anything else: CONV_ERR_UNSUPPORTED
- * (there is no fallback path).  Device-side wait timeouts are reported by
- * conv_get_device_status, not by this return value. */
+ * pads <= 15 for the im2col class.  Convolutions with stride == filter and
+ * zero padding outside those limits (e.g. 14x14 or 16x16 patches of an RGB
+ * image) take the patch class, whose gathered rows need workspace
+ * (conv_fwd_plan's size; a smaller one returns CONV_ERR_INVALID).  Anything
+ * else: CONV_ERR_UNSUPPORTED (there is no fallback path).  Device-side wait
+ * timeouts are reported by conv_get_device_status, not by this return value. */
 int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
              const int stride[3], const int pad[3], const int dil[3], int dtype,
              const float* scale_x, const float* scale_w, void* out, void* workspace,

@@ -81,10 +81,17 @@ def test_plan_classifies_the_workloads(pkg):
     # input spatial in (filter, 2*filter-1] with stride == filter: rows are not contiguous
     p = pkg.conv_fwd_plan((8, 5, 5, 5, 16), (32, 4, 4, 4, 16), 4, 0, 1, 0, sms)
     assert p["class"] == "generic"
-    # the im2col traversal stride is at most 8
+    # the im2col traversal stride is at most 8; non-overlapping patches beyond
+    # it (stride == filter) are gathered into GEMM rows instead
     with pytest.raises(pkg.ConvError) as e:
-        pkg.conv_fwd_plan((4, 1, 20, 20, 16), (32, 1, 14, 14, 16), (1, 14, 14), 0, 1, 0, sms)
+        pkg.conv_fwd_plan((4, 1, 20, 20, 16), (32, 1, 3, 3, 16), (1, 14, 14), 0, 1, 0, sms)
     assert e.value.status == pkg.CONV_ERR_UNSUPPORTED
+    p = pkg.conv_fwd_plan((4, 1, 20, 20, 16), (32, 1, 14, 14, 16), (1, 14, 14), 0, 1, 0, sms)
+    assert p["class"] == "patch_gemm" and p["workspace_bytes"] > 0
+    # ViT-style patch embeddings: 16x16 and 14x14 patches of RGB images
+    for k in (16, 14):
+        p = pkg.conv_fwd_plan((8, 1, 224, 224, 3), (768, 1, k, k, 3), (1, k, k), 0, 1, 0, sms)
+        assert p["class"] == "patch_gemm"
     assert {w.name for w in cw.WORKLOADS} >= {"tiny_conv3d_bf16", "video_conv3d_bf16"}
 
 

@@ -404,3 +404,43 @@ def test_bias_zero_weights_is_exact(pkg):
         y = pkg.conv_fwd(x, w, 1, 1, 1, split_k=split_k, bias=b)
         torch.cuda.synchronize()
         assert torch.equal(y.float(), b.to(torch.bfloat16).float().expand_as(y))
+
+
+# Non-overlapping patches (stride == filter, zero padding) that the implicit
+# classes cannot read: RGB channels (6-byte rows), strides above the im2col
+# limit; leftover rows / columns / frames past the last whole patch; a
+# 3-D filter; odd patch lengths (2-byte gather).
+PATCH_CASES = [
+    ((2, 1, 32, 48, 3), (64, 1, 16, 16, 3), (1, 16, 16)),
+    ((3, 1, 44, 30, 3), (40, 1, 14, 14, 3), (1, 14, 14)),
+    ((2, 5, 32, 37, 3), (48, 2, 16, 16, 3), (2, 16, 16)),
+    ((2, 1, 40, 40, 16), (72, 1, 10, 10, 16), (1, 10, 10)),
+    ((1, 1, 20, 20, 16), (32, 1, 14, 14, 16), (1, 14, 14)),
+    ((4, 1, 56, 56, 3), (96, 1, 7, 7, 3), (1, 7, 7)),
+    ((2, 1, 224, 224, 3), (256, 1, 16, 16, 3), (1, 16, 16)),
+]
+
+
+@pytest.mark.parametrize("case", PATCH_CASES, ids=[str(i) for i in range(len(PATCH_CASES))])
+def test_patch_gemm(pkg, case):
+    xs, ws, st = case
+    assert pkg.conv_fwd_plan(xs, ws, st, 0, 1)["class"] == "patch_gemm"
+    _run_and_check(pkg, xs, ws, st, 0, 1, seed=200 + PATCH_CASES.index(case),
+                   what=f"patch {case}")
+    # also with a bias and without split-K (workspace holding the gather only)
+    x, w = _inputs(xs, ws, 210 + PATCH_CASES.index(case))
+    b = torch.linspace(-1.0, 1.0, ws[0], dtype=torch.float32, device="cuda")
+    plan = pkg.conv_fwd_plan(xs, ws, st, 0, 1)
+    y = pkg.conv_fwd(x, w, st, 0, 1, bias=b)
+    torch.cuda.synchronize()
+    ref = oracle.conv3d(bits16(x), bits16(w), st, (0, 0, 0), (1, 1, 1),
+                        bias=b.double().cpu().numpy())
+    assert_close(as_f64(y), ref, f"patch+bias {case} {plan}")
+
+
+def test_patch_gemm_needs_workspace(pkg):
+    x, w = _inputs((2, 1, 32, 48, 3), (64, 1, 16, 16, 3), 220)
+    with pytest.raises(pkg.ConvError) as e:
+        pkg.conv_fwd(x, w, (1, 16, 16), 0, 1, split_k=False)
+    assert e.value.status == pkg.CONV_ERR_INVALID
+    assert "workspace" in str(e.value)

@@ -186,3 +186,20 @@ def test_fp8_conv_with_bias(pkg):
         ref = oracle.conv3d(bytes8(qx), bytes8(qw), (1, 1, 1), (0, 1, 1), (1, 1, 1), sx.item(),
                             sw.item(), bias=b.double().cpu().numpy())
         assert_close(as_f64(y), ref, f"fp8 bias split={split_k}")
+
+
+@pytest.mark.parametrize("shapes", [((2, 3, 1, 32, 48), (64, 3, 1, 16, 16), (1, 16, 16)),
+                                    ((3, 3, 1, 28, 35), (40, 3, 1, 7, 7), (1, 7, 7))])
+def test_fp8_patch_gemm(pkg, shapes):
+    """fp8 non-overlapping patches (the gathered-patch GEMM), packed from
+    NCDHW / KCTRS bf16; the 7x7x3 patch is 147 bytes (byte-wise gather)."""
+    xs, ws, st = shapes
+    x = cw.randn_bf16(xs, 440, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 540, 1.0 / np.sqrt(ws[1] * ws[3] * ws[4]), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    assert pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), st, 0, 1, 1)["class"] == "patch_gemm"
+    y = pkg.conv_fwd(qx, qw, st, 0, 1, scale_x=sx, scale_w=sw)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    ref = oracle.conv3d(bytes8(qx), bytes8(qw), st, (0, 0, 0), (1, 1, 1), sx.item(), sw.item())
+    assert_close(as_f64(y), ref, f"fp8 patch {shapes}")

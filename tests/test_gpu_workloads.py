@@ -126,3 +126,18 @@ def test_temporal_big_sampled(pkg):
     assert plan["class"] == "temporal"
     idx = _sample(tuple(y.shape), wl, plan["tile_n"])
     _check_sampled(y, bits16(x), bits16(w), idx, wl)
+
+
+@pytest.mark.parametrize("name", ["vit_patch16_bf16", "vit_patch14_bf16"])
+def test_vit_patch_embed_sampled(pkg, name):
+    """Patch embeddings with 196 / 256 patches per image, at full size: the
+    gathered-patch GEMM, sampled like the other large workloads."""
+    wl = cw.BY_NAME[name]
+    x, w = cw.make_inputs(wl, "cuda")
+    plan = pkg.conv_fwd_plan(wl.x_shape, wl.w_shape, wl.stride, wl.pad, wl.dil)
+    assert plan["class"] == "patch_gemm"
+    y = pkg.conv_fwd(x, w, wl.stride, wl.pad, wl.dil)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    idx = _sample(tuple(y.shape), wl, plan["tile_n"])
+    _check_sampled(y, bits16(x), bits16(w), idx, wl)
