@@ -242,7 +242,9 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias
         raise RuntimeError("device status reports a timeout")
     times = Timer(steps, flush).run(step)
     res = {"plan": plan, "ms": times, "flop": flops(wl),
-           "launches_per_step": 1 + (1 if plan["splits"] > 1 else 0)}
+           "launches_per_step": pkg.conv_fwd_kernel_launches(
+               tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
+               1 if wl.dtype == "fp8" else 0, ws.numel())}
     if wl.dtype == "fp8":
         # with the pack of the activation (the weight pack is a one-off prep)
         xb = ops["x_bf16_ncdhw"]

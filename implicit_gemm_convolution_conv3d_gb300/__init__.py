@@ -87,6 +87,9 @@ def load_library(path: str = LIB_PATH):
         for fn in (lib.conv_bwd_data_point, lib.conv_bwd_weight_point):
             fn.argtypes = [vp, vp, i64p, i64p, i32p, i32p, i32p, vp, vp, ctypes.c_size_t, vp]
             fn.restype = ctypes.c_int
+        lib.conv_fwd_kernel_launches.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int,
+                                                 ctypes.c_size_t, i32p]
+        lib.conv_fwd_kernel_launches.restype = ctypes.c_int
         lib.conv_fwd_noalloc.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
                                          vp, vp, vp]
         lib.conv_fwd_noalloc.restype = ctypes.c_int
@@ -175,6 +178,18 @@ def conv_fwd_plan(x_shape, w_shape, stride=1, pad=0, dil=1, dtype: int = CONV_DT
     cls, bn, bk, st, sp, ctas = (a.value for a in v)
     return {"class": CLASS_NAMES.get(cls, str(cls)), "tile_n": bn, "k_bytes": bk, "stages": st,
             "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
+
+
+def conv_fwd_kernel_launches(x_shape, w_shape, stride=1, pad=0, dil=1,
+                             dtype: int = CONV_DTYPE_BF16, workspace_bytes: int = 0) -> int:
+    """Kernels one conv_fwd call launches for this problem and workspace."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    _check(lib.conv_fwd_kernel_launches(_I64_5(*x_shape), _I64_5(*w_shape),
+                                        _I32_3(*_triple(stride)), _I32_3(*_triple(pad)),
+                                        _I32_3(*_triple(dil)), int(dtype), int(workspace_bytes),
+                                        ctypes.byref(n)), "conv_fwd_kernel_launches")
+    return int(n.value)
 
 
 def conv_set_wait_limit_ns(ns: int) -> None:

@@ -89,6 +89,14 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
                   int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
                   size_t* workspace_bytes);
 
+/* Number of kernels conv_fwd launches for this problem and workspace size on
+ * the current device (operand copies / patch gather, the convolution's
+ * launches -- long reductions run as several launches of whole waves --, and
+ * the split-K reduction).  Needs a GPU. */
+int conv_fwd_kernel_launches(const int64_t x_dims[5], const int64_t w_dims[5],
+                             const int stride[3], const int pad[3], const int dil[3], int dtype,
+                             size_t workspace_bytes, int* launches);
+
 /* Forward convolution:
  *   out[n,od,oh,ow,k] = bf16_rn( scale_x * scale_w *
  *       sum_{t,r,s,c} x[n, od*sd-pd+t*dd, oh*sh-ph+r*dh, ow*sw-pw+s*dw, c] * w[k,t,r,s,c] )

@@ -444,3 +444,42 @@ def test_patch_gemm_needs_workspace(pkg):
         pkg.conv_fwd(x, w, (1, 16, 16), 0, 1, split_k=False)
     assert e.value.status == pkg.CONV_ERR_INVALID
     assert "workspace" in str(e.value)
+
+
+@pytest.mark.parametrize("case", [GENERIC[4], TEMPORAL[5], GENERIC[10]],
+                         ids=["generic", "temporal", "generic256"])
+@pytest.mark.parametrize("slices", [2, 3, 7])
+def test_sliced_launches_are_bit_identical(pkg, case, slices):
+    """The convolution cut into several launches of whole waves (the rule for
+    long reductions, forced here on small shapes) computes every tile as one
+    launch does: identical bits, and the oracle's values."""
+    xs, ws, st, pa, di = case
+    x, w = _inputs(xs, ws, 230)
+    one = pkg.conv_fwd(x, w, st, pa, di, split_k=False)
+    with env_vars(CONV3D_SLICES=slices):
+        sl = pkg.conv_fwd(x, w, st, pa, di, split_k=False)
+        n = pkg.conv_fwd_kernel_launches(xs, ws, st, pa, di, 0, 0)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    assert 1 <= n <= slices
+    assert torch.equal(one.view(torch.int16), sl.view(torch.int16))
+    assert_close(as_f64(sl), oracle_conv(x, w, pkg._triple(st), pkg._triple(pa), pkg._triple(di)),
+                 f"sliced {case}")
+
+
+def test_kernel_launch_counts(pkg):
+    tiny = cw.BY_NAME["tiny_conv3d_bf16"]
+    p = pkg.conv_fwd_plan(tiny.x_shape, tiny.w_shape, tiny.stride, tiny.pad, tiny.dil)
+    assert p["splits"] > 1
+    assert pkg.conv_fwd_kernel_launches(tiny.x_shape, tiny.w_shape, tiny.stride, tiny.pad,
+                                        tiny.dil, 0, p["workspace_bytes"]) == 2
+    assert pkg.conv_fwd_kernel_launches(tiny.x_shape, tiny.w_shape, tiny.stride, tiny.pad,
+                                        tiny.dil, 0, 0) == 1
+    pe = cw.BY_NAME["patch_embed_bf16"]
+    p = pkg.conv_fwd_plan(pe.x_shape, pe.w_shape, pe.stride, pe.pad, pe.dil)
+    assert pkg.conv_fwd_kernel_launches(pe.x_shape, pe.w_shape, pe.stride, pe.pad, pe.dil, 0,
+                                        p["workspace_bytes"]) == 2   # weight copies + GEMM
+    video = cw.BY_NAME["video_conv3d_bf16"]
+    n = pkg.conv_fwd_kernel_launches(video.x_shape, video.w_shape, video.stride, video.pad,
+                                     video.dil, 0, 0)
+    assert n > 4   # the long reduction runs in slices of whole waves
