@@ -450,7 +450,8 @@ def main_arm(args):
                 r = run_workload(pkg, cw.BY_NAME[name.split("+")[0]], device, args.steps,
                                  args.warmup, flush, with_e2e=False, with_bias=name.endswith("+bias"))
                 m = statistics.mean(r["ms"])
-                ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m, "plan": r["plan"]}
+                ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m,
+                       "ms_median": statistics.median(r["ms"]), "plan": r["plan"]}
                 if "ms_with_pack" in r:
                     mp = statistics.mean(r["ms_with_pack"])
                     ent["tflops_with_pack"] = r["flop"] / (mp * 1e-3) / 1e12

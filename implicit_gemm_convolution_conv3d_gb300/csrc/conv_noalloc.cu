@@ -68,8 +68,9 @@ extern "C" int conv_fwd_noalloc(const void* x, const int64_t x_dims[5], const vo
     int rc = conv_fwd_plan(x_dims, w_dims, stride, pad, dil, dtype, 0, nullptr, nullptr, nullptr,
                            nullptr, nullptr, nullptr, nullptr);
     if (rc != CONV_OK) return rc;
-    // only the split-K partials must fit; workspace uses that do not fit
-    // (aligned operand copies) are skipped by conv_fwd itself
+    // the split-K partials must fit; optional operand copies that do not fit
+    // are skipped by conv_fwd itself, and a patch-class problem whose
+    // gathered rows do not fit is rejected there
     const size_t need = c3d::splitk_workspace_bytes(x_dims, w_dims, stride, pad, dil, dtype);
     if (need > c3d::kNoallocScratchBytes) {
         char msg[160];

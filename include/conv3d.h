@@ -242,6 +242,11 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
  *   - A problem whose split-K partials need more than
  *     CONV_NOALLOC_SCRATCH_BYTES is rejected with CONV_ERR_INVALID
  *     (conv_last_error says how many bytes it needed).
+ *   - Operand copies that conv_fwd makes in its workspace (aligned copies of
+ *     a point-output GEMM's operands, the gathered rows of the patch class)
+ *     go to the array too when they fit; the optional ones are skipped
+ *     otherwise, while a patch-class problem whose gathered rows do not fit
+ *     is rejected with CONV_ERR_INVALID.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
