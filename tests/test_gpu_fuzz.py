@@ -1,9 +1,10 @@
 """Seeded random parity sweep of the forward convolution.
 
 Each case draws a random problem of one dispatch class (im2col implicit GEMM,
-temporal T x 1 x 1, point-output GEMM, pointwise GEMM) in bf16 or fp8-e4m3,
-and a random plan (tile width, k-step bytes, pipeline depth, raster group,
-split-K, CTA pair, row sub-tiles) forced through the plan overrides.  A plan
+temporal T x 1 x 1, point-output GEMM, pointwise GEMM, non-overlapping
+patches) in bf16 or fp8-e4m3, and a random plan (tile width, k-step bytes,
+pipeline depth, raster group, split-K, CTA pair, row sub-tiles, launch
+slices) forced through the plan overrides.  A plan
 the library rejects for the shape falls back to the default plan, so every
 drawn problem runs.  Every output element is compared with the fp64 oracle
 on the exact bytes the GPU consumed."""
@@ -52,13 +53,25 @@ def _out_len(n, f, s, p, d):
 
 def _draw_problem(rng):
     fp8 = bool(rng.random() < 0.3)
-    kind = rng.choice(["generic", "temporal", "point", "pointwise"], p=[0.45, 0.25, 0.15, 0.15])
+    kind = rng.choice(["generic", "temporal", "point", "pointwise", "patch"],
+                      p=[0.40, 0.20, 0.13, 0.12, 0.15])
     K = int(rng.integers(1, 321))
     if kind == "point":
         T, R, S = (int(v) for v in rng.integers(1, 9, size=3))
         C = int(rng.integers(1, 9)) * (4 if fp8 else 2)
         N = int(rng.integers(1, 400))
         return fp8, kind, (N, T, R, S, C), (K, T, R, S, C), (T, R, S), (0, 0, 0), (1, 1, 1)
+    if kind == "patch":
+        # stride == filter, zero padding, many patches, leftovers past the
+        # last whole patch; channels an RGB-like count or a 16-byte multiple
+        T = int(rng.choice([1, 1, 2]))
+        R, S = (int(v) for v in rng.integers(2, 17, size=2))
+        C = int(rng.choice([1, 3, 4, 8, 16])) * (4 if fp8 and rng.random() < 0.5 else 1)
+        D = T * int(rng.integers(1, 3)) + int(rng.integers(0, T))
+        H = R * int(rng.integers(1, 5)) + int(rng.integers(0, R))
+        W = S * int(rng.integers(1, 5)) + int(rng.integers(0, S))
+        N = int(rng.integers(1, 5))
+        return fp8, kind, (N, D, H, W, C), (K, T, R, S, C), (T, R, S), (0, 0, 0), (1, 1, 1)
     C = int(rng.integers(1, 25)) * (16 if fp8 else 8)
     N = int(rng.integers(1, 4))
     if kind == "pointwise":
@@ -89,7 +102,8 @@ def _draw_plan(rng):
     group = int(rng.choice([1, 2, 4, 8]))
     splits = int(rng.choice([1, 1, 2, 3, 5]))
     return {"CONV3D_FORCE_TILE": f"{bn},{bk},{stages},{group},{splits}",
-            "CONV3D_PAIR": int(rng.integers(0, 2)), "CONV3D_MSUB": int(rng.integers(1, 3))}
+            "CONV3D_PAIR": int(rng.integers(0, 2)), "CONV3D_MSUB": int(rng.integers(1, 3)),
+            "CONV3D_SLICES": int(rng.choice([1, 1, 2, 3]))}
 
 
 def _case(i):
