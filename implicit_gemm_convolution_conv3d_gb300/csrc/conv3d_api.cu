@@ -770,6 +770,59 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.wait_ns = g_wait_ns;
 }
 
+// ------------------------------------------------------------ MN-major A GEMM
+// out[m, n] = sum_k A[k, m] * B[n, k] (bf16 in, fp32 accumulation, bf16 out
+// [M, Nn]) with A stored MN-major -- Kr rows of M contiguous elements (the
+// GEMM reads it in place: TMA boxes of 64 M x 64 k and tcgen05 MN-major
+// descriptors) -- and B K-major, Nn rows of Kp elements (Kp a multiple of 8,
+// zero past Kr).  The backward-weights GEMM (dy is [N, K]: MN-major as the
+// A of dW = dy^T x).  Plans as the pointwise GEMM of [M, Kp] by [Nn, Kp];
+// returns CONV_ERR_UNSUPPORTED when that plan does not use 128-byte k-steps
+// and one row sub-tile.
+int gemm_mn_a(const void* a, long long M, long long Kr, const void* b, long long Nn,
+              long long Kp, void* out, void* workspace, size_t workspace_bytes, DeviceInfo* dev,
+              cudaStream_t stream) {
+    const int64_t xi[5] = {M, 1, 1, 1, Kp}, wi[5] = {Nn, 1, 1, 1, Kp};
+    const int one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+    Geo g;
+    int rc = make_geo(xi, wi, one, zero, one, &g);
+    if (rc) return rc;
+    if (!load_entry_points()) {
+        set_error("cuTensorMapEncode* entry points unavailable");
+        return CONV_ERR_CUDA;
+    }
+    Plan P;
+    if ((rc = make_plan(g, CONV_DTYPE_BF16, dev->num_sms, dev->smem_optin, workspace_bytes, &P)))
+        return rc;
+    if (P.amode != AM_GEMM_TMA || P.BK != 128 || P.msub != 1 || P.phases != 1 || P.repack ||
+        (M * 2) % 16 != 0) {
+        set_error("MN-major GEMM plan unavailable for this shape");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    TMaps tm;
+    if ((rc = build_maps(g, P, a, b, &tm))) return rc;   // B (K-major) as planned
+    {
+        // A in place: dims {M (inner), Kr}, boxes of 64 x 64, 128-byte swizzle
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(Kr)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(M) * 2};
+        const cuuint32_t box[2] = {64, 64};
+        if ((rc = encode_tiled(&tm.a[0], 0, 2, a, dims, str, box, 128))) return rc;
+    }
+    if ((rc = build_out_map(g, P, out, &tm))) return rc;
+    KParams k;
+    fill_params(g, P, a, b, out, workspace, nullptr, nullptr, nullptr, dev->status, &k);
+    k.a_mn = 1;
+    k.idesc |= 1u << 15;   // A major-ness: MN
+    cudaError_t e = launch_igemm(P.amode, 0, &tm, k, P.grid, P.smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
+    if (P.splits > 1) {
+        e = launch_splitk_reduce(k.ws, out, M * Nn, P.splits, nullptr, nullptr, nullptr, Nn,
+                                 dev->num_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+    }
+    return CONV_OK;
+}
+
 // ------------------------------------------------------------ backward passes
 // Point-output geometry (MIOpen PR #10912): zero padding and the input
 // spatially equal to the filter, so each batch element has one output
@@ -1444,6 +1497,20 @@ int conv_bwd_weight_point(const void* x, const void* dy, const int64_t x_dims[5]
     // the reduction runs over the batch: dy^T [K, Np] and x^T [J, Np], rows
     // zero-padded to Np (a multiple of 8 elements, 16 bytes)
     const long long Np = (N + 7) / 8 * 8;
+    const char* amn = std::getenv("CONV3D_AMN");
+    if (K % 8 == 0 && !(amn && amn[0] == '0')) {
+        // dy's rows are 16-byte multiples: the GEMM reads dy in place as an
+        // MN-major A; only x is transposed
+        const size_t head = round256(J * Np * 2);
+        if (workspace && workspace_bytes >= head) {
+            unsigned char* wsb = static_cast<unsigned char*>(workspace);
+            cudaError_t e = launch_transpose_pad(x, N, J, wsb, Np, dev->num_sms, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+            rc = gemm_mn_a(dy, K, N, wsb, J, Np, dw, wsb + head, workspace_bytes - head, dev,
+                           stream);
+            if (rc != CONV_ERR_UNSUPPORTED) return rc;
+        }
+    }
     const size_t dyt = round256(K * Np * 2), head = dyt + round256(J * Np * 2);
     if (!workspace || workspace_bytes < head) {
         set_error("workspace smaller than the transposed operands (see conv_bwd_point_workspace_bytes)");

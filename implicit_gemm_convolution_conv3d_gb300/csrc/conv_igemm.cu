@@ -277,7 +277,11 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
                                            uint32_t tmem_base, uint32_t* misc,
                                            volatile uint32_t* abort_flag) {
     const int total_units = p.m_tiles * p.n_tiles * p.splits;
-    const uint64_t adesc0 = make_smem_desc(tiles, p.sbo, p.layout);
+    // MN-major A (SW128): 64-element MN blocks 8 KB apart (two per 128-row
+    // tile), 8-row K groups 1 KB apart; a 16-row K slice advances 2 KB
+    const uint64_t adesc0 = p.a_mn ? make_smem_desc(tiles, 1024u, p.layout, 8192u)
+                                   : make_smem_desc(tiles, p.sbo, p.layout);
+    const uint32_t a_slice = p.a_mn ? 128u : 2u;   // encoded advance per 16-element K slice
     const uint64_t bdesc0 = make_smem_desc(tiles + p.a_stage_bytes, p.sbo, p.layout);
     const uint32_t stage_step = p.stage_bytes >> 4;
     // msub row sub-tiles share each B stage; the TMEM holds 2/msub unit
@@ -311,7 +315,7 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
 #pragma unroll
                 for (int sub = 0; sub < MSUB; ++sub) {
                     const uint32_t d = d_tmem + static_cast<uint32_t>(sub * p.BN);
-                    const uint64_t a = ad + sub * sub_step + box * abox_step + 2 * kin;
+                    const uint64_t a = ad + sub * sub_step + box * abox_step + a_slice * kin;
                     if (PAIR) {
                         if (FP8)
                             tc_mma_f8_pair(d, a, b, p.idesc, accum);
@@ -430,10 +434,20 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
                     const int kj = k0 + j * box_e;
                     for (int sub = 0; sub < MSUB; ++sub) {
                         const uint32_t adst = adst0 + (sub * NB + j) * abox;
-                        if (PAIR)
+                        if (p.a_mn) {
+                            // MN-major A: two boxes of 64 MN x 64 K rows
+                            if (PAIR) {
+                                tma_load_2d_pair(adst, tmA, fb, am0[sub], kj);
+                                tma_load_2d_pair(adst + 8192u, tmA, fb, am0[sub] + 64, kj);
+                            } else {
+                                tma_load_2d(adst, tmA, fb, am0[sub], kj);
+                                tma_load_2d(adst + 8192u, tmA, fb, am0[sub] + 64, kj);
+                            }
+                        } else if (PAIR) {
                             tma_load_2d_pair(adst, tmA, fb, kj, am0[sub]);
-                        else
+                        } else {
                             tma_load_2d(adst, tmA, fb, kj, am0[sub]);
+                        }
                     }
                     if (PAIR)
                         tma_load_2d_pair(bdst + j * bbox, tmB, fb, kj, n0);

@@ -356,10 +356,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // distance between 8-row groups), fixed version bits 46-48 = 0b001, and the
 // swizzle layout in bits 61-63 (2 = 128B, 4 = 64B, 6 = 32B).
 __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t sbo_bytes,
-                                                   uint32_t layout) {
+                                                   uint32_t layout, uint32_t lbo_bytes = 16) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(layout & 7u) << 61;

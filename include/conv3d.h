@@ -179,8 +179,9 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
  *   conv_bwd_weight_point: dw[k, j] = sum_n dy[n, k] * x[n, j]
  *       x device NDHWC; dy device [N,1,1,1,K]; dw device KTRSC (w's shape)
  * x_dims / w_dims / stride / pad / dil describe the forward conv.  Both
- * transpose their operands K-major into `workspace` (dx: w^T [J, K]; dw:
- * dy^T [K, N'] and x^T [J, N'], N' = N rounded up to 8, zero-padded) and run
+ * transpose operands K-major into `workspace` (dx: w^T [J, K]; dw: x^T
+ * [J, N'], N' = N rounded up to 8, zero-padded, and -- unless K % 8 == 0,
+ * when dy is read in place as an MN-major operand -- dy^T [K, N']) and run
  * the pointwise forward GEMM on them (split-K over the batch for dw when the
  * rest of the workspace holds the partials).  A workspace smaller than the
  * transposes returns CONV_ERR_INVALID; conv_bwd_point_workspace_bytes

@@ -109,3 +109,32 @@ def test_backward_odd_extents(pkg):
     torch.cuda.synchronize()
     assert pkg.conv_get_device_status() == 0
     assert_close(as_f64(dw), oracle.conv3d_bwd_weight(bits16(x), bits16(dy), ws, st), "wgrad odd")
+
+
+@pytest.mark.parametrize("amn", ["0", "1"])
+def test_backward_weight_both_operand_paths(pkg, amn):
+    """dW with dy read in place as an MN-major operand (K % 8 == 0, the default)
+    and through the transposed copy (CONV3D_AMN=0): both against the oracle,
+    with split-K and without (a workspace holding only the copies)."""
+    import os
+    xs, K = (700, 1, 14, 14, 3), 256
+    x, w, dy, ws, st = _operands(xs, K, 14)
+    old = os.environ.get("CONV3D_AMN")
+    os.environ["CONV3D_AMN"] = amn
+    try:
+        for small in (False, True):
+            wsp = None
+            if small:
+                Np = (xs[0] + 7) // 8 * 8
+                wsp = torch.empty(((K * Np * 2 + 255) // 256 + (588 * Np * 2 + 255) // 256) * 256,
+                                  dtype=torch.uint8, device="cuda")
+            dw = pkg.conv_bwd_weight_point(x, dy, ws, st, workspace=wsp)
+            torch.cuda.synchronize()
+            assert pkg.conv_get_device_status() == 0
+            assert_close(as_f64(dw), oracle.conv3d_bwd_weight(bits16(x), bits16(dy), ws, st),
+                         f"wgrad amn={amn} small_ws={small}")
+    finally:
+        if old is None:
+            os.environ.pop("CONV3D_AMN", None)
+        else:
+            os.environ["CONV3D_AMN"] = old
