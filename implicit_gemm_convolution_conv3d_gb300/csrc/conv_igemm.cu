@@ -6,20 +6,24 @@
 // point-output conv is the same kernel with a plain row-major A (MIOpen PR
 // #10912, description).
 //
-// One persistent CTA per SM walks a strided list of work units (m-tile,
-// n-tile, split).  Warp roles:
-//   warp 0      TMA producer: one A box and one B box per k-step into a
+// One persistent CTA per SM (or CTA pair per two SMs) walks a strided list of
+// work units (m-tile, n-tile, split) of one launch's m-tile range.  Warp roles:
+//   warp 0      TMA producer: the A and B boxes of each k-step (one or two
+//               128-byte boxes per operand, per row sub-tile) into a
 //               multi-stage shared-memory ring (full/empty mbarriers).  The A
 //               box is an im2col-mode box (generic conv), a 4-D tiled box of
-//               H*W rows (T x 1 x 1 temporal conv) or a 2-D tiled box (GEMM);
-//               padding taps read as zeros through TMA bounds.
+//               H*W rows (T x 1 x 1 temporal conv) or a 2-D tiled box (GEMM:
+//               K-major, MN-major, or one of two row phases); padding taps
+//               and reduction tails read as zeros through TMA bounds.
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (kind::f16 for
-//               bf16, kind::f8f6f4 for e4m3) into a double-buffered fp32
-//               accumulator and commits stages back to the producer.
-//   warps 2..5  epilogue: tcgen05.ld -> scale -> bf16 -> 16-byte stores (or
-//               fp32 split-K partials), overlapping the next tile's mainloop.
+//               bf16, kind::f8f6f4 for e4m3; cta_group::2 for pairs) into
+//               fp32 accumulators and commits stages back to the producer.
+//   warps 2..5  epilogue: tcgen05.ld -> scale (+ bias) -> bf16 -> staged in
+//               shared memory -> TMA tensor stores, or 8- / 4-byte stores for
+//               rows that are not 16-byte multiples, or direct fp32 split-K
+//               partials; overlaps the next unit's mainloop.
 //   warps 6..9  (row-gather GEMM only) cp.async producers for operands whose
-//               rows are not 16-byte aligned.
+//               rows are not 16-byte aligned and no workspace is given.
 // Every wait is bounded: on expiry the kernel records CONV_ERR_TIMEOUT,
 // drains its copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_bf16.h>
