@@ -45,6 +45,14 @@ struct Unit {
     int m_tile, n_tile, split;
 };
 
+// Columns unit t's MMAs compute: BN, or for a last column tile that K does
+// not fill, the rest of K rounded up to 32 (whole 32-column epilogue chunks;
+// a tcgen05 N for either CTA count).
+__device__ __forceinline__ int tile_cols(int n_tile, const KParams& p) {
+    const int rest = p.K - n_tile * p.BN;
+    return rest >= p.BN ? p.BN : ((rest + 31) & ~31);
+}
+
 // Temporal m-tile -> ((n, d) plane, H*W tile).  Plane-major by default (output
 // row order); H*W-tile-major when p.hw_major, so that the units running at
 // once cover one H*W tile of consecutive planes and share their input planes
@@ -304,6 +312,9 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
         const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
         if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns)) return;
         tc_fence_after();
+        // the instruction descriptor's N (bits 17-22, N / 8) for this tile
+        const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) |
+                               (static_cast<uint32_t>(tile_cols(t.n_tile, p) >> 3) << 17);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MSUB * p.BN);
         uint32_t accum = 0u;
         for (int ks = ks0; ks < ks1; ++ks) {
@@ -322,14 +333,14 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
                     const uint64_t a = ad + sub * sub_step + box * abox_step + a_slice * kin;
                     if (PAIR) {
                         if (FP8)
-                            tc_mma_f8_pair(d, a, b, p.idesc, accum);
+                            tc_mma_f8_pair(d, a, b, idesc, accum);
                         else
-                            tc_mma_f16_pair(d, a, b, p.idesc, accum);
+                            tc_mma_f16_pair(d, a, b, idesc, accum);
                     } else {
                         if (FP8)
-                            tc_mma_f8(d, a, b, p.idesc, accum);
+                            tc_mma_f8(d, a, b, idesc, accum);
                         else
-                            tc_mma_f16(d, a, b, p.idesc, accum);
+                            tc_mma_f16(d, a, b, idesc, accum);
                     }
                 }
                 accum = 1u;
@@ -383,7 +394,9 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
         const CUtensorMap* tmA = &tm.a[rphase];
         const CUtensorMap* tmB = &tm.b[rphase];
         // this CTA's B rows: all BN columns, or its half of them in a pair
-        const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (p.BN >> PAIR);
+        // (a pair splits the tile's MMA columns evenly: the peer's half starts
+        // at half of this tile's computed width)
+        const int n0 = t.n_tile * p.BN + static_cast<int>(rank) * (tile_cols(t.n_tile, p) >> PAIR);
         // A coordinates of each row sub-tile (128 rows of this CTA)
         int aw[2] = {0, 0}, ah[2] = {0, 0}, ad[2] = {0, 0}, an[2] = {0, 0}, am0[2] = {0, 0};
         for (int sub = 0; sub < MSUB; ++sub) {
