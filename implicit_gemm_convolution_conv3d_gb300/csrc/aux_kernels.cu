@@ -239,10 +239,13 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const __nv_bfloat16* __
     const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
     for (long long tile = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
          tile < tiles; tile += warps) {
-        const long long st = tile % s_tiles;
-        const long long rest = tile / s_tiles;
-        const long long ct = rest % c_tiles;
-        const long long n = rest / c_tiles;
+        // channel tiles fastest: the warps that write the other channels of
+        // the same output positions run at the same time, so each output
+        // line is completed in L2 before it is written back
+        const long long ct = tile % c_tiles;
+        const long long rest = tile / c_tiles;
+        const long long st = rest % s_tiles;
+        const long long n = rest / s_tiles;
         const long long c0 = ct * 64 + cg * 16;
         const long long s0 = st * 64 + sb * 8;
         if (c0 >= C || s0 >= S) continue;
