@@ -84,15 +84,16 @@ def kernel_source_sha() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch of the conv kernel from the committed ncu summary,
-    or None when the kernel sources changed since it was taken."""
+    """DRAM bytes of one step's conv kernel launches (a long reduction runs
+    as several launches of whole waves) from the committed ncu summary, or
+    None when the kernel sources changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)
     if not d or d.get("kernel_sha") != kernel_source_sha():
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get("dram_bytes_per_step")
 
 
 class ClockSampler:
@@ -484,6 +485,7 @@ def main_arm(args):
     traffic = measured_traffic(wl.name)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
+            "per": f"one conv_fwd step ({res['launches_per_step']} kernel launches)",
             "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
             "kernel": "conv_igemm_kernel (tcgen05, TMA im2col)"}
     cpu = None
