@@ -91,6 +91,8 @@ def _load():
         lib.oracle_conv3d_fwd_points.restype = ctypes.c_int
         lib.oracle_conv3d_fwd_points.argtypes = conv_args + [_I64P, ctypes.c_int64,
                                                              ctypes.c_void_p]
+        lib.oracle_conv3d_fwd_points_ncdhw.restype = ctypes.c_int
+        lib.oracle_conv3d_fwd_points_ncdhw.argtypes = lib.oracle_conv3d_fwd_points.argtypes
         bwd_args = [ctypes.c_void_p, _I64P, ctypes.c_void_p, _I64P, _I32P, _I32P, _I32P,
                     ctypes.c_int, ctypes.c_void_p]
         lib.oracle_conv3d_bwd_data.restype = ctypes.c_int
@@ -221,9 +223,12 @@ def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1
 
 def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1),
                   pad=(0, 0, 0), dil=(1, 1, 1), scale_x: float = 1.0,
-                  scale_w: float = 1.0, bias=None) -> np.ndarray:
+                  scale_w: float = 1.0, bias=None, x_layout: str = "ndhwc") -> np.ndarray:
     """fp64 conv evaluated at flat NDHWC output indices ``idx`` (int64), plus
-    bias[k] of each index's filter k when given."""
+    bias[k] of each index's filter k when given.  ``x_layout="ncdhw"``: x is
+    stored channel-major [N,C,D,H,W] (the output indices stay NDHWC)."""
+    if x_layout not in ("ndhwc", "ncdhw"):
+        raise ValueError("x_layout must be 'ndhwc' or 'ncdhw'")
     x = np.ascontiguousarray(x)
     w = np.ascontiguousarray(w)
     elem = _elem_of(x)
@@ -231,12 +236,14 @@ def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1
         raise TypeError("x and w must have the same element type")
     idx = np.ascontiguousarray(idx, dtype=np.int64)
     vals = np.empty(idx.shape, dtype=np.float64)
-    rc = _load().oracle_conv3d_fwd_points(
+    fn = (_load().oracle_conv3d_fwd_points if x_layout == "ndhwc"
+          else _load().oracle_conv3d_fwd_points_ncdhw)
+    rc = fn(
         x.ctypes.data, _dims(x.shape, 5), w.ctypes.data, _dims(w.shape, 5), _ints3(stride),
         _ints3(pad), _ints3(dil), elem, float(scale_x), float(scale_w),
         idx.ctypes.data_as(_I64P), idx.size, vals.ctypes.data)
     if rc != 0:
-        raise ValueError("oracle_conv3d_fwd_points: bad shapes or index out of range")
+        raise ValueError("oracle conv3d points: bad shapes or index out of range")
     if bias is not None:
         vals += np.asarray(bias, dtype=np.float64).reshape(-1)[idx % w.shape[0]]
     return vals

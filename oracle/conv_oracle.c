@@ -212,7 +212,8 @@ int64_t oracle_out_extent(int64_t in, int64_t filt, int stride, int pad, int dil
 }
 
 typedef struct {
-    int64_t N, D, H, W, C;       /* x: NDHWC */
+    int64_t N, D, H, W, C;       /* x extents */
+    int64_t xn, xd, xh, xw, xc;  /* x element strides: NDHWC, or NCDHW */
     int64_t K, T, R, S;          /* w: KTRSC (C shared) */
     int64_t Do, Ho, Wo;          /* out: N Do Ho Wo K */
     int sd, sh, sw, pd, ph, pw, dd, dh, dw;
@@ -222,6 +223,8 @@ static int make_geom(conv_geom *g, const int64_t xd[5], const int64_t wd[5], con
                      const int pad[3], const int dil[3])
 {
     g->N = xd[0]; g->D = xd[1]; g->H = xd[2]; g->W = xd[3]; g->C = xd[4];
+    g->xc = 1; g->xw = g->C; g->xh = g->W * g->C; g->xd = g->H * g->W * g->C;
+    g->xn = g->D * g->H * g->W * g->C;
     g->K = wd[0]; g->T = wd[1]; g->R = wd[2]; g->S = wd[3];
     if (wd[4] != xd[4])
         return -1;
@@ -256,10 +259,10 @@ static double conv_point(const conv_geom *g, const void *x, const void *w, int e
                 int64_t xrow, wrow;
                 if (iw < 0 || iw >= g->W)
                     continue;
-                xrow = (((n * g->D + id) * g->H + ih) * g->W + iw) * g->C;
+                xrow = n * g->xn + id * g->xd + ih * g->xh + iw * g->xw;
                 wrow = (((k * g->T + t) * g->R + r) * g->S + s) * g->C;
                 for (c = 0; c < g->C; ++c)
-                    acc += load_elem(x, xrow + c, elem) * load_elem(w, wrow + c, elem);
+                    acc += load_elem(x, xrow + c * g->xc, elem) * load_elem(w, wrow + c, elem);
             }
         }
     }
@@ -290,15 +293,41 @@ int oracle_conv3d_fwd(const void *x, const int64_t xd[5], const void *w, const i
 }
 
 /* The same definition evaluated only at the given flat NDHWC output indices. */
+static int fwd_points(const conv_geom *gp, const void *x, const void *w, int elem, double scale_x,
+                      double scale_w, const int64_t *idx, int64_t n_idx, double *vals);
+
 int oracle_conv3d_fwd_points(const void *x, const int64_t xd[5], const void *w,
                              const int64_t wd[5], const int stride[3], const int pad[3],
                              const int dil[3], int elem, double scale_x, double scale_w,
                              const int64_t *idx, int64_t n_idx, double *vals)
 {
     conv_geom g;
-    int64_t i, total;
     if (make_geom(&g, xd, wd, stride, pad, dil) != 0)
         return -1;
+    return fwd_points(&g, x, w, elem, scale_x, scale_w, idx, n_idx, vals);
+}
+
+/* The same, with x stored channel-major: x[n,c,d,h,w] at
+ * (((n*C + c)*D + d)*H + h)*W + w, xd = {N, C, D, H, W} (torch's own layout);
+ * the output indices are still flat NDHWC [N,Do,Ho,Wo,K]. */
+int oracle_conv3d_fwd_points_ncdhw(const void *x, const int64_t xd[5], const void *w,
+                                   const int64_t wd[5], const int stride[3], const int pad[3],
+                                   const int dil[3], int elem, double scale_x, double scale_w,
+                                   const int64_t *idx, int64_t n_idx, double *vals)
+{
+    conv_geom g;
+    const int64_t nd[5] = {xd[0], xd[2], xd[3], xd[4], xd[1]};
+    if (make_geom(&g, nd, wd, stride, pad, dil) != 0)
+        return -1;
+    g.xw = 1; g.xh = g.W; g.xd = g.H * g.W; g.xc = g.D * g.H * g.W; g.xn = g.C * g.xc;
+    return fwd_points(&g, x, w, elem, scale_x, scale_w, idx, n_idx, vals);
+}
+
+static int fwd_points(const conv_geom *gp, const void *x, const void *w, int elem, double scale_x,
+                      double scale_w, const int64_t *idx, int64_t n_idx, double *vals)
+{
+    const conv_geom g = *gp;
+    int64_t i, total;
     total = g.N * g.Do * g.Ho * g.Wo * g.K;
     for (i = 0; i < n_idx; ++i)
         if (idx[i] < 0 || idx[i] >= total)

@@ -221,6 +221,28 @@ def test_points_equal_full_evaluation():
     assert np.array_equal(pts, full.ravel()[idx])
 
 
+def test_points_on_channel_major_x_match_torch():
+    """The channel-major (NCDHW) evaluation against torch CPU fp64 F.conv3d
+    on the same array, in torch's own layout (no permutation of x), over
+    random geometries; a swapped stride of the NCDHW indexing (c vs w, d vs
+    h) fails it.  Outputs are compared at every flat NDHWC index."""
+    rng = np.random.default_rng(606)
+    for _ in range(60):
+        (N, D, H, W, C), ws, stride, pad, dil = _random_case(rng)
+        x = rng.standard_normal((N, C, D, H, W))
+        w = rng.standard_normal(ws)
+        wt = torch.from_numpy(np.ascontiguousarray(w)).permute(0, 4, 1, 2, 3)
+        ref = F.conv3d(torch.from_numpy(x), wt, stride=tuple(stride), padding=tuple(pad),
+                       dilation=tuple(dil)).permute(0, 2, 3, 4, 1).contiguous().numpy()
+        idx = np.arange(ref.size, dtype=np.int64)
+        got = oracle.conv3d_points(x, w, idx, stride, pad, dil, x_layout="ncdhw")
+        np.testing.assert_allclose(got, ref.ravel(), rtol=1e-12, atol=1e-12)
+        # and the same numbers as the channel-last evaluation of the permuted x
+        nd = oracle.conv3d_points(np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1)), w, idx,
+                                  stride, pad, dil)
+        assert np.array_equal(got, nd)
+
+
 def test_points_reject_out_of_range_index():
     x = np.zeros((1, 2, 2, 2, 1))
     w = np.zeros((1, 1, 1, 1, 1))
