@@ -207,8 +207,13 @@ def barrier(dist):
 
 # ---------------------------------------------------------------- workloads
 
+def reads_ncdhw(wl: cw.Workload) -> bool:
+    """bf16 workloads whose channel-major activation conv_fwd_ncdhw reads in place."""
+    return wl.x_layout == "ncdhw" and wl.dtype == "bf16"
+
+
 def prepare(pkg, wl: cw.Workload, device):
-    """Device-resident operands of workload wl in the layout conv_fwd takes."""
+    """Device-resident operands of workload wl in the layout its conv call takes."""
     x, w = cw.make_inputs(wl, device)
     if wl.dtype == "fp8":
         qx, sx = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)
@@ -218,17 +223,32 @@ def prepare(pkg, wl: cw.Workload, device):
 
 
 def conv_step(pkg, wl, ops, out, ws, bias=None):
+    if reads_ncdhw(wl):
+        return lambda: pkg.conv_fwd_ncdhw(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil,
+                                          bias=bias, out=out, workspace=ws)
     return lambda: pkg.conv_fwd(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil, scale_x=ops["sx"],
                                 scale_w=ops["sw"], out=out, workspace=ws, bias=bias)
+
+
+def ndhwc_shape(wl: cw.Workload):
+    """The activation's shape in NDHWC order."""
+    if wl.x_layout == "ncdhw":
+        N, C, D, H, W = wl.x_shape
+        return (N, D, H, W, C)
+    return tuple(wl.x_shape)
 
 
 def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias=False):
     """with_bias: the same step through conv_fwd_bias (a per-filter fp32 bias)."""
     ops = prepare(pkg, wl, device)
     x, w = ops["x"], ops["w"]
-    plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
-                             1 if wl.dtype == "fp8" else 0)
-    od = pkg.conv_out_dims(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil)
+    ncdhw = reads_ncdhw(wl)
+    if ncdhw:
+        plan = pkg.conv_fwd_ncdhw_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil)
+    else:
+        plan = pkg.conv_fwd_plan(tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
+                                 1 if wl.dtype == "fp8" else 0)
+    od = pkg.conv_out_dims(ndhwc_shape(wl), tuple(w.shape), wl.stride, wl.pad, wl.dil)
     out = torch.empty(od, dtype=torch.bfloat16, device=device)
     ws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=device)
     bias = None
@@ -242,10 +262,28 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias
     if pkg.conv_get_device_status() != 0:
         raise RuntimeError("device status reports a timeout")
     times = Timer(steps, flush).run(step)
-    res = {"plan": plan, "ms": times, "flop": flops(wl),
-           "launches_per_step": pkg.conv_fwd_kernel_launches(
-               tuple(x.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil,
-               1 if wl.dtype == "fp8" else 0, ws.numel())}
+    if ncdhw:
+        # the channel-major plans here run unsliced (reductions under 384 k-steps)
+        launches = 1 + (plan["splits"] > 1)
+    else:
+        launches = pkg.conv_fwd_kernel_launches(tuple(x.shape), tuple(w.shape), wl.stride,
+                                                wl.pad, wl.dil, 1 if wl.dtype == "fp8" else 0,
+                                                ws.numel())
+    res = {"plan": plan, "ms": times, "flop": flops(wl), "launches_per_step": launches}
+    if ncdhw:
+        # the alternative: the NCDHW -> NDHWC pass, then conv_fwd
+        xn = torch.empty(ndhwc_shape(wl), dtype=torch.bfloat16, device=device)
+        cplan = pkg.conv_fwd_plan(tuple(xn.shape), tuple(w.shape), wl.stride, wl.pad, wl.dil)
+        cws = torch.empty(max(cplan["workspace_bytes"], 16), dtype=torch.uint8, device=device)
+
+        def pack_then_conv():
+            pkg.pack_ncdhw_bf16_to_ndhwc(x, out=xn)
+            pkg.conv_fwd(xn, w, wl.stride, wl.pad, wl.dil, out=out, workspace=cws)
+        for _ in range(warmup):
+            pack_then_conv()
+        res["ms_pack_then_conv"] = Timer(steps, flush).run(pack_then_conv)
+        res["io_bytes"] = (x.numel() + w.numel() + out.numel()) * 2
+        del xn
     if wl.dtype == "fp8":
         # with the pack of the activation (the weight pack is a one-off prep)
         xb = ops["x_bf16_ncdhw"]
@@ -276,7 +314,8 @@ def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
     needs all of it on the device before the pack, so the copies, the pack
     and the conv run in sequence."""
     # the host holds the activation as the user has it (bf16 NCDHW for the fp8
-    # workload, which is packed on the device every step) and the prepared weight
+    # workload, which is packed on the device every step; channel-major x for
+    # conv_fwd_ncdhw) and the prepared weight
     dx = ops["x_bf16_ncdhw"] if wl.dtype == "fp8" else ops["x"]
     hx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
     hx.copy_(dx)
@@ -286,6 +325,12 @@ def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
 
     def step():
+        if reads_ncdhw(wl):
+            dx.copy_(hx, non_blocking=True)
+            ops["w"].copy_(hw, non_blocking=True)
+            pkg.conv_fwd_ncdhw(dx, ops["w"], wl.stride, wl.pad, wl.dil, out=out, workspace=ws)
+            hout.copy_(out, non_blocking=True)
+            return
         if wl.dtype != "fp8":
             pkg.conv_fwd_from_host(hx, hw, wl.stride, wl.pad, wl.dil, out_host=hout,
                                    x_dev=ops["x"], w_dev=ops["w"], out_dev=out, workspace=ws)
@@ -322,12 +367,13 @@ def cpu_oracle_rate(wl: cw.Workload, x_host, w_host, target_s: float = 10.0):
     rng = np.random.default_rng(wl.sample_seed)
     probe = rng.integers(0, total, size=256)
     t0 = time.perf_counter()
-    oracle.conv3d_points(x_host, w_host, probe, wl.stride, wl.pad, wl.dil)
+    lay = "ncdhw" if wl.x_layout == "ncdhw" else "ndhwc"
+    oracle.conv3d_points(x_host, w_host, probe, wl.stride, wl.pad, wl.dil, x_layout=lay)
     per = (time.perf_counter() - t0) / probe.size
     n = int(min(max(256, target_s / max(per, 1e-9)), 5_000_000))
     idx = rng.integers(0, total, size=n)
     t0 = time.perf_counter()
-    oracle.conv3d_points(x_host, w_host, idx, wl.stride, wl.pad, wl.dil)
+    oracle.conv3d_points(x_host, w_host, idx, wl.stride, wl.pad, wl.dil, x_layout=lay)
     dt = time.perf_counter() - t0
     return {"value": 2.0 * n * R / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
             "kind": "oracle",
@@ -337,8 +383,11 @@ def cpu_oracle_rate(wl: cw.Workload, x_host, w_host, target_s: float = 10.0):
 
 def host_inputs(wl: cw.Workload):
     """The workload's operands as the host bytes the oracle reads (generated
-    on the CPU with the same seeds and recipe)."""
+    on the CPU with the same seeds and recipe): x as stored (NDHWC, or NCDHW),
+    w as KTRSC (values of the bf16 weight before any fp8 pack)."""
     x, w = cw.make_inputs(wl, "cpu")
+    if wl.w_layout == "kctrs":
+        w = w.permute(0, 2, 3, 4, 1).contiguous()
     xb = x.view(torch.int16).numpy().view(np.uint16)
     wb = w.view(torch.int16).numpy().view(np.uint16)
     return xb, wb
@@ -415,6 +464,11 @@ def run_backward(pkg, wl, device, steps, warmup, flush):
 # MI355X figures for the patch embedding's backward passes (MIOpen PR #10912,
 # test plan and review thread): context, not a target on this hardware
 PAGE_BACKWARD_MS = {"dgrad": 0.028, "wgrad": 0.040}
+# FlyDSL PR #860, 1x1x1 commit (MI355X): the pointwise conv of a channel-major
+# activation through the NCDHW -> NDHWC transpose and the im2col kernel, and
+# through torch.matmul on the channel-major tensor
+PAGE_NCDHW_MS = {"pointwise_1x1x1_bf16_ncdhw": {"transpose_then_conv": 8.7,
+                                                "matmul_on_ncdhw": 3.4}}
 
 
 # ---------------------------------------------------------------- main arm
@@ -442,7 +496,8 @@ def main_arm(args):
     secondary = {}
     if not args.no_secondary:
         names = [n for n in ("fp8_conv3d_1x3x3", "temporal_3x1x1_bf16_big", "patch_embed_bf16",
-                             "tiny_conv3d_bf16", "vit_patch16_bf16", "vit_patch14_bf16")
+                             "tiny_conv3d_bf16", "vit_patch16_bf16", "vit_patch14_bf16",
+                             "temporal_3x1x1_bf16_ncdhw", "pointwise_1x1x1_bf16_ncdhw")
                  if n != wl.name]
         # the bias epilogue on the headline and on the epilogue-heavy patch embedding
         names += [wl.name + "+bias", "patch_embed_bf16+bias"]
@@ -460,6 +515,11 @@ def main_arm(args):
                     pk = statistics.mean(r["ms_pack"])
                     ent["pack_ms"] = pk
                     ent["pack_gbs"] = r["pack_bytes"] / (pk * 1e-3) / 1e9
+                if "ms_pack_then_conv" in r:
+                    ent["ms_pack_then_conv"] = statistics.mean(r["ms_pack_then_conv"])
+                    ent["io_gbs"] = r["io_bytes"] / (m * 1e-3) / 1e9
+                    if name in PAGE_NCDHW_MS:
+                        ent["page_mi355x_ms"] = PAGE_NCDHW_MS[name]
                 secondary[name] = ent
             except Exception as e:  # a secondary workload never hides the headline line
                 secondary[name] = {"error": f"{type(e).__name__}: {e}"}

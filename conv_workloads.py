@@ -97,7 +97,21 @@ PATCH_WORKLOADS = [
              (0, 0, 0)),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS + PATCH_WORKLOADS}
+# Channel-major (NCDHW) activations read in place by conv_fwd_ncdhw: the
+# temporal workload with its activation in torch's layout, and the pointwise
+# conv FlyDSL PR #860's 1x1x1 commit measures (a 14 GB bf16 activation of 512
+# channels over [240, 320, 180], 48 filters; 6.8e11 flop at 8.7 ms = 78 TF).
+NCDHW_WORKLOADS = [
+    Workload("temporal_3x1x1_bf16_ncdhw", 10, (1, 640, 240, 160, 90), (640, 3, 1, 1, 640),
+             (1, 1, 1), (1, 0, 0), x_layout="ncdhw"),
+    Workload("pointwise_1x1x1_bf16_ncdhw", 11, (1, 512, 240, 320, 180), (48, 1, 1, 1, 512),
+             (1, 1, 1), (0, 0, 0), x_layout="ncdhw"),
+    # profiler-capture size of the first (16 frames, 295 MB)
+    Workload("temporal_3x1x1_bf16_ncdhw_small", 12, (1, 640, 16, 160, 90), (640, 3, 1, 1, 640),
+             (1, 1, 1), (1, 0, 0), x_layout="ncdhw"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS + PATCH_WORKLOADS + NCDHW_WORKLOADS}
 
 
 def randn_bf16(shape, seed: int, std: float = 1.0, device="cpu",

@@ -81,6 +81,10 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd_bias.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp,
                                       vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_fwd_bias.restype = ctypes.c_int
+        lib.conv_fwd_ncdhw_plan.argtypes = lib.conv_fwd_plan.argtypes
+        lib.conv_fwd_ncdhw_plan.restype = ctypes.c_int
+        lib.conv_fwd_ncdhw.argtypes = lib.conv_fwd_bias.argtypes
+        lib.conv_fwd_ncdhw.restype = ctypes.c_int
         lib.conv_bwd_point_workspace_bytes.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int,
                                                        ctypes.POINTER(ctypes.c_size_t)]
         lib.conv_bwd_point_workspace_bytes.restype = ctypes.c_int
@@ -180,6 +184,21 @@ def conv_fwd_plan(x_shape, w_shape, stride=1, pad=0, dil=1, dtype: int = CONV_DT
             "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
 
 
+def conv_fwd_ncdhw_plan(x_shape, w_shape, stride=1, pad=0, dil=1,
+                        dtype: int = CONV_DTYPE_BF16, num_sms: int = 0) -> dict:
+    """conv_fwd_plan for conv_fwd_ncdhw: x_shape is (N, C, D, H, W)."""
+    lib = load_library()
+    v = [ctypes.c_int(0) for _ in range(6)]
+    ws = ctypes.c_size_t(0)
+    _check(lib.conv_fwd_ncdhw_plan(_I64_5(*x_shape), _I64_5(*w_shape), _I32_3(*_triple(stride)),
+                                   _I32_3(*_triple(pad)), _I32_3(*_triple(dil)), int(dtype),
+                                   int(num_sms), *[ctypes.byref(a) for a in v], ctypes.byref(ws)),
+           "conv_fwd_ncdhw_plan")
+    cls, bn, bk, st, sp, ctas = (a.value for a in v)
+    return {"class": CLASS_NAMES.get(cls, str(cls)), "tile_n": bn, "k_bytes": bk, "stages": st,
+            "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
+
+
 def conv_fwd_kernel_launches(x_shape, w_shape, stride=1, pad=0, dil=1,
                              dtype: int = CONV_DTYPE_BF16, workspace_bytes: int = 0) -> int:
     """Kernels one conv_fwd call launches for this problem and workspace."""
@@ -253,6 +272,50 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
                                _ptr(scale_w), bias.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes,
                                _stream_handle(stream))
         _check(rc, "conv_fwd_bias")
+    return out
+
+
+def conv_fwd_ncdhw(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
+                   scale_x: Optional[torch.Tensor] = None, scale_w: Optional[torch.Tensor] = None,
+                   bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None,
+                   split_k: bool = True) -> torch.Tensor:
+    """Forward conv of a channel-major activation read in place: x NCDHW
+    [N,C,D,H,W] bf16, w KTRSC [K,T,1,1,C] bf16 -> out NDHWC [N,Do,H,W,K] bf16
+    (T x 1 x 1 filters, unit H/W stride, no H/W padding; H*W and C multiples
+    of 8).  Other arguments as for conv_fwd."""
+    lib = load_library()
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError("x must be [N,C,D,H,W] and w [K,T,R,S,C]")
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("conv_fwd_ncdhw takes bf16 x and w")
+    for s in (scale_x, scale_w):
+        if s is not None and (s.dtype != torch.float32 or s.numel() < 1):
+            raise TypeError("scales must be float32 device tensors")
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (w.shape[0],)):
+        raise TypeError("bias must be a float32 device tensor of shape [K]")
+    _require_cuda(x, w, scale_x, scale_w, out, workspace, bias)
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    n, c, d, h, wd = (int(v) for v in x.shape)
+    od = conv_out_dims((n, d, h, wd, c), tuple(w.shape), st, pa, di)
+    if out is None:
+        out = torch.empty(od, dtype=torch.bfloat16, device=x.device)
+    elif tuple(out.shape) != od or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 {od}")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    elif split_k:
+        need = conv_fwd_ncdhw_plan(tuple(x.shape), tuple(w.shape), st, pa, di)["workspace_bytes"]
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+            ws_ptr, ws_bytes = workspace.data_ptr(), need
+    rc = lib.conv_fwd_ncdhw(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                            _I32_3(*st), _I32_3(*pa), _I32_3(*di), CONV_DTYPE_BF16,
+                            _ptr(scale_x), _ptr(scale_w), _ptr(bias), out.data_ptr(), ws_ptr,
+                            ws_bytes, _stream_handle(stream))
+    _check(rc, "conv_fwd_ncdhw")
     return out
 
 
@@ -464,4 +527,7 @@ __all__ = [
     "conv_fwd", "conv_fwd_noalloc", "conv_fwd_plan", "conv_out_dims", "conv_get_device_status",
     "conv_set_wait_limit_ns", "pack_ncdhw_bf16_to_ndhwc", "pack_ncdhw_bf16_to_ndhwc_fp8",
     "conv3d", "conv2d", "conv1d", "load_library", "ConvError", "LIB_PATH",
+    "conv_fwd_from_host", "conv_fwd_kernel_launches", "conv_fwd_ncdhw",
+    "conv_fwd_ncdhw_plan", "conv_bwd_point_workspace_bytes", "conv_bwd_data_point",
+    "conv_bwd_weight_point",
 ]

@@ -182,6 +182,7 @@ struct Plan {
     int pair;                // CTA-pair kernel: 256-row units on clusters of two CTAs
     int msub;                // row sub-tiles per unit sharing each B stage
     int slices;              // launches the units are cut into (whole waves each)
+    int a_ncdhw;             // 1: x is channel-major (NCDHW), read as MN-major A boxes
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
@@ -273,7 +274,10 @@ bool patch_gather_class(const Geo& g, long long elt) {
 // ws_avail: workspace bytes the call can use (SIZE_MAX: plan the preferred
 // layout and report its size).  Split-K partials and the aligned operand
 // copies of the point-output GEMM are used only when they fit.
-int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_avail, Plan* P) {
+// ncdhw: x is channel-major [N, C, D, H, W] (g keeps the NDHWC names); only
+// the temporal class reads it, as MN-major A boxes of H*W positions.
+int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_avail, Plan* P,
+              bool ncdhw = false) {
     if (dtype != CONV_DTYPE_BF16 && dtype != CONV_DTYPE_FP8_E4M3) {
         set_error("unknown dtype");
         return CONV_ERR_INVALID;
@@ -282,12 +286,29 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     P->fp8 = dtype == CONV_DTYPE_FP8_E4M3;
     P->elt = P->fp8 ? 1 : 2;
     const long long elt = P->elt;
+    if (ncdhw) {
+        // a position-contiguous A tile needs the filter to leave H and W
+        // alone; TMA needs 16-byte plane and filter-row pitches
+        if (P->fp8) {
+            set_error("channel-major x: bf16 only");
+            return CONV_ERR_UNSUPPORTED;
+        }
+        if (!temporal_class(g)) {
+            set_error("channel-major x: T x 1 x 1 filters, unit H/W stride, no H/W padding");
+            return CONV_ERR_UNSUPPORTED;
+        }
+        if ((g.H * g.W) % 8 != 0 || (g.C * elt) % 16 != 0) {
+            set_error("channel-major x: H*W and C must be multiples of 8");
+            return CONV_ERR_UNSUPPORTED;
+        }
+        P->a_ncdhw = 1;
+    }
     const bool zero_pad = g.pd == 0 && g.ph == 0 && g.pw == 0;
     const bool unit_stride = g.sd == 1 && g.sh == 1 && g.sw == 1;
     const bool point_output = zero_pad && g.D == g.T && g.H == g.R && g.W == g.S;
     const bool pointwise = g.T == 1 && g.R == 1 && g.S == 1 && unit_stride && zero_pad;
     long long rg = 0;   // GEMM reduction length (elements)
-    if (point_output || pointwise) {
+    if (!ncdhw && (point_output || pointwise)) {
         P->cls = CONV_CLASS_POINT_GEMM;
         P->M = point_output ? g.N : g.N * g.D * g.H * g.W;
         rg = point_output ? g.T * g.R * g.S * g.C : g.C;
@@ -332,7 +353,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
             set_error("point-output GEMM needs T*R*S*C*elem_bytes %% 4 == 0");
             return CONV_ERR_UNSUPPORTED;
         }
-    } else if (patch_gather_class(g, elt)) {
+    } else if (!ncdhw && patch_gather_class(g, elt)) {
         // stride == filter, output larger than one point, and the implicit
         // classes cannot read x (channel rows or strides TMA cannot address):
         // gather the non-overlapping patches into GEMM rows, then one GEMM
@@ -403,6 +424,8 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         msub_pref = e->msub;
     }
     force_tile(&BN, &BK, &stages, &group_m, &splits);
+    // MN-major A boxes are 64 channel rows of 128 bytes: 128- or 256-byte k-steps
+    if (P->a_ncdhw && BK < 128) BK = 128;
     if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128 || BK == 256) ||
         (P->amode == AM_GEMM_GATHER && BK != 128) || group_m < 1) {
         set_error("invalid tile override");
@@ -665,6 +688,18 @@ int build_maps(const Geo& g, const Plan& P, const void* x, const void* w, TMaps*
         if (rc) return rc;
     }
     const cuuint64_t row = static_cast<cuuint64_t>(g.C) * elt;
+    if (P.amode == AM_TEMPORAL && P.a_ncdhw) {
+        // x as [N, C, D, H*W] -> dims {HW, D, C, N}, box {64, 1, 64, 1}:
+        // 64 channel rows of 64 positions, the MN-major 128-byte swizzle atom
+        const cuuint64_t hw = static_cast<cuuint64_t>(g.H * g.W);
+        const cuuint64_t plane = hw * elt;
+        const cuuint64_t adims[4] = {hw, static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.C),
+                                     static_cast<cuuint64_t>(g.N)};
+        const cuuint64_t astr[3] = {plane, plane * static_cast<cuuint64_t>(g.D),
+                                    plane * static_cast<cuuint64_t>(g.D * g.C)};
+        const cuuint32_t abox[4] = {64, 1, bke, 1};
+        return encode_tiled(tmA, 0, 4, x, adims, astr, abox, 128);
+    }
     if (P.amode == AM_TEMPORAL) {
         // x as [N, D, H*W, C] -> dims {C, HW, D, N}, box {bke, 128, 1, 1}
         const cuuint64_t hw = static_cast<cuuint64_t>(g.H * g.W);
@@ -768,6 +803,10 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.bias = bias;
     k.status = status;
     k.wait_ns = g_wait_ns;
+    if (P.a_ncdhw) {
+        k.a_mn = 1;
+        k.idesc |= 1u << 15;   // A major-ness: MN
+    }
 }
 
 // ------------------------------------------------------------ MN-major A GEMM
@@ -1063,13 +1102,18 @@ int conv_out_dims(const int64_t x_dims[5], const int64_t w_dims[5], const int st
     return CONV_OK;
 }
 
-int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
-                  const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
-                  int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
-                  size_t* workspace_bytes) {
-    Geo g;
-    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
-    if (rc) return rc;
+}   // extern "C"
+
+namespace {
+
+// NCDHW dims [N, C, D, H, W] in the NDHWC order the geometry uses
+void ndhwc_dims(const int64_t ncdhw[5], int64_t out[5]) {
+    out[0] = ncdhw[0]; out[1] = ncdhw[2]; out[2] = ncdhw[3]; out[3] = ncdhw[4]; out[4] = ncdhw[1];
+}
+
+int plan_query(const Geo& g, bool ncdhw, int dtype, int num_sms, int* cls, int* tile_n,
+               int* k_bytes, int* stages, int* splits, int* ctas, size_t* workspace_bytes) {
+    int rc = CONV_OK;
     int sms = num_sms, smem = 232448;
     if (sms <= 0) {
         DeviceInfo* d = nullptr;
@@ -1078,7 +1122,7 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
         smem = d->smem_optin;
     }
     Plan P;
-    if ((rc = make_plan(g, dtype, sms, smem, SIZE_MAX, &P))) return rc;
+    if ((rc = make_plan(g, dtype, sms, smem, SIZE_MAX, &P, ncdhw))) return rc;
     if (cls) *cls = P.cls;
     if (tile_n) *tile_n = P.BN;
     if (k_bytes) *k_bytes = P.BK;
@@ -1087,6 +1131,42 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
     if (ctas) *ctas = P.grid;
     if (workspace_bytes) *workspace_bytes = P.ws_bytes;
     return CONV_OK;
+}
+
+int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
+             const float* scale_x, const float* scale_w, const float* bias, void* out,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace
+
+extern "C" {
+
+int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                  const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
+                  int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
+                  size_t* workspace_bytes) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    return plan_query(g, false, dtype, num_sms, cls, tile_n, k_bytes, stages, splits, ctas,
+                      workspace_bytes);
+}
+
+int conv_fwd_ncdhw_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                        const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
+                        int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
+                        size_t* workspace_bytes) {
+    if (!x_dims) {
+        set_error("null shape argument");
+        return CONV_ERR_INVALID;
+    }
+    int64_t xd[5];
+    ndhwc_dims(x_dims, xd);
+    Geo g;
+    int rc = make_geo(xd, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    return plan_query(g, true, dtype, num_sms, cls, tile_n, k_bytes, stages, splits, ctas,
+                      workspace_bytes);
 }
 
 int conv_fwd(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
@@ -1104,6 +1184,35 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
     Geo g;
     int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
     if (rc) return rc;
+    return fwd_impl(g, false, x, w, dtype, scale_x, scale_w, bias, out, workspace,
+                    workspace_bytes, stream);
+}
+
+int conv_fwd_ncdhw(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+                   const int stride[3], const int pad[3], const int dil[3], int dtype,
+                   const float* scale_x, const float* scale_w, const float* bias, void* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x_dims) {
+        set_error("null shape argument");
+        return CONV_ERR_INVALID;
+    }
+    int64_t xd[5];
+    ndhwc_dims(x_dims, xd);
+    Geo g;
+    int rc = make_geo(xd, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    return fwd_impl(g, true, x, w, dtype, scale_x, scale_w, bias, out, workspace,
+                    workspace_bytes, stream);
+}
+
+}   // extern "C"
+
+namespace {
+
+int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
+             const float* scale_x, const float* scale_w, const float* bias, void* out,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int rc = CONV_OK;
     if (!x || !w || !out) {
         set_error("null tensor pointer");
         return CONV_ERR_INVALID;
@@ -1123,7 +1232,7 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
     }
     Plan P;
     if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace ? workspace_bytes : 0,
-                        &P)))
+                        &P, ncdhw)))
         return rc;
     const void* xa = x;
     const void* wa = w;
@@ -1205,6 +1314,10 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
     }
     return CONV_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* w_host,
                        const int64_t w_dims[5], const int stride[3], const int pad[3],

@@ -481,7 +481,20 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
                     const int cj = c0 + j * box_e;   // channels past C read as zeros
                     for (int sub = 0; sub < MSUB; ++sub) {
                         const uint32_t adst = adst0 + (sub * NB + j) * abox;
-                        if (PAIR) {
+                        if (AMODE == AM_TEMPORAL && p.a_mn) {
+                            // channel-major x (NCDHW): the tap's input plane
+                            // as two MN-major boxes of 64 H*W positions x 64
+                            // channels (map dims {H*W, D, C, N})
+                            const int dpl = ad[sub] + ft * p.dd;
+                            if (PAIR) {
+                                tma_load_4d_pair(adst, tmA, fb, ah[sub], dpl, cj, an[sub]);
+                                tma_load_4d_pair(adst + 8192u, tmA, fb, ah[sub] + 64, dpl, cj,
+                                                 an[sub]);
+                            } else {
+                                tma_load_4d(adst, tmA, fb, ah[sub], dpl, cj, an[sub]);
+                                tma_load_4d(adst + 8192u, tmA, fb, ah[sub] + 64, dpl, cj, an[sub]);
+                            }
+                        } else if (PAIR) {
                             if (AMODE == AM_IM2COL)
                                 tma_load_im2col_5d_pair(adst, tmA, fb, cj, aw[sub], ah[sub],
                                                         ad[sub], an[sub], ow, oh, od);

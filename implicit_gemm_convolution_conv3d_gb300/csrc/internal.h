@@ -58,8 +58,8 @@ struct KParams {
     uint32_t epi_bytes; // shared staging of the epilogue (0: direct stores from registers)
     int epi_mode;       // 0 direct stores, 1 TMA tensor stores, 2 staged 8- / 4-byte stores
     int pair;           // 1: CTA-pair kernel (cluster of 2, 256-row units)
-    int a_mn;           // 1: A is MN-major in memory ([K rows, M contiguous]; GEMM mode,
-                        //    128-byte k-steps, one row sub-tile)
+    int a_mn;           // 1: A is MN-major in memory (M contiguous; 128- or 256-byte k-steps):
+                        //    GEMM mode [K rows, M], or temporal mode over channel-major x
     int msub;           // row sub-tiles per unit sharing each B stage (1 or 2)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;

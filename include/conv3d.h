@@ -13,6 +13,9 @@
  *     conv2d/conv1d reshape wrappers.  Point-output (patch-embedding) shapes
  *     are one plain GEMM: MIOpen PR #10912 "Use a single GEMM for
  *     point-output conv in all three directions", description.
+ *   - conv_fwd_ncdhw: the same conv reading a channel-major activation in
+ *     place, the NCDHW-direct kernel FlyDSL PR #860's 3x1x1 / 1x1x1 commits
+ *     leave to future work.
  *   - pack_ncdhw_bf16_to_ndhwc(_fp8): FlyDSL PR #860, commit adding the
  *     tiled NCDHW->NDHWC bf16->fp8 pack kernel (replacing torch.permute) and
  *     the commit fixing its >2 GB addressing.
@@ -133,6 +136,40 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
                   const int stride[3], const int pad[3], const int dil[3], int dtype,
                   const float* scale_x, const float* scale_w, const float* bias, void* out,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* conv_fwd_bias over a channel-major (NCDHW) activation, read in place: no
+ * NCDHW -> NDHWC pass before the convolution.
+ *   out[n,od,h,w,k] = bf16_rn( scale_x * scale_w *
+ *       sum_{t,c} x[n, c, od*sd-pd+t*dd, h, w] * w[k,t,0,0,c] + bias[k] )
+ *   x        device, NCDHW [N,C,D,H,W] bf16, 16-byte aligned
+ *   x_dims   = {N, C, D, H, W}  (channel-major order, unlike conv_fwd)
+ *   w        device, KTRSC [K,T,1,1,C] bf16
+ *   out      device, NDHWC [N,Do,H,W,K] bf16 (conv_out_dims of the NDHWC
+ *            view); fully overwritten
+ *   stride, pad, dil, scale_x, scale_w, bias, workspace, stream: as for
+ *            conv_fwd_bias (workspace size from conv_fwd_ncdhw_plan)
+ * Coverage: bf16; T x 1 x 1 filters (any T, temporal stride, pad and
+ * dilation; T = 1 is the pointwise conv) with unit H/W stride and no H/W
+ * padding; H*W and C multiples of 8.  Anything else: CONV_ERR_UNSUPPORTED
+ * (no fallback).  Each tap's A tile is 128 consecutive H*W positions of one
+ * input plane by a block of channels, loaded as position-contiguous
+ * (MN-major) TMA boxes.  Defined by: FlyDSL PR #860, the commits that drop
+ * the 3x1x1 unfold path (a kernel reading NCDHW straight into the GEMM,
+ * without materialising A, is left to future work) and the 1x1x1 matmul
+ * path (the NCDHW -> NDHWC transpose costs about 5-6 ms of the 8.7 ms
+ * pointwise conv); the math is conv_fwd's.  An fp8 variant that quantises
+ * while loading is not covered. */
+int conv_fwd_ncdhw(const void* x, const int64_t x_dims[5], const void* w, const int64_t w_dims[5],
+                   const int stride[3], const int pad[3], const int dil[3], int dtype,
+                   const float* scale_x, const float* scale_w, const float* bias, void* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* conv_fwd_plan for conv_fwd_ncdhw (x_dims = {N, C, D, H, W}); the class is
+ * always CONV_CLASS_TEMPORAL.  Host-only when num_sms > 0. */
+int conv_fwd_ncdhw_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
+                        const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
+                        int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
+                        size_t* workspace_bytes);
 
 /* conv_fwd with the operands and the result in HOST memory: the same
  * convolution (same definition and plan as conv_fwd, so the same output

@@ -201,3 +201,35 @@ def test_backward_argument_checks(pkg):
         # a 3x3 filter over an 8x8 input has many output positions
         assert fn(a, b, I5(2, 1, 8, 8, 16), I5(32, 1, 3, 3, 16), one, zero, one, a, a,
                   ctypes.c_size_t(1 << 20), None) == pkg.CONV_ERR_UNSUPPORTED
+
+
+def test_ncdhw_plan_coverage(pkg):
+    """conv_fwd_ncdhw plans: always the temporal class with 128- or 256-byte
+    k-steps (MN-major boxes of 64 channel rows); T x 1 x 1 filters only,
+    bf16 only, H*W and C multiples of 8."""
+    sms = 148
+    p = pkg.conv_fwd_ncdhw_plan((1, 640, 240, 160, 90), (640, 3, 1, 1, 640), 1, (1, 0, 0), 1, 0, sms)
+    assert p["class"] == "temporal" and p["k_bytes"] == 256 and p["splits"] == 1
+    # the pointwise conv stays in the temporal class (its NDHWC form is a GEMM)
+    p = pkg.conv_fwd_ncdhw_plan((2, 64, 3, 4, 6), (32, 1, 1, 1, 64), 1, 0, 1, 0, sms)
+    assert p["class"] == "temporal" and p["k_bytes"] >= 128
+    assert pkg.conv_fwd_plan((2, 3, 4, 6, 64), (32, 1, 1, 1, 64), 1, 0, 1, 0, sms)["class"] == \
+        "point_gemm"
+    # narrow channel rows still take 128-byte k-steps (channels past C read zero)
+    p = pkg.conv_fwd_ncdhw_plan((1, 8, 5, 4, 4), (16, 2, 1, 1, 8), (2, 1, 1), (1, 0, 0), (2, 1, 1),
+                                0, sms)
+    assert p["class"] == "temporal" and p["k_bytes"] == 128
+    bad = [
+        ((1, 64, 4, 8, 8), (32, 1, 3, 3, 64), 1, (0, 1, 1), 0),    # spatial taps
+        ((1, 64, 4, 8, 8), (32, 3, 1, 1, 64), (1, 2, 2), (1, 0, 0), 0),   # H/W stride
+        ((1, 64, 4, 5, 5), (32, 3, 1, 1, 64), 1, (1, 0, 0), 0),    # H*W = 25
+        ((1, 60, 4, 8, 8), (32, 3, 1, 1, 60), 1, (1, 0, 0), 0),    # C % 8 != 0
+        ((1, 64, 4, 8, 8), (32, 3, 1, 1, 64), 1, (1, 0, 0), 1),    # fp8
+    ]
+    for xs, ws, st, pa, dt in bad:
+        with pytest.raises(pkg.ConvError) as e:
+            pkg.conv_fwd_ncdhw_plan(xs, ws, st, pa, 1, dt, sms)
+        assert e.value.status == pkg.CONV_ERR_UNSUPPORTED, (xs, ws)
+    with pytest.raises(pkg.ConvError) as e:   # C of x (dim 1) against w
+        pkg.conv_fwd_ncdhw_plan((1, 64, 4, 8, 8), (32, 3, 1, 1, 32), 1, 0, 1, 0, sms)
+    assert e.value.status == pkg.CONV_ERR_INVALID

@@ -128,6 +128,27 @@ def test_temporal_big_sampled(pkg):
     _check_sampled(y, bits16(x), bits16(w), idx, wl)
 
 
+@pytest.mark.parametrize("name", ["temporal_3x1x1_bf16_ncdhw", "pointwise_1x1x1_bf16_ncdhw"])
+def test_channel_major_sampled(pkg, name):
+    """conv_fwd_ncdhw at full size on channel-major activations: the temporal
+    workload (2.2e9 elements, 64-bit offsets) and the 14 GB pointwise conv,
+    against the oracle reading the same NCDHW bytes."""
+    wl = cw.BY_NAME[name]
+    x, w = cw.make_inputs(wl, "cuda")
+    y = pkg.conv_fwd_ncdhw(x, w, wl.stride, wl.pad, wl.dil)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    plan = pkg.conv_fwd_ncdhw_plan(wl.x_shape, wl.w_shape, wl.stride, wl.pad, wl.dil)
+    idx = _sample(tuple(y.shape), wl, plan["tile_n"])
+    got = y.view(-1)[torch.from_numpy(idx).cuda()].float().cpu().double().numpy()
+    del y
+    xb, wb = bits16(x), bits16(w)
+    del x
+    torch.cuda.empty_cache()
+    ref = oracle.conv3d_points(xb, wb, idx, wl.stride, wl.pad, wl.dil, x_layout="ncdhw")
+    assert_close(got, ref, wl.name)
+
+
 @pytest.mark.parametrize("name", ["vit_patch16_bf16", "vit_patch14_bf16"])
 def test_vit_patch_embed_sampled(pkg, name):
     """Patch embeddings with 196 / 256 patches per image, at full size: the
