@@ -106,8 +106,11 @@ NCDHW_WORKLOADS = [
              (1, 1, 1), (1, 0, 0), x_layout="ncdhw"),
     Workload("pointwise_1x1x1_bf16_ncdhw", 11, (1, 512, 240, 320, 180), (48, 1, 1, 1, 512),
              (1, 1, 1), (0, 0, 0), x_layout="ncdhw"),
-    # profiler-capture size of the first (16 frames, 295 MB)
+    # profiler-capture sizes of the first: 16 frames (channel planes 0.46 MB
+    # apart) and 96 frames (2.8 MB apart, past a 2 MB page per channel plane)
     Workload("temporal_3x1x1_bf16_ncdhw_small", 12, (1, 640, 16, 160, 90), (640, 3, 1, 1, 640),
+             (1, 1, 1), (1, 0, 0), x_layout="ncdhw"),
+    Workload("temporal_3x1x1_bf16_ncdhw_d96", 13, (1, 640, 96, 160, 90), (640, 3, 1, 1, 640),
              (1, 1, 1), (1, 0, 0), x_layout="ncdhw"),
 ]
 

@@ -183,6 +183,8 @@ struct Plan {
     int msub;                // row sub-tiles per unit sharing each B stage
     int slices;              // launches the units are cut into (whole waves each)
     int a_ncdhw;             // 1: x is channel-major (NCDHW), read as MN-major A boxes
+    int ncdhw_pack;          // 1: x is channel-major, packed to an NDHWC copy in the
+                             //    workspace before the conv reads it
     size_t ws_bytes;         // split-K workspace needed by this plan
 };
 
@@ -274,8 +276,14 @@ bool patch_gather_class(const Geo& g, long long elt) {
 // ws_avail: workspace bytes the call can use (SIZE_MAX: plan the preferred
 // layout and report its size).  Split-K partials and the aligned operand
 // copies of the point-output GEMM are used only when they fit.
+// Channel planes (D*H*W elements of one channel) up to this size are read in
+// place from a channel-major x; larger ones are packed first when the filter
+// has several taps.
+constexpr long long kInPlaceChannelBytes = 1ll << 20;
+
 // ncdhw: x is channel-major [N, C, D, H, W] (g keeps the NDHWC names); only
-// the temporal class reads it, as MN-major A boxes of H*W positions.
+// the temporal class reads it, as MN-major A boxes of H*W positions, or from
+// an NDHWC copy packed into the workspace (ncdhw_pack).
 int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_avail, Plan* P,
               bool ncdhw = false) {
     if (dtype != CONV_DTYPE_BF16 && dtype != CONV_DTYPE_FP8_E4M3) {
@@ -301,7 +309,23 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
             set_error("channel-major x: H*W and C must be multiples of 8");
             return CONV_ERR_UNSUPPORTED;
         }
-        P->a_ncdhw = 1;
+        // In-place reads touch one page per channel plane per tile: with
+        // channel planes past about 1 MB (a 2 MB page each) and every plane
+        // read again by the other taps, the translations miss and L2 reuse
+        // collapses (3x the DRAM reads, 1.8x the time on the 3x1x1 workload).
+        // There, when the workspace holds an NDHWC copy, x is packed into it
+        // first (6.4 ms against 8.7 ms in place on that workload).
+        // CONV3D_NCDHW_INPLACE=1 keeps in-place reads.
+        const size_t xcopy =
+            static_cast<size_t>((g.N * g.C * g.D * g.H * g.W * elt + 255) / 256 * 256);
+        const char* ip = std::getenv("CONV3D_NCDHW_INPLACE");
+        if (g.T > 1 && g.D * g.H * g.W * elt > kInPlaceChannelBytes && g.C % 16 == 0 &&
+            ws_avail >= xcopy && !(ip && ip[0] == '1')) {
+            P->ncdhw_pack = 1;
+            P->repack_bytes = xcopy;
+        } else {
+            P->a_ncdhw = 1;
+        }
     }
     const bool zero_pad = g.pd == 0 && g.ph == 0 && g.pw == 0;
     const bool unit_stride = g.sd == 1 && g.sh == 1 && g.sw == 1;
@@ -1209,6 +1233,52 @@ int conv_fwd_ncdhw(const void* x, const int64_t x_dims[5], const void* w, const 
 
 namespace {
 
+// Launch the conv units of plan P whose kernel parameters are k (all
+// m-tiles): one launch, or P.slices launches of whole waves.
+cudaError_t launch_units(const Plan& P, const TMaps& tm, const KParams& k, cudaStream_t stream) {
+    int bounds[kMaxChunks + 1];
+    const int nsl = P.slices > 1 ? plan_even_slices(P, P.slices, bounds) : 1;
+    if (nsl == 1) return launch_igemm(P.amode, P.fp8, &tm, k, P.grid, P.smem, stream);
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < nsl && e == cudaSuccess; ++i) {
+        KParams ki = k;
+        ki.m_tile0 = bounds[i];
+        ki.m_tiles = bounds[i + 1] - bounds[i];
+        const long long units = static_cast<long long>(ki.m_tiles) * P.n_tiles;
+        const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
+                                : static_cast<int>(std::min<long long>(units, P.grid));
+        e = launch_igemm(P.amode, P.fp8, &tm, ki, grid, P.smem, stream);
+    }
+    return e;
+}
+
+// Channel-major x through an NDHWC copy at the head of the workspace: the
+// pack, then the conv of the copy, both on the caller's stream.  (Packing
+// slice by slice on a second stream while the conv runs was slower, 6.9-7.2
+// ms against 6.4 ms on the 3x1x1 workload: under the power cap the pack's
+// draw slows the tensor-bound conv by more than the overlap saves.)
+int ncdhw_via_copy(const Geo& g, const Plan& P, DeviceInfo* dev, const void* x, const void* w,
+                   const float* scale_x, const float* scale_w, const float* bias, void* out,
+                   void* workspace, cudaStream_t stream) {
+    int rc;
+    void* xc = workspace;
+    TMaps tm;
+    if ((rc = build_maps(g, P, xc, w, &tm))) return rc;
+    if ((rc = build_out_map(g, P, out, &tm))) return rc;
+    KParams k;
+    fill_params(g, P, xc, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
+    cudaError_t e = launch_pack(x, g.N, g.C, g.D * g.H * g.W, xc, 0, nullptr, nullptr,
+                                dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    if ((e = launch_units(P, tm, k, stream)) != cudaSuccess)
+        return cuda_fail(e, "conv kernel launch");
+    if (P.splits > 1 &&
+        (e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K,
+                                  dev->num_sms, stream)) != cudaSuccess)
+        return cuda_fail(e, "split-K reduce launch");
+    return CONV_OK;
+}
+
 int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
              const float* scale_x, const float* scale_w, const float* bias, void* out,
              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -1234,6 +1304,8 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
     if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace ? workspace_bytes : 0,
                         &P, ncdhw)))
         return rc;
+    if (P.ncdhw_pack)
+        return ncdhw_via_copy(g, P, dev, x, w, scale_x, scale_w, bias, out, workspace, stream);
     const void* xa = x;
     const void* wa = w;
     if (P.repack == 2) {
@@ -1290,22 +1362,7 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
                      P.m_tiles, P.n_tiles, P.grid, P.smem, P.tmem_cols, P.epi_bytes, P.pair, P.msub,
                      P.phases, P.repack);
     }
-    cudaError_t e = cudaSuccess;
-    int bounds[kMaxChunks + 1];
-    const int nsl = P.slices > 1 ? plan_even_slices(P, P.slices, bounds) : 1;
-    if (nsl > 1) {
-        for (int i = 0; i < nsl && e == cudaSuccess; ++i) {
-            KParams ki = k;
-            ki.m_tile0 = bounds[i];
-            ki.m_tiles = bounds[i + 1] - bounds[i];
-            const long long units = static_cast<long long>(ki.m_tiles) * P.n_tiles;
-            const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
-                                    : static_cast<int>(std::min<long long>(units, P.grid));
-            e = launch_igemm(P.amode, P.fp8, &tm, ki, grid, P.smem, stream);
-        }
-    } else {
-        e = launch_igemm(P.amode, P.fp8, &tm, k, P.grid, P.smem, stream);
-    }
+    cudaError_t e = launch_units(P, tm, k, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
         e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K,

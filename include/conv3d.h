@@ -153,7 +153,12 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
  * padding; H*W and C multiples of 8.  Anything else: CONV_ERR_UNSUPPORTED
  * (no fallback).  Each tap's A tile is 128 consecutive H*W positions of one
  * input plane by a block of channels, loaded as position-contiguous
- * (MN-major) TMA boxes.  Defined by: FlyDSL PR #860, the commits that drop
+ * (MN-major) TMA boxes.  Exception: with T > 1, C % 16 == 0, channel planes
+ * (D*H*W*2 bytes) above 1 MiB and a workspace that holds an NDHWC copy of x
+ * (the size conv_fwd_ncdhw_plan reports), x is first packed into that copy
+ * and the copy convolved: in-place reads of such planes, revisited by every
+ * tap, thrash address translation and L2 (three times the DRAM reads).  A
+ * smaller workspace keeps the in-place reads; the result is the same.  Defined by: FlyDSL PR #860, the commits that drop
  * the 3x1x1 unfold path (a kernel reading NCDHW straight into the GEMM,
  * without materialising A, is left to future work) and the 1x1x1 matmul
  * path (the NCDHW -> NDHWC transpose costs about 5-6 ms of the 8.7 ms

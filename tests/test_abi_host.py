@@ -210,6 +210,11 @@ def test_ncdhw_plan_coverage(pkg):
     sms = 148
     p = pkg.conv_fwd_ncdhw_plan((1, 640, 240, 160, 90), (640, 3, 1, 1, 640), 1, (1, 0, 0), 1, 0, sms)
     assert p["class"] == "temporal" and p["k_bytes"] == 256 and p["splits"] == 1
+    # 6.9 MB channel planes read by three taps: packed to an NDHWC copy in the workspace
+    assert p["workspace_bytes"] >= 640 * 240 * 160 * 90 * 2
+    # 0.46 MB channel planes: read in place, no workspace
+    p = pkg.conv_fwd_ncdhw_plan((1, 640, 16, 160, 90), (640, 3, 1, 1, 640), 1, (1, 0, 0), 1, 0, sms)
+    assert p["workspace_bytes"] == 0
     # the pointwise conv stays in the temporal class (its NDHWC form is a GEMM)
     p = pkg.conv_fwd_ncdhw_plan((2, 64, 3, 4, 6), (32, 1, 1, 1, 64), 1, 0, 1, 0, sms)
     assert p["class"] == "temporal" and p["k_bytes"] >= 128

@@ -202,3 +202,62 @@ def test_ncdhw_rejects_uncovered_shapes(pkg):
         pkg.conv_fwd_ncdhw(x.to(torch.float8_e4m3fn),
                            torch.zeros((32, 3, 1, 1, 64), dtype=torch.float8_e4m3fn,
                                        device="cuda"), 1, (1, 0, 0), 1)
+
+
+# Channel planes past 1 MB with several taps: x is packed to an NDHWC copy in
+# the workspace, then convolved.
+PIPE_CASES = [
+    ((1, 16, 40, 128, 128), 32, 3, 1, 1, 1),    # 1.3 MB channel planes
+    ((2, 16, 32, 128, 160), 48, 2, 1, 1, 1),    # two images
+    ((1, 32, 36, 128, 128), 40, 3, 2, 2, 2),    # temporal stride and dilation
+]
+
+
+@pytest.mark.parametrize("i", range(len(PIPE_CASES)))
+def test_ncdhw_packed_copy_matches_oracle(pkg, i):
+    xs, K, T, st, pa, di = _geometry(PIPE_CASES[i])
+    x, w = _operands(xs, K, T, 300 + i)
+    plan = pkg.conv_fwd_ncdhw_plan(xs, tuple(w.shape), st, pa, di)
+    assert plan["workspace_bytes"] >= x.numel() * 2   # the NDHWC copy
+    y = pkg.conv_fwd_ncdhw(x, w, st, pa, di)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    idx, ref = _reference(x, w, st, pa, di, tuple(y.shape), 300 + i)
+    assert_close(_got(y, idx), ref, f"packed-copy case {i} x{xs} K{K} T{T}")
+    # the same bits as conv_fwd over an NDHWC copy (same plan, same reduction order)
+    xn = x.permute(0, 2, 3, 4, 1).contiguous()
+    b = pkg.conv_fwd(xn, w, st, pa, di)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), b.view(torch.int16))
+
+
+def test_ncdhw_small_workspace_reads_in_place(pkg):
+    """Without room for the NDHWC copy (or with CONV3D_NCDHW_INPLACE=1) the
+    same problem reads x in place; both against the oracle."""
+    xs, K, T, st, pa, di = _geometry(PIPE_CASES[0])
+    x, w = _operands(xs, K, T, 310)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    a = pkg.conv_fwd_ncdhw(x, w, st, pa, di, workspace=ws)
+    with _env({"CONV3D_NCDHW_INPLACE": 1}):
+        b = pkg.conv_fwd_ncdhw(x, w, st, pa, di)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    idx, ref = _reference(x, w, st, pa, di, tuple(a.shape), 310)
+    assert_close(_got(a, idx), ref, "in place (small workspace)")
+    assert_close(_got(b, idx), ref, "in place (forced)")
+
+
+def test_ncdhw_packed_copy_on_side_stream(pkg):
+    """The call on a non-default stream: the result is ordered on that stream."""
+    xs, K, T, st, pa, di = _geometry(PIPE_CASES[1])
+    x, w = _operands(xs, K, T, 320)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = pkg.conv_fwd_ncdhw(x, w, st, pa, di, stream=s)
+        z = y.float().sum()
+    s.synchronize()
+    xn = x.permute(0, 2, 3, 4, 1).contiguous()
+    b = pkg.conv_fwd(xn, w, st, pa, di)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), b.view(torch.int16))
+    assert torch.isfinite(z)
