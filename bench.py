@@ -263,8 +263,9 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias
         raise RuntimeError("device status reports a timeout")
     times = Timer(steps, flush).run(step)
     if ncdhw:
-        # the channel-major plans here run unsliced (reductions under 384 k-steps)
-        launches = 1 + (plan["splits"] > 1)
+        # the channel-major plans here run unsliced (reductions under 384 k-steps);
+        # a plan whose workspace holds an NDHWC copy of x packs it first
+        launches = 1 + (plan["splits"] > 1) + (plan["workspace_bytes"] >= x.numel() * 2)
     else:
         launches = pkg.conv_fwd_kernel_launches(tuple(x.shape), tuple(w.shape), wl.stride,
                                                 wl.pad, wl.dil, 1 if wl.dtype == "fp8" else 0,
