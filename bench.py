@@ -348,7 +348,24 @@ def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
     times = Timer(steps, flush).run(step)
     h2d = hx.numel() * hx.element_size() + hw.numel() * hw.element_size()
     d2h = hout.numel() * hout.element_size()
-    return {"ms": times, "h2d": h2d, "d2h": d2h}
+    return {"ms": times, "h2d": h2d, "d2h": d2h, "link": link_bandwidth(hx, dx, hout, out)}
+
+
+def link_bandwidth(h_in, d_in, h_out, d_out):
+    """Host<->device copy bandwidth of this machine (GB/s), one plain copy
+    each way between the e2e leg's own pinned buffers, alone on the stream:
+    the bound the end-to-end number cannot beat."""
+    res = {}
+    for name, dst, src in (("h2d_gbs", d_in, h_in), ("d2h_gbs", h_out, d_out)):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        dst.copy_(src, non_blocking=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle arm
@@ -564,7 +581,8 @@ def main_arm(args):
                            baseline_note="vs_baseline divides by the MI355X figure for this shape "
                                          "(967 TFLOPS, FlyDSL PR #860): context only"),
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": res["e2e"]["h2d"],
-                    "d2h_bytes_per_step": res["e2e"]["d2h"], "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": res["e2e"]["d2h"], "ms_per_step": e2e_ms,
+                    "link_gbs_measured": res["e2e"]["link"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(),
             "workloads": secondary}
