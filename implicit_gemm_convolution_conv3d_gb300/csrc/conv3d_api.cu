@@ -927,11 +927,12 @@ int bwd_setup(const int64_t x_dims[5], const int64_t w_dims[5], const int stride
 // Per device: a copy-in and a copy-out stream and the events that order them
 // against the caller's stream.  Created on first use, kept until exit.
 constexpr int kMaxChunks = 32;
+constexpr int kMaxWGroups = 8;   // weight copies the first slice is split over
 struct Pipe {
     bool ready;
     cudaStream_t s_in, s_out;
     cudaEvent_t start, in_done, out_done;
-    cudaEvent_t ev_in[kMaxChunks], ev_conv[kMaxChunks];
+    cudaEvent_t ev_in[kMaxChunks], ev_conv[kMaxChunks], ev_w[kMaxWGroups];
     std::mutex mu;   // one enqueue at a time per device
 };
 Pipe g_pipe[kMaxDevices];
@@ -954,7 +955,7 @@ int pipe_for_device(Pipe** out) {
             cudaStreamDestroy(p.s_in);
             return cuda_fail(e, "cudaStreamCreateWithFlags");
         }
-        cudaEvent_t* evs[3 + 2 * kMaxChunks];
+        cudaEvent_t* evs[3 + 2 * kMaxChunks + kMaxWGroups];
         int n = 0;
         evs[n++] = &p.start;
         evs[n++] = &p.in_done;
@@ -963,6 +964,7 @@ int pipe_for_device(Pipe** out) {
             evs[n++] = &p.ev_in[i];
             evs[n++] = &p.ev_conv[i];
         }
+        for (int i = 0; i < kMaxWGroups; ++i) evs[n++] = &p.ev_w[i];
         for (int i = 0; i < n; ++i) {
             if ((e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming)) != cudaSuccess) {
                 for (int j = 0; j < i; ++j) cudaEventDestroy(*evs[j]);
@@ -1453,9 +1455,32 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         (e = cudaStreamWaitEvent(pp->s_in, pp->start, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(pp->s_out, pp->start, 0)) != cudaSuccess)
         return cuda_fail(e, "stream ordering");
-    if ((e = cudaMemcpyAsync(w_dev, w_host, w_bytes, cudaMemcpyHostToDevice, pp->s_in)) !=
-        cudaSuccess)
-        what = "cudaMemcpyAsync (weights)";
+    // The first slice (one block: whole waves over all column tiles) runs as
+    // one wave per group of column tiles, each launched once that group's
+    // weight rows have landed: the lead-in before the first kernel copies one
+    // group's weights and the slice's input planes, not all the weights.
+    int wgroups = 1, gtiles = P.n_tiles;
+    {
+        const long long wave = P.grid >> P.pair;
+        const long long units0 = static_cast<long long>(bounds[1] - bounds[0]) * P.n_tiles;
+        const long long waves0 = units0 % wave == 0 ? units0 / wave : 0;
+        const char* ws = std::getenv("CONV3D_WSPLIT");
+        if (waves0 >= 2 && waves0 <= kMaxWGroups && P.n_tiles % waves0 == 0 && !(ws && ws[0] == '0')) {
+            wgroups = static_cast<int>(waves0);
+            gtiles = P.n_tiles / wgroups;
+        }
+    }
+    const size_t w_row = w_bytes / static_cast<size_t>(g.K);   // one filter's bytes
+    auto copy_w_group = [&](int s) -> cudaError_t {
+        const long long r0 = static_cast<long long>(s) * gtiles * P.BN;
+        const long long r1 = s == wgroups - 1 ? g.K : std::min<long long>(g.K, r0 + gtiles * P.BN);
+        if (r1 <= r0) return cudaSuccess;
+        return cudaMemcpyAsync(static_cast<unsigned char*>(w_dev) + r0 * w_row,
+                               static_cast<const unsigned char*>(w_host) + r0 * w_row,
+                               static_cast<size_t>(r1 - r0) * w_row, cudaMemcpyHostToDevice,
+                               pp->s_in);
+    };
+    if ((e = copy_w_group(0)) != cudaSuccess) what = "cudaMemcpyAsync (weights)";
     size_t x_done = 0;
     for (int i = 0; i < n && !what; ++i) {
         const int mt0 = bounds[i], mt1 = bounds[i + 1];
@@ -1475,19 +1500,35 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
             what = "stream ordering";
             break;
         }
+        // the other weight groups follow the first slice's input planes
+        for (int s = 1; i == 0 && s < wgroups && !what; ++s)
+            if ((e = copy_w_group(s)) != cudaSuccess ||
+                (e = cudaEventRecord(pp->ev_w[s], pp->s_in)) != cudaSuccess)
+                what = "cudaMemcpyAsync (weights)";
+        if (what) break;
         k.m_tile0 = mt0;
         k.m_tiles = mt1 - mt0;
-        const long long units = static_cast<long long>(k.m_tiles) * P.n_tiles;
-        const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
-                                : static_cast<int>(std::min<long long>(units, P.grid));
-        if (std::getenv("CONV3D_LOG"))
-            std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) rows [%lld, %lld) "
-                         "x prefix %zu B grid %d\n", i, mt0, mt1, row_lo, row_hi, x_done, grid);
-        if ((e = launch_igemm(P.amode, P.fp8, &tm, k, grid, P.smem, stream)) !=
-            cudaSuccess) {
-            what = "conv kernel launch";
-            break;
+        const int parts = i == 0 ? wgroups : 1;
+        for (int s = 0; s < parts && !what; ++s) {
+            k.n_tile0 = parts > 1 ? s * gtiles : 0;
+            k.n_tiles = parts > 1 ? gtiles : P.n_tiles;
+            if (s > 0 && (e = cudaStreamWaitEvent(stream, pp->ev_w[s], 0)) != cudaSuccess) {
+                what = "stream ordering";
+                break;
+            }
+            const long long units = static_cast<long long>(k.m_tiles) * k.n_tiles;
+            const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
+                                    : static_cast<int>(std::min<long long>(units, P.grid));
+            if (std::getenv("CONV3D_LOG"))
+                std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) n-tiles "
+                             "[%d, %d) rows [%lld, %lld) x prefix %zu B grid %d\n", i, mt0, mt1,
+                             k.n_tile0, k.n_tile0 + k.n_tiles, row_lo, row_hi, x_done, grid);
+            if ((e = launch_igemm(P.amode, P.fp8, &tm, k, grid, P.smem, stream)) != cudaSuccess)
+                what = "conv kernel launch";
         }
+        k.n_tile0 = 0;
+        k.n_tiles = P.n_tiles;
+        if (what) break;
         if ((e = cudaEventRecord(pp->ev_conv[i], stream)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(pp->s_out, pp->ev_conv[i], 0)) != cudaSuccess) {
             what = "stream ordering";

@@ -71,7 +71,8 @@ __device__ __forceinline__ void temporal_tile(int m_tile, const KParams& p, int&
 // Work unit -> (m-tile, n-tile, split).  Within a split, tiles are walked in
 // groups of `group_m` m-tiles: down M first, then across N, so that CTAs
 // running at the same time share both A rows and B columns in L2.  A launch
-// covers the m-tiles [m_tile0, m_tile0 + m_tiles).
+// covers the m-tiles [m_tile0, m_tile0 + m_tiles) and the column tiles
+// [n_tile0, n_tile0 + n_tiles).
 __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     const int tiles = p.m_tiles * p.n_tiles;
     Unit r;
@@ -83,7 +84,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     const int gm = min(p.group_m, p.m_tiles - first_m);
     const int local = t - g * group;
     r.m_tile = p.m_tile0 + first_m + local % gm;
-    r.n_tile = local / gm;
+    r.n_tile = p.n_tile0 + local / gm;
     return r;
 }
 
@@ -622,7 +623,7 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                 const Unit t = decode_unit(u, p);
                 const long long m0 = static_cast<long long>(t.m_tile) * kBM;
                 const long long n0 = static_cast<long long>(t.n_tile) * p.BN;
-                if (t.n_tile == 0 && t.split == 0)
+                if (t.n_tile == p.n_tile0 && t.split == 0)
                     prefetch_rows(p.ga, m0, min(m0 + kBM, p.M), p.g_row_bytes);
                 if (t.m_tile == p.m_tile0 && t.split == 0)
                     prefetch_rows(p.gb, n0, min(n0 + p.BN, static_cast<long long>(p.K)),

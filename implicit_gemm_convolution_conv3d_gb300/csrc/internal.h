@@ -61,6 +61,7 @@ struct KParams {
     int a_mn;           // 1: A is MN-major in memory (M contiguous; 128- or 256-byte k-steps):
                         //    GEMM mode [K rows, M], or temporal mode over channel-major x
     int msub;           // row sub-tiles per unit sharing each B stage (1 or 2)
+    int n_tile0;        // first column tile of this launch (n_tiles column tiles from it)
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;
     const unsigned char* gb;
