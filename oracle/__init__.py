@@ -198,12 +198,40 @@ def out_dims(x_shape, w_shape, stride, pad, dil):
             out_extent(W, S, stride[2], pad[2], dil[2]), K)
 
 
+ACTIVATIONS = ("none", "relu", "silu", "gelu")
+
+
+def activate(v: np.ndarray, act: str = "none") -> np.ndarray:
+    """The epilogue activation in fp64, each its textbook definition: relu =
+    max(v, 0); silu = v * sigmoid(v) = v / (1 + e^-v); gelu = v * Phi(v) with
+    Phi the standard normal CDF, v/2 * (1 + erf(v / sqrt 2)).  (The pages name
+    no activation; FlyDSL PR #860's fp8 conv tests stop at a bias.)"""
+    v = np.asarray(v, dtype=np.float64)
+    if act == "none":
+        return v
+    if act == "relu":
+        return np.maximum(v, 0.0)
+    if act == "silu":
+        with np.errstate(over="ignore"):
+            return v / (1.0 + np.exp(-v))
+    if act == "gelu":
+        try:
+            from scipy.special import erf
+        except ImportError:   # scipy-less hosts: the scalar library erf
+            import math
+            erf = np.vectorize(math.erf, otypes=[np.float64])
+        return 0.5 * v * (1.0 + erf(v / np.sqrt(2.0)))
+    raise ValueError(f"act must be one of {ACTIVATIONS}")
+
+
 def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1, 1, 1),
-           scale_x: float = 1.0, scale_w: float = 1.0, bias=None) -> np.ndarray:
+           scale_x: float = 1.0, scale_w: float = 1.0, bias=None,
+           act: str = "none") -> np.ndarray:
     """Full fp64 forward conv.  x [N,D,H,W,C], w [K,T,R,S,C]; both bf16 bits
     (uint16), e4m3 bytes (uint8) or float64.  Returns fp64 [N,Do,Ho,Wo,K]:
     scale_x * scale_w * (the sum), plus bias[k] (a per-filter vector, FlyDSL
-    PR #860's fp8 conv tests include a bias case) when given."""
+    PR #860's fp8 conv tests include a bias case) when given, then the
+    activation ``act``."""
     x = np.ascontiguousarray(x)
     w = np.ascontiguousarray(w)
     elem = _elem_of(x)
@@ -218,15 +246,17 @@ def conv3d(x: np.ndarray, w: np.ndarray, stride=(1, 1, 1), pad=(0, 0, 0), dil=(1
         raise ValueError("oracle_conv3d_fwd: bad shapes")
     if bias is not None:
         out += np.asarray(bias, dtype=np.float64).reshape(-1)
-    return out
+    return activate(out, act)
 
 
 def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1),
                   pad=(0, 0, 0), dil=(1, 1, 1), scale_x: float = 1.0,
-                  scale_w: float = 1.0, bias=None, x_layout: str = "ndhwc") -> np.ndarray:
+                  scale_w: float = 1.0, bias=None, x_layout: str = "ndhwc",
+                  act: str = "none") -> np.ndarray:
     """fp64 conv evaluated at flat NDHWC output indices ``idx`` (int64), plus
-    bias[k] of each index's filter k when given.  ``x_layout="ncdhw"``: x is
-    stored channel-major [N,C,D,H,W] (the output indices stay NDHWC)."""
+    bias[k] of each index's filter k when given, then the activation ``act``.
+    ``x_layout="ncdhw"``: x is stored channel-major [N,C,D,H,W] (the output
+    indices stay NDHWC)."""
     if x_layout not in ("ndhwc", "ncdhw"):
         raise ValueError("x_layout must be 'ndhwc' or 'ncdhw'")
     x = np.ascontiguousarray(x)
@@ -246,7 +276,7 @@ def conv3d_points(x: np.ndarray, w: np.ndarray, idx: np.ndarray, stride=(1, 1, 1
         raise ValueError("oracle conv3d points: bad shapes or index out of range")
     if bias is not None:
         vals += np.asarray(bias, dtype=np.float64).reshape(-1)[idx % w.shape[0]]
-    return vals
+    return activate(vals, act)
 
 
 def conv3d_bwd_data(dy: np.ndarray, w: np.ndarray, x_shape, stride=(1, 1, 1), pad=(0, 0, 0),

@@ -243,6 +243,47 @@ def test_points_on_channel_major_x_match_torch():
         assert np.array_equal(got, nd)
 
 
+def test_activations_match_torch_fp64():
+    """The epilogue activations against torch's own fp64 relu / silu / gelu
+    (erf form) on values spanning the tails, plus exact special values."""
+    rng = np.random.default_rng(77)
+    v = np.concatenate([rng.standard_normal(5000) * 4, np.linspace(-40, 40, 801),
+                        [0.0, -0.0, 1e-30, -1e-30]])
+    tv = torch.from_numpy(v)
+    ref = {"relu": F.relu(tv), "silu": F.silu(tv), "gelu": F.gelu(tv)}
+    for act, r in ref.items():
+        got = oracle.activate(v, act)
+        np.testing.assert_allclose(got, r.numpy(), rtol=1e-12, atol=1e-15, err_msg=act)
+    assert np.array_equal(oracle.activate(v, "none"), v)
+    assert oracle.activate(np.array([-2.0, 0.0, 3.0]), "relu").tolist() == [0.0, 0.0, 3.0]
+    assert oracle.activate(np.array([0.0]), "silu")[0] == 0.0
+    assert oracle.activate(np.array([0.0]), "gelu")[0] == 0.0
+    # far tails: silu and gelu approach the identity above and zero below
+    big = oracle.activate(np.array([60.0, -60.0]), "gelu")
+    assert big[0] == 60.0 and abs(big[1]) < 1e-300
+    with pytest.raises(ValueError):
+        oracle.activate(v, "tanh")
+
+
+def test_conv_with_bias_and_activation_matches_torch():
+    """conv + bias + activation against torch CPU fp64 F.conv3d (with its own
+    bias) followed by torch's activation."""
+    rng = np.random.default_rng(78)
+    x = rng.standard_normal((2, 4, 5, 6, 7))
+    w = rng.standard_normal((9, 3, 2, 3, 7)) / 8
+    b = rng.standard_normal(9)
+    xt = torch.from_numpy(x).permute(0, 4, 1, 2, 3)
+    wt = torch.from_numpy(w).permute(0, 4, 1, 2, 3)
+    y = F.conv3d(xt, wt, bias=torch.from_numpy(b), stride=(1, 2, 1), padding=(1, 1, 0))
+    for act, fn in (("relu", F.relu), ("silu", F.silu), ("gelu", F.gelu)):
+        ref = fn(y).permute(0, 2, 3, 4, 1).contiguous().numpy()
+        got = oracle.conv3d(x, w, (1, 2, 1), (1, 1, 0), (1, 1, 1), bias=b, act=act)
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12, err_msg=act)
+        idx = np.arange(ref.size, dtype=np.int64)[::7]
+        pts = oracle.conv3d_points(x, w, idx, (1, 2, 1), (1, 1, 0), (1, 1, 1), bias=b, act=act)
+        assert np.array_equal(pts, got.ravel()[idx])
+
+
 def test_points_reject_out_of_range_index():
     x = np.zeros((1, 2, 2, 2, 1))
     w = np.zeros((1, 1, 1, 1, 1))
