@@ -222,12 +222,12 @@ def prepare(pkg, wl: cw.Workload, device):
     return {"x": x, "w": w, "sx": None, "sw": None}
 
 
-def conv_step(pkg, wl, ops, out, ws, bias=None):
+def conv_step(pkg, wl, ops, out, ws, bias=None, act="none"):
     if reads_ncdhw(wl):
         return lambda: pkg.conv_fwd_ncdhw(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil,
                                           bias=bias, out=out, workspace=ws)
     return lambda: pkg.conv_fwd(ops["x"], ops["w"], wl.stride, wl.pad, wl.dil, scale_x=ops["sx"],
-                                scale_w=ops["sw"], out=out, workspace=ws, bias=bias)
+                                scale_w=ops["sw"], out=out, workspace=ws, bias=bias, act=act)
 
 
 def ndhwc_shape(wl: cw.Workload):
@@ -238,8 +238,10 @@ def ndhwc_shape(wl: cw.Workload):
     return tuple(wl.x_shape)
 
 
-def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias=False):
-    """with_bias: the same step through conv_fwd_bias (a per-filter fp32 bias)."""
+def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias=False,
+                 act="none"):
+    """with_bias: the same step through conv_fwd_bias (a per-filter fp32 bias);
+    act: then an activation (conv_fwd_bias_act)."""
     ops = prepare(pkg, wl, device)
     x, w = ops["x"], ops["w"]
     ncdhw = reads_ncdhw(wl)
@@ -255,7 +257,7 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias
     if with_bias:
         g = torch.Generator(device="cpu").manual_seed(wl.w_seed + 500)
         bias = torch.randn(w.shape[0], generator=g).float().to(device)
-    step = conv_step(pkg, wl, ops, out, ws, bias)
+    step = conv_step(pkg, wl, ops, out, ws, bias, act)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -518,11 +520,13 @@ def main_arm(args):
                              "temporal_3x1x1_bf16_ncdhw", "pointwise_1x1x1_bf16_ncdhw")
                  if n != wl.name]
         # the bias epilogue on the headline and on the epilogue-heavy patch embedding
-        names += [wl.name + "+bias", "patch_embed_bf16+bias"]
+        names += [wl.name + "+bias", "patch_embed_bf16+bias", wl.name + "+bias+gelu"]
         for name in names:
             try:
                 r = run_workload(pkg, cw.BY_NAME[name.split("+")[0]], device, args.steps,
-                                 args.warmup, flush, with_e2e=False, with_bias=name.endswith("+bias"))
+                                 args.warmup, flush, with_e2e=False,
+                                 with_bias="+bias" in name,
+                                 act="gelu" if name.endswith("+gelu") else "none")
                 m = statistics.mean(r["ms"])
                 ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m,
                        "ms_median": statistics.median(r["ms"]), "plan": r["plan"]}

@@ -35,6 +35,11 @@ CONV_DTYPE_FP8_E4M3 = 1
 
 CLASS_NAMES = {0: "generic", 1: "temporal", 2: "point_gemm", 3: "patch_gemm"}
 
+# epilogue activations (conv_fwd_bias_act)
+CONV_ACT_NONE, CONV_ACT_RELU, CONV_ACT_SILU, CONV_ACT_GELU = 0, 1, 2, 3
+ACT_CODES = {"none": CONV_ACT_NONE, "relu": CONV_ACT_RELU, "silu": CONV_ACT_SILU,
+             "gelu": CONV_ACT_GELU}
+
 _I64_5 = ctypes.c_int64 * 5
 _I32_3 = ctypes.c_int * 3
 _lock = threading.Lock()
@@ -81,6 +86,9 @@ def load_library(path: str = LIB_PATH):
         lib.conv_fwd_bias.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp, vp,
                                       vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_fwd_bias.restype = ctypes.c_int
+        lib.conv_fwd_bias_act.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, ctypes.c_int, vp,
+                                          vp, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+        lib.conv_fwd_bias_act.restype = ctypes.c_int
         lib.conv_fwd_ncdhw_plan.argtypes = lib.conv_fwd_plan.argtypes
         lib.conv_fwd_ncdhw_plan.restype = ctypes.c_int
         lib.conv_fwd_ncdhw.argtypes = lib.conv_fwd_bias.argtypes
@@ -229,12 +237,15 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
              scale_x: Optional[torch.Tensor] = None, scale_w: Optional[torch.Tensor] = None,
              out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None, split_k: bool = True,
-             bias: Optional[torch.Tensor] = None) -> torch.Tensor:
+             bias: Optional[torch.Tensor] = None, act: str = "none") -> torch.Tensor:
     """Forward conv: x NDHWC [N,D,H,W,C], w KTRSC [K,T,R,S,C] (both bf16, or
     both float8_e4m3fn with fp32 device scales) -> out NDHWC [N,Do,Ho,Wo,K]
-    bf16, plus ``bias`` (fp32 [K], through conv_fwd_bias) when given.  A
+    bf16, plus ``bias`` (fp32 [K], through conv_fwd_bias) when given, then
+    ``act`` ("relu", "silu" or "gelu", through conv_fwd_bias_act).  A
     split-K workspace is taken from torch's allocator when the plan wants one
     and none is given (``split_k=False`` runs without)."""
+    if act not in ACT_CODES:
+        raise ValueError(f"act must be one of {sorted(ACT_CODES)}")
     lib = load_library()
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x must be [N,D,H,W,C] and w [K,T,R,S,C]")
@@ -261,7 +272,13 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
             ws_ptr, ws_bytes = workspace.data_ptr(), need
-    if bias is None:
+    if act != "none":
+        rc = lib.conv_fwd_bias_act(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(),
+                                   _I64_5(*w.shape), _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype,
+                                   _ptr(scale_x), _ptr(scale_w), _ptr(bias), ACT_CODES[act],
+                                   out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
+        _check(rc, "conv_fwd_bias_act")
+    elif bias is None:
         rc = lib.conv_fwd(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
                           _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
                           _ptr(scale_w), out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))

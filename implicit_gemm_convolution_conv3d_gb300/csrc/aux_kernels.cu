@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
                                                             long long MK, int splits,
                                                             const float* scale_x,
                                                             const float* scale_w,
-                                                            const float* bias, long long K) {
+                                                            const float* bias, long long K,
+                                                            int act) {
     float scale = 1.0f;
     if (scale_x) scale *= *scale_x;
     if (scale_w) scale *= *scale_w;
@@ -44,8 +45,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 #pragma unroll
                 for (int j = 0; j < 4; ++j) b[j] = __ldg(bias + (k0 + j) % K);
             }
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * scale + b[0], acc.y * scale + b[1]);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * scale + b[2], acc.w * scale + b[3]);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(activate(acc.x * scale + b[0], act),
+                                                      activate(acc.y * scale + b[1], act));
+            __nv_bfloat162 hi = __floats2bfloat162_rn(activate(acc.z * scale + b[2], act),
+                                                      activate(acc.w * scale + b[3], act));
             uint2 o;
             o.x = *reinterpret_cast<uint32_t*>(&lo);
             o.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -55,7 +58,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
         for (long long i = tid; i < MK; i += stride) {
             float acc = ws[i];
             for (int s = 1; s < splits; ++s) acc += ws[s * MK + i];
-            out[i] = __float2bfloat16_rn(acc * scale + (bias ? __ldg(bias + i % K) : 0.f));
+            out[i] = __float2bfloat16_rn(
+                activate(acc * scale + (bias ? __ldg(bias + i % K) : 0.f), act));
         }
     }
 }
@@ -582,14 +586,14 @@ cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, con
 
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
                                  const float* scale_x, const float* scale_w, const float* bias,
-                                 long long K, int num_sms, cudaStream_t stream) {
+                                 long long K, int act, int num_sms, cudaStream_t stream) {
     const long long units = (MK & 3) == 0 ? (MK >> 2) : MK;
     long long blocks = (units + 255) / 256;
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        ws, reinterpret_cast<__nv_bfloat16*>(out), MK, splits, scale_x, scale_w, bias, K);
+        ws, reinterpret_cast<__nv_bfloat16*>(out), MK, splits, scale_x, scale_w, bias, K, act);
     return cudaGetLastError();
 }
 

@@ -879,7 +879,7 @@ int gemm_mn_a(const void* a, long long M, long long Kr, const void* b, long long
     cudaError_t e = launch_igemm(P.amode, 0, &tm, k, P.grid, P.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
-        e = launch_splitk_reduce(k.ws, out, M * Nn, P.splits, nullptr, nullptr, nullptr, Nn,
+        e = launch_splitk_reduce(k.ws, out, M * Nn, P.splits, nullptr, nullptr, nullptr, Nn, 0,
                                  dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }
@@ -1160,7 +1160,7 @@ int plan_query(const Geo& g, bool ncdhw, int dtype, int num_sms, int* cls, int* 
 }
 
 int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
-             const float* scale_x, const float* scale_w, const float* bias, void* out,
+             const float* scale_x, const float* scale_w, const float* bias, int act, void* out,
              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace
@@ -1210,7 +1210,19 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
     Geo g;
     int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
     if (rc) return rc;
-    return fwd_impl(g, false, x, w, dtype, scale_x, scale_w, bias, out, workspace,
+    return fwd_impl(g, false, x, w, dtype, scale_x, scale_w, bias, kActNone, out, workspace,
+                    workspace_bytes, stream);
+}
+
+int conv_fwd_bias_act(const void* x, const int64_t x_dims[5], const void* w,
+                      const int64_t w_dims[5], const int stride[3], const int pad[3],
+                      const int dil[3], int dtype, const float* scale_x, const float* scale_w,
+                      const float* bias, int act, void* out, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    return fwd_impl(g, false, x, w, dtype, scale_x, scale_w, bias, act, out, workspace,
                     workspace_bytes, stream);
 }
 
@@ -1227,7 +1239,7 @@ int conv_fwd_ncdhw(const void* x, const int64_t x_dims[5], const void* w, const 
     Geo g;
     int rc = make_geo(xd, w_dims, stride, pad, dil, &g);
     if (rc) return rc;
-    return fwd_impl(g, true, x, w, dtype, scale_x, scale_w, bias, out, workspace,
+    return fwd_impl(g, true, x, w, dtype, scale_x, scale_w, bias, kActNone, out, workspace,
                     workspace_bytes, stream);
 }
 
@@ -1260,8 +1272,8 @@ cudaError_t launch_units(const Plan& P, const TMaps& tm, const KParams& k, cudaS
 // ms against 6.4 ms on the 3x1x1 workload: under the power cap the pack's
 // draw slows the tensor-bound conv by more than the overlap saves.)
 int ncdhw_via_copy(const Geo& g, const Plan& P, DeviceInfo* dev, const void* x, const void* w,
-                   const float* scale_x, const float* scale_w, const float* bias, void* out,
-                   void* workspace, cudaStream_t stream) {
+                   const float* scale_x, const float* scale_w, const float* bias, int act,
+                   void* out, void* workspace, cudaStream_t stream) {
     int rc;
     void* xc = workspace;
     TMaps tm;
@@ -1269,22 +1281,27 @@ int ncdhw_via_copy(const Geo& g, const Plan& P, DeviceInfo* dev, const void* x, 
     if ((rc = build_out_map(g, P, out, &tm))) return rc;
     KParams k;
     fill_params(g, P, xc, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
+    k.act = act;
     cudaError_t e = launch_pack(x, g.N, g.C, g.D * g.H * g.W, xc, 0, nullptr, nullptr,
                                 dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     if ((e = launch_units(P, tm, k, stream)) != cudaSuccess)
         return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1 &&
-        (e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K,
+        (e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K, k.act,
                                   dev->num_sms, stream)) != cudaSuccess)
         return cuda_fail(e, "split-K reduce launch");
     return CONV_OK;
 }
 
 int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
-             const float* scale_x, const float* scale_w, const float* bias, void* out,
+             const float* scale_x, const float* scale_w, const float* bias, int act, void* out,
              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     int rc = CONV_OK;
+    if (act < kActNone || act > kActGelu) {
+        set_error("unknown activation");
+        return CONV_ERR_INVALID;
+    }
     if (!x || !w || !out) {
         set_error("null tensor pointer");
         return CONV_ERR_INVALID;
@@ -1307,7 +1324,8 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
                         &P, ncdhw)))
         return rc;
     if (P.ncdhw_pack)
-        return ncdhw_via_copy(g, P, dev, x, w, scale_x, scale_w, bias, out, workspace, stream);
+        return ncdhw_via_copy(g, P, dev, x, w, scale_x, scale_w, bias, act, out, workspace,
+                              stream);
     const void* xa = x;
     const void* wa = w;
     if (P.repack == 2) {
@@ -1354,6 +1372,7 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
 
     KParams k;
     fill_params(g, P, x, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
+    k.act = act;
 
     if (std::getenv("CONV3D_LOG")) {
         std::fprintf(stderr,
@@ -1367,7 +1386,7 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
     cudaError_t e = launch_units(P, tm, k, stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (P.splits > 1) {
-        e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K,
+        e = launch_splitk_reduce(k.ws, out, P.M * g.K, P.splits, scale_x, scale_w, bias, g.K, k.act,
                                  dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }

@@ -19,6 +19,49 @@ enum AMode : int {
 
 constexpr int kBM = 128;               // rows of a tile (tcgen05 M, one CTA)
 constexpr int kEpiWarps = 4;           // warps reading TMEM in the epilogue
+// epilogue activations (values of conv_fwd_bias_act's `act`)
+constexpr int kActNone = 0, kActRelu = 1, kActSilu = 2, kActGelu = 3;
+
+// 1/x by the approximate reciprocal instruction (about 1 ulp; 1/inf = 0):
+// the epilogue's activations feed bf16 outputs, far coarser than that.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: 1 - (a1 t + ... + a5 t^5) e^(-x^2), t = 1 / (1 + p x) for x >= 0,
+// odd in x; |error| <= 1.5e-7, far below the bf16 output's resolution, at a
+// fraction of the cost of a full-precision erf in an epilogue that has one
+// evaluation per output element.
+__device__ __forceinline__ float erf_as7126(float x) {
+    const float a = fabsf(x);
+    const float t = rcp_approx(fmaf(0.3275911f, a, 1.0f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
+                         -0.284496736f),
+                 0.254829592f);
+    return copysignf(1.0f - poly * __expf(-a * a), x);
+}
+
+// The activation on an fp32 epilogue value: max(v, 0); v * sigmoid(v);
+// v * Phi(v) = v/2 * (1 + erf(v / sqrt(2))), the erf form of GELU.
+template <int ACT>
+__device__ __forceinline__ float activate_c(float v) {
+    if constexpr (ACT == kActRelu) return fmaxf(v, 0.0f);
+    else if constexpr (ACT == kActSilu) return v * rcp_approx(1.0f + __expf(-v));
+    else if constexpr (ACT == kActGelu)
+        return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752f));
+    else return v;
+}
+
+__device__ __forceinline__ float activate(float v, int act) {
+    if (act == kActRelu) return activate_c<kActRelu>(v);
+    if (act == kActSilu) return activate_c<kActSilu>(v);
+    if (act == kActGelu) return activate_c<kActGelu>(v);
+    return v;
+}
 constexpr int kGatherThreads = 128;    // producer threads of AM_GEMM_GATHER
 constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;              // one warp's 32x32 bf16 chunk
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 2 * kEpiChunkBytes;   // double-buffered
@@ -62,6 +105,7 @@ struct KParams {
                         //    GEMM mode [K rows, M], or temporal mode over channel-major x
     int msub;           // row sub-tiles per unit sharing each B stage (1 or 2)
     int n_tile0;        // first column tile of this launch (n_tiles column tiles from it)
+    int act;            // activation after scale and bias: kActNone / Relu / Silu / Gelu
     // AM_GEMM_GATHER operands: A [M, g_cols], B [K, g_cols] row-major
     const unsigned char* ga;
     const unsigned char* gb;
@@ -86,11 +130,11 @@ struct TMaps {
 cudaError_t launch_igemm(int amode, int fp8, const TMaps* maps, const KParams& p, int grid,
                          size_t smem, cudaStream_t stream);
 
-// Deterministic split-K reduction: out = bf16(scale * sum_s ws[s] + bias[k]) in
-// split order (bias may be NULL; k = column of the [M, K] output).
+// Deterministic split-K reduction: out = bf16(act(scale * sum_s ws[s] + bias[k]))
+// in split order (bias may be NULL; k = column of the [M, K] output).
 cudaError_t launch_splitk_reduce(const float* ws, void* out, long long MK, int splits,
                                  const float* scale_x, const float* scale_w, const float* bias,
-                                 long long K, int num_sms, cudaStream_t stream);
+                                 long long K, int act, int num_sms, cudaStream_t stream);
 
 // Row repack of two matrices with equal row pitches: copy rows of
 // src_row_bytes into rows of dst_row_bytes, matrix 1's rows shifted right by

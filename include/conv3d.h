@@ -137,6 +137,30 @@ int conv_fwd_bias(const void* x, const int64_t x_dims[5], const void* w, const i
                   const float* scale_x, const float* scale_w, const float* bias, void* out,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Epilogue activations of conv_fwd_bias_act. */
+typedef enum {
+    CONV_ACT_NONE = 0,
+    CONV_ACT_RELU = 1,   /* max(v, 0) */
+    CONV_ACT_SILU = 2,   /* v * sigmoid(v) = v / (1 + exp(-v)) */
+    CONV_ACT_GELU = 3    /* v * Phi(v) = v/2 * (1 + erf(v / sqrt(2))), the erf form */
+} conv_act;
+
+/* conv_fwd_bias followed by an elementwise activation, applied in fp32 to
+ * each output before the bf16 rounding:
+ *   out[n,od,oh,ow,k] = bf16_rn( act( scale_x * scale_w * (the conv_fwd sum) + bias[k] ) )
+ *   act    one of conv_act; anything else returns CONV_ERR_INVALID
+ * bias may be NULL.  Every other argument, the plan and the error behaviour
+ * are conv_fwd_bias's (with split-K the activation is applied once, in the
+ * reduction, after the bias).  Defined by: FlyDSL PR #860, PR summary, which
+ * lists a bias case among the fp8 conv's tests; the pages name no activation
+ * function, so the usual epilogue extension of that bias is offered in three
+ * common forms, each as its textbook definition. */
+int conv_fwd_bias_act(const void* x, const int64_t x_dims[5], const void* w,
+                      const int64_t w_dims[5], const int stride[3], const int pad[3],
+                      const int dil[3], int dtype, const float* scale_x, const float* scale_w,
+                      const float* bias, int act, void* out, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
 /* conv_fwd_bias over a channel-major (NCDHW) activation, read in place: no
  * NCDHW -> NDHWC pass before the convolution.
  *   out[n,od,h,w,k] = bf16_rn( scale_x * scale_w *

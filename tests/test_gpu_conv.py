@@ -395,6 +395,45 @@ def test_bias(pkg, case, split_k):
     assert_close(as_f64(y), ref, f"bias {case} split={split_k}")
 
 
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu"])
+@pytest.mark.parametrize("case", BIAS_CASES, ids=[str(i) for i in range(len(BIAS_CASES))])
+@pytest.mark.parametrize("split_k", [True, False])
+def test_bias_activation(pkg, case, split_k, act):
+    """bias + activation epilogue (conv_fwd_bias_act) in every store path:
+    TMA tensor stores, staged 8-/4-byte stores, direct stores, the split-K
+    reduction; against the fp64 oracle's textbook activation."""
+    xs, ws, st, pa, di = case
+    x, w = _inputs(xs, ws, 180 + BIAS_CASES.index(case))
+    g = torch.Generator(device="cpu").manual_seed(190 + BIAS_CASES.index(case))
+    b = (torch.randn(ws[0], generator=g) * 0.5).float()
+    y = pkg.conv_fwd(x, w, st, pa, di, split_k=split_k, bias=b.cuda(), act=act)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    st3, pa3, di3 = pkg._triple(st), pkg._triple(pa), pkg._triple(di)
+    ref = oracle.conv3d(bits16(x), bits16(w), st3, pa3, di3, bias=b.double().numpy(), act=act)
+    assert_close(as_f64(y), ref, f"bias+{act} {case} split={split_k}")
+
+
+def test_activation_without_bias_and_bad_code(pkg):
+    xs, ws = (2, 5, 9, 11, 64), (272, 3, 3, 3, 64)
+    x, w = _inputs(xs, ws, 185)
+    y = pkg.conv_fwd(x, w, 1, 1, 1, act="gelu")
+    torch.cuda.synchronize()
+    ref = oracle.conv3d(bits16(x), bits16(w), (1, 1, 1), (1, 1, 1), (1, 1, 1), act="gelu")
+    assert_close(as_f64(y), ref, "gelu without bias")
+    # relu of an all-negative output is exactly zero
+    yn = pkg.conv_fwd(x, w, 1, 1, 1, act="relu",
+                      bias=torch.full((272,), -1e4, dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(yn.float()) == 0
+    lib = pkg.load_library()
+    out = torch.empty_like(y)
+    rc = lib.conv_fwd_bias_act(x.data_ptr(), pkg._I64_5(*xs), w.data_ptr(), pkg._I64_5(*ws),
+                               pkg._I32_3(1, 1, 1), pkg._I32_3(1, 1, 1), pkg._I32_3(1, 1, 1), 0,
+                               None, None, None, 7, out.data_ptr(), None, 0, None)
+    assert rc == pkg.CONV_ERR_INVALID
+
+
 def test_bias_zero_weights_is_exact(pkg):
     """Zero weights: every output is bf16_rn(bias[k]) exactly."""
     x = cw.randn_bf16((1, 4, 6, 6, 32), 195, 1.0, "cuda")

@@ -188,6 +188,24 @@ def test_fp8_conv_with_bias(pkg):
         assert_close(as_f64(y), ref, f"fp8 bias split={split_k}")
 
 
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu"])
+def test_fp8_conv_with_bias_and_activation(pkg, act):
+    """The fp8 conv with both scales, a bias and an activation."""
+    xs, ws = (1, 64, 4, 9, 11), (96, 64, 1, 3, 3)
+    x = cw.randn_bf16(xs, 431, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 531, 1.0 / np.sqrt(576), "cuda")
+    qx, sx, qw, sw = _fp8_operands(pkg, x, w)
+    b = torch.linspace(-1.0, 2.0, 96, dtype=torch.float32, device="cuda")
+    for split_k in (True, False):
+        y = pkg.conv_fwd(qx, qw, 1, (0, 1, 1), 1, scale_x=sx, scale_w=sw, split_k=split_k, bias=b,
+                         act=act)
+        torch.cuda.synchronize()
+        assert pkg.conv_get_device_status() == 0
+        ref = oracle.conv3d(bytes8(qx), bytes8(qw), (1, 1, 1), (0, 1, 1), (1, 1, 1), sx.item(),
+                            sw.item(), bias=b.double().cpu().numpy(), act=act)
+        assert_close(as_f64(y), ref, f"fp8 bias+{act} split={split_k}")
+
+
 @pytest.mark.parametrize("shapes", [((2, 3, 1, 32, 48), (64, 3, 1, 16, 16), (1, 16, 16)),
                                     ((3, 3, 1, 28, 35), (40, 3, 1, 7, 7), (1, 7, 7))])
 def test_fp8_patch_gemm(pkg, shapes):
