@@ -284,8 +284,9 @@ constexpr long long kInPlaceChannelBytes = 1ll << 20;
 // ncdhw: x is channel-major [N, C, D, H, W] (g keeps the NDHWC names); only
 // the temporal class reads it, as MN-major A boxes of H*W positions, or from
 // an NDHWC copy packed into the workspace (ncdhw_pack).
+// act: the epilogue activation (plans with one store through the direct path).
 int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_avail, Plan* P,
-              bool ncdhw = false) {
+              bool ncdhw = false, int act = kActNone) {
     if (dtype != CONV_DTYPE_BF16 && dtype != CONV_DTYPE_FP8_E4M3) {
         set_error("unknown dtype");
         return CONV_ERR_INVALID;
@@ -555,9 +556,12 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     // bf16 rows of an even K whose pitch is not a multiple of 16 bytes are
     // staged the same way and leave in 8- or 4-byte pieces, several rows per
     // instruction, instead of 2-byte stores from each lane's own row
-    P->epi_mode = splits > 1 ? 0 : (g.K % 8 == 0 ? 1 : (g.K % 2 == 0 ? 2 : 0));
+    // An activation is applied on the direct-store path only, which keeps one
+    // compiled copy of its code out of the staged epilogues (their code size
+    // is what the short point-output kernels are sensitive to).
+    P->epi_mode = splits > 1 || act != kActNone ? 0 : (g.K % 8 == 0 ? 1 : (g.K % 2 == 0 ? 2 : 0));
     // CONV3D_EPI=tma / staged / direct overrides the epilogue kind (for sweeps)
-    if (const char* e = std::getenv("CONV3D_EPI")) {
+    if (const char* e = act != kActNone ? nullptr : std::getenv("CONV3D_EPI")) {
         if (e[0] == 't' && splits == 1 && g.K % 8 == 0) P->epi_mode = 1;
         if (e[0] == 's' && splits == 1 && g.K % 2 == 0) P->epi_mode = 2;
         if (e[0] == 'd') P->epi_mode = 0;
@@ -1321,7 +1325,7 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
     }
     Plan P;
     if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace ? workspace_bytes : 0,
-                        &P, ncdhw)))
+                        &P, ncdhw, act)))
         return rc;
     if (P.ncdhw_pack)
         return ncdhw_via_copy(g, P, dev, x, w, scale_x, scale_w, bias, act, out, workspace,

@@ -140,13 +140,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Store 32 accumulator columns of one output row (bf16): act(v * scale + bias)
+// Store 32 accumulator columns of one output row (bf16): v * scale + bias
 // (bias: the 32 columns' entries, or NULL).
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
-                                               float scale, const float* bias, int act,
-                                               int count, bool vec_ok) {
+                                               float scale, const float* bias, int count,
+                                               bool vec_ok) {
     auto val = [&](int i) {
-        return activate(__uint_as_float(v[i]) * scale + (bias ? __ldg(bias + i) : 0.0f), act);
+        return __uint_as_float(v[i]) * scale + (bias ? __ldg(bias + i) : 0.0f);
     };
     if (count == 32 && vec_ok) {
         uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -163,6 +163,41 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             if (i < count) dst[i] = __float2bfloat16_rn(val(i));
+    }
+}
+
+// The same with an activation after the bias: act(v * scale + bias).  Plans
+// with an activation store through this path only; it is kept out of line so
+// that its code (one loop per activation) stays out of the kernel's body.
+__device__ __noinline__ void store_row_bf16_act(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                                float scale, const float* bias, int act,
+                                                int count, bool vec_ok) {
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        y[i] = __uint_as_float(v[i]) * scale + (bias && i < count ? __ldg(bias + i) : 0.0f);
+    if (act == kActRelu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = activate_c<kActRelu>(y[i]);
+    } else if (act == kActSilu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = activate_c<kActSilu>(y[i]);
+    } else if (act == kActGelu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = activate_c<kActGelu>(y[i]);
+    }
+    if (count == 32 && vec_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(y[8 * i + 0], y[8 * i + 1]),
+                               pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
+                               pack_bf16x2(y[8 * i + 4], y[8 * i + 5]),
+                               pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < count) dst[i] = __float2bfloat16_rn(y[i]);
     }
 }
 
@@ -722,16 +757,13 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     // staged in shared memory (64-byte swizzle, two buffers)
                     if (!any) continue;
                     // one 32-column chunk: stage in the next buffer, store by TMA
-                    // (with_bias: column i's bias is lane i's entry bj; act_tag:
-                    // the activation, a compile-time kAct* value)
-                    auto store_chunk = [&](const uint32_t (&v)[32], int j, float bj, auto with_bias,
-                                           auto act_tag) {
+                    // (with_bias: column i's bias is lane i's entry bj)
+                    auto store_chunk = [&](const uint32_t (&v)[32], int j, float bj, auto with_bias) {
                         constexpr bool kBias = decltype(with_bias)::value;
-                        constexpr int kActC = decltype(act_tag)::value;
                         const int n0 = t.n_tile * p.BN + 32 * j;
                         auto val = [&](int i) {
                             const float b = kBias ? __shfl_sync(0xffffffffu, bj, i) : 0.0f;
-                            return activate_c<kActC>(__uint_as_float(v[i]) * scale + b);
+                            return __uint_as_float(v[i]) * scale + b;
                         };
                         const uint32_t buf = bufs + static_cast<uint32_t>(epi_iter & 1) * kEpiChunkBytes;
                         ++epi_iter;
@@ -800,38 +832,11 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     // j + 1 is in flight while chunk j is converted and stored
                     const int nch = min(p.BN / 32, (p.K - t.n_tile * p.BN + 31) / 32);
                     uint32_t va[32], vb[32];
-                    using T_ = std::integral_constant<bool, true>;
-                    using F_ = std::integral_constant<bool, false>;
-                    using A0_ = std::integral_constant<int, kActNone>;
-                    if (p.act != kActNone) {
-                        // one compiled loop per activation, chunk by chunk (no
-                        // TMEM double buffer: the activation code stays one copy)
-                        auto act_chunks = [&](auto act_tag) {
-#pragma unroll 1
-                            for (int j = 0; j < nch; ++j) {
-                                tmem_ld_32x32b_x32(tb + 32 * j, va);
-                                tmem_ld_wait();
-                                const int col = t.n_tile * p.BN + 32 * j + lane;
-                                const float bj = p.bias && col < p.K ? __ldg(p.bias + col) : 0.0f;
-                                if (p.bias)
-                                    store_chunk(va, j, bj, T_(), act_tag);
-                                else
-                                    store_chunk(va, j, bj, F_(), act_tag);
-                            }
-                        };
-                        if (p.act == kActRelu)
-                            act_chunks(std::integral_constant<int, kActRelu>());
-                        else if (p.act == kActSilu)
-                            act_chunks(std::integral_constant<int, kActSilu>());
-                        else
-                            act_chunks(std::integral_constant<int, kActGelu>());
-                        continue;
-                    }
                     auto chunk = [&](const uint32_t (&v)[32], int j, float bj) {
                         if (p.bias)
-                            store_chunk(v, j, bj, T_(), A0_());
+                            store_chunk(v, j, bj, std::integral_constant<bool, true>());
                         else
-                            store_chunk(v, j, bj, F_(), A0_());
+                            store_chunk(v, j, bj, std::integral_constant<bool, false>());
                     };
                     tmem_ld_32x32b_x32(tb, va);
 #pragma unroll
@@ -855,8 +860,13 @@ __global__ void __launch_bounds__(AMODE == AM_GEMM_GATHER ? 320 : 192, 1)
                     if (valid && n0 < p.K) {
                         const int cnt = min(32, p.K - n0);
                         if (p.splits == 1) {
-                            store_row_bf16(out + m * p.K + n0, v, scale,
-                                           p.bias ? p.bias + n0 : nullptr, p.act, cnt, vec_out);
+                            if (p.act == kActNone)
+                                store_row_bf16(out + m * p.K + n0, v, scale,
+                                               p.bias ? p.bias + n0 : nullptr, cnt, vec_out);
+                            else
+                                store_row_bf16_act(out + m * p.K + n0, v, scale,
+                                                   p.bias ? p.bias + n0 : nullptr, p.act, cnt,
+                                                   vec_out);
                         } else {
                             float* dst = p.ws + (static_cast<long long>(t.split) * p.M + m) * p.K + n0;
                             store_row_f32(dst, v, cnt, vec_ws);
