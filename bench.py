@@ -354,19 +354,23 @@ def run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush):
 
 
 def link_bandwidth(h_in, d_in, h_out, d_out):
-    """Host<->device copy bandwidth of this machine (GB/s), one plain copy
-    each way between the e2e leg's own pinned buffers, alone on the stream:
-    the bound the end-to-end number cannot beat."""
+    """Host<->device copy bandwidth of this machine (GB/s): the best of three
+    plain copies each way between the e2e leg's own pinned buffers, alone on
+    the stream -- the bound the end-to-end number cannot beat."""
     res = {}
     for name, dst, src in (("h2d_gbs", d_in, h_in), ("d2h_gbs", h_out, d_out)):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         dst.copy_(src, non_blocking=True)
-        a.record()
-        dst.copy_(src, non_blocking=True)
-        b.record()
-        torch.cuda.synchronize()
-        res[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+        best = 0.0
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            best = max(best, src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9)
+        res[name] = best
     return res
 
 
