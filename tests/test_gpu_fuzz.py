@@ -2,9 +2,9 @@
 
 Each case draws a random problem of one dispatch class (im2col implicit GEMM,
 temporal T x 1 x 1, point-output GEMM, pointwise GEMM, non-overlapping
-patches) in bf16 or fp8-e4m3, and a random plan (tile width, k-step bytes,
-pipeline depth, raster group, split-K, CTA pair, row sub-tiles, launch
-slices) forced through the plan overrides.  A plan
+patches) in bf16 or fp8-e4m3, an optional bias and activation, and a random
+plan (tile width, k-step bytes, pipeline depth, raster group, split-K, CTA
+pair, row sub-tiles, launch slices) forced through the plan overrides.  A plan
 the library rejects for the shape falls back to the default plan, so every
 drawn problem runs.  Every output element is compared with the fp64 oracle
 on the exact bytes the GPU consumed."""
@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import conv_workloads as cw
+import oracle
 from _gpu_util import as_f64, assert_close, oracle_conv
 
 pytestmark = pytest.mark.gpu
@@ -117,6 +118,15 @@ def _case(i):
             return prob, _draw_plan(rng)
 
 
+def _epilogue(i, K):
+    """Cases 0-95 draw nothing here (their draws stay as they were); an
+    independent generator picks a bias (fp32 [K]) and an activation."""
+    rng = np.random.default_rng(17000 + i)
+    bias = rng.standard_normal(K).astype(np.float32) * 0.5 if rng.random() < 0.35 else None
+    act = str(rng.choice(["none", "none", "none", "relu", "silu", "gelu"]))
+    return bias, act
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_problem_random_plan(pkg, i):
     (fp8, kind, xs, ws, st, pa, di), plan = _case(i)
@@ -144,12 +154,17 @@ def test_random_problem_random_plan(pkg, i):
             p = pkg.conv_fwd_plan(xs, ws, st, pa, di, dtype)
         except pkg.ConvError:
             env, p = {}, None
+    bias, act = _epilogue(i, ws[0])
+    bias_t = torch.from_numpy(bias).cuda() if bias is not None else None
     with _env(env):
         if p is None:
             p = pkg.conv_fwd_plan(xs, ws, st, pa, di, dtype)
-        y = pkg.conv_fwd(x, w, st, pa, di, scale_x=sx, scale_w=sw)
+        y = pkg.conv_fwd(x, w, st, pa, di, scale_x=sx, scale_w=sw, bias=bias_t, act=act)
         torch.cuda.synchronize()
     assert pkg.conv_get_device_status() == 0
     ref = oracle_conv(x, w, st, pa, di, sxv, swv)
+    if bias is not None:
+        ref = ref + bias.astype(np.float64)
+    ref = oracle.activate(ref, act)
     assert_close(as_f64(y), ref, f"case {i}: {kind} fp8={fp8} x{xs} w{ws} s{st} p{pa} d{di} "
-                                 f"env={env} plan={p}")
+                                 f"env={env} plan={p} bias={bias is not None} act={act}")
