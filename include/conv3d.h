@@ -149,7 +149,10 @@ typedef enum {
  * each output before the bf16 rounding:
  *   out[n,od,oh,ow,k] = bf16_rn( act( scale_x * scale_w * (the conv_fwd sum) + bias[k] ) )
  *   act    one of conv_act; anything else returns CONV_ERR_INVALID
- * bias may be NULL.  Every other argument, the plan and the error behaviour
+ * GELU's erf is evaluated by Abramowitz & Stegun 7.1.26 (|error| <= 1.5e-7)
+ * and the sigmoid with an approximate reciprocal, both far below the bf16
+ * output's resolution.  Plans with an activation store through the direct
+ * (non-staged) epilogue.  bias may be NULL.  Every other argument, the plan and the error behaviour
  * are conv_fwd_bias's (with split-K the activation is applied once, in the
  * reduction, after the bias).  Defined by: FlyDSL PR #860, PR summary, which
  * lists a bias case among the fp8 conv's tests; the pages name no activation
