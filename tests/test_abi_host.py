@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from implicit_gemm_convolution_conv3d_gb300 import build as pkg_build
@@ -157,6 +158,18 @@ def test_invalid_and_unsupported_arguments(pkg):
         pkg.conv_fwd_plan((1, 4, 8, 8, 16), (32, 3, 3, 3, 16), 1, 1, 1, 7, 148)
     assert e.value.status == pkg.CONV_ERR_INVALID
     rc = lib.pack_ncdhw_bf16_to_ndhwc(None, I5(1, 2, 3, 4, 5), None, None)
+    assert rc == pkg.CONV_ERR_INVALID
+    # an unknown activation code, and null tensors with a valid one: both
+    # rejected before any device work
+    for act in (-1, 4, 99, 1):
+        rc = lib.conv_fwd_bias_act(None, args[0], None, args[2], args[3], args[4], args[5], 0,
+                                   None, None, None, act, None, None, ctypes.c_size_t(0), None)
+        assert rc == pkg.CONV_ERR_INVALID, act
+    with pytest.raises(ValueError):
+        pkg.conv_fwd(torch.zeros(1), torch.zeros(1), act="tanh")
+    rc = lib.conv_fwd_ncdhw(None, I5(1, 16, 4, 8, 8), None, I5(32, 3, 1, 1, 16), args[3],
+                            I3(1, 0, 0), args[5], 0, None, None, None, None, None,
+                            ctypes.c_size_t(0), None)
     assert rc == pkg.CONV_ERR_INVALID
     lib.conv_status_string.restype = ctypes.c_char_p
     for s in range(5):
