@@ -220,7 +220,10 @@ int conv_fwd_ncdhw_plan(const int64_t x_dims[5], const int64_t w_dims[5], const 
  * i's input planes ((n, d) planes of x, a growing prefix) are copied on a
  * library-owned copy-in stream, the kernel for slice i's output rows runs on
  * `stream` once they have landed, and slice i's output rows go back on a
- * copy-out stream while slice i+1 computes.  The weights are copied first.
+ * copy-out stream while slice i+1 computes.  The weights are copied first:
+ * when the first slice spans several waves over all column tiles, only the
+ * rows of its first group of column tiles come before its input planes, and
+ * that slice runs as one launch per group, each after its rows have landed.
  * Work queued on `stream` before the call runs before the copies; work
  * queued after it runs after the last copy: synchronise `stream` before
  * reading out_host.  Point-output GEMM and split-K plans run unsliced (copy
