@@ -399,7 +399,7 @@ def cpu_oracle_rate(wl: cw.Workload, x_host, w_host, target_s: float = 10.0):
     t0 = time.perf_counter()
     oracle.conv3d_points(x_host, w_host, idx, wl.stride, wl.pad, wl.dil, x_layout=lay)
     dt = time.perf_counter() - t0
-    return {"value": 2.0 * n * R / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+    return {"value": r4(2.0 * n * R / dt / 1e12), "unit": "TFLOPS", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{n} output elements of {wl.name} (each a {R}-term fp64 dot product), "
                       f"{dt:.1f} s"}
@@ -429,22 +429,28 @@ def reference_arm(args):
         max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_oracle_rate(wl, xb, wb, target_s=min(per_step_s, 5.0))
-    vals = []
+    vals, secs = [], []
     last = None
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         last = cpu_oracle_rate(wl, xb, wb, target_s=per_step_s)
+        secs.append(time.perf_counter() - t0)
         vals.append(last["value"])
     value = statistics.median(vals)
     flop = flops(wl)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+    # a step is one bounded sample of the workload's output elements:
+    # ms_per_step is the measured wall time of such a step; the time the
+    # oracle would take for the whole workload is extrapolated from the rate
+    line = {"impl": "reference", "metric": METRIC, "value": r4(value), "unit": "TFLOPS",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": flop / (value * 1e12) * 1e3, "higher_is_better": True,
+            "ms_per_step": r4(statistics.mean(secs) * 1e3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl),
-            "cpu_baseline": dict(last, value=value),
-            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+            "ms_full_workload_extrapolated": r4(flop / (value * 1e12) * 1e3),
+            "cpu_baseline": dict(last, value=r4(value)),
+            "e2e": {"value": r4(value), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-    print(json.dumps(line))
+    print(json.dumps(line, separators=(",", ":")))
 
 
 def workload_config(wl):
@@ -531,22 +537,7 @@ def main_arm(args):
                                  args.warmup, flush, with_e2e=False,
                                  with_bias="+bias" in name,
                                  act="gelu" if name.endswith("+gelu") else "none")
-                m = statistics.mean(r["ms"])
-                ent = {"tflops": r["flop"] / (m * 1e-3) / 1e12, "ms": m,
-                       "ms_median": statistics.median(r["ms"]), "plan": r["plan"]}
-                if "ms_with_pack" in r:
-                    mp = statistics.mean(r["ms_with_pack"])
-                    ent["tflops_with_pack"] = r["flop"] / (mp * 1e-3) / 1e12
-                    ent["ms_with_pack"] = mp
-                    pk = statistics.mean(r["ms_pack"])
-                    ent["pack_ms"] = pk
-                    ent["pack_gbs"] = r["pack_bytes"] / (pk * 1e-3) / 1e9
-                if "ms_pack_then_conv" in r:
-                    ent["ms_pack_then_conv"] = statistics.mean(r["ms_pack_then_conv"])
-                    ent["io_gbs"] = r["io_bytes"] / (m * 1e-3) / 1e9
-                    if name in PAGE_NCDHW_MS:
-                        ent["page_mi355x_ms"] = PAGE_NCDHW_MS[name]
-                secondary[name] = ent
+                secondary[name] = r
             except Exception as e:  # a secondary workload never hides the headline line
                 secondary[name] = {"error": f"{type(e).__name__}: {e}"}
             torch.cuda.empty_cache()
@@ -555,11 +546,7 @@ def main_arm(args):
             pe = cw.BY_NAME["patch_embed_bf16"]
             rb = run_backward(pkg, pe, device, args.steps, args.warmup, flush)
             for name, t in rb.items():
-                m = statistics.mean(t)
-                secondary["patch_embed_bf16_" + name] = {
-                    "tflops": flops(pe) / (m * 1e-3) / 1e12, "ms": m,
-                    "ms_median": statistics.median(t),
-                    "page_mi355x_ms": PAGE_BACKWARD_MS[name]}
+                secondary["patch_embed_bf16_" + name] = {"ms": t, "flop": flops(pe)}
         except Exception as e:
             secondary["patch_embed_bf16_backward"] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
@@ -569,8 +556,8 @@ def main_arm(args):
     peak = peaks["bf16_tflops"] if wl.dtype == "bf16" else 2.0 * peaks["bf16_tflops"]
     achieved = res["flop"] / (ms * 1e-3) / 1e12
     traffic = measured_traffic(wl.name)
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": traffic,
+    roof = {"bound": "tensor", "achieved": r4(achieved), "peak": peak, "unit": "TFLOP/s",
+            "frac": r4(achieved / peak), "traffic": traffic,
             "per": f"one conv_fwd step ({res['launches_per_step']} kernel launches)",
             "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
             "kernel": "conv_igemm_kernel (tcgen05, TMA im2col)"}
@@ -579,22 +566,74 @@ def main_arm(args):
         xb, wb = host_inputs(wl)
         cpu = cpu_oracle_rate(wl, xb, wb)
     base = PAGE_BASELINE_TFLOPS.get(wl.name)
-    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+    line = {"metric": METRIC, "value": r4(value), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r4(ms_max),
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": (value / base) if base else None,
+            "vs_baseline": r4(value / base) if base else None,
             "dtype": wl.dtype, "data": "synthetic",
-            "config": dict(workload_config(wl), parallelism=f"replicas{world}",
-                           plan=res["plan"],
-                           baseline_note="vs_baseline divides by the MI355X figure for this shape "
-                                         "(967 TFLOPS, FlyDSL PR #860): context only"),
-            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": res["e2e"]["h2d"],
-                    "d2h_bytes_per_step": res["e2e"]["d2h"], "ms_per_step": e2e_ms,
-                    "link_gbs_measured": res["e2e"]["link"]},
+            "config": workload_config(wl),
+            "e2e": {"value": r4(e2e_value), "unit": "TFLOPS",
+                    "h2d_bytes_per_step": res["e2e"]["h2d"],
+                    "d2h_bytes_per_step": res["e2e"]["d2h"], "ms_per_step": r4(e2e_ms),
+                    "link_gbs": {k: r4(v) for k, v in res["e2e"]["link"].items()}},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "roofline": roof, "cpu_baseline": cpu, "clocks": clk.summary(),
-            "workloads": secondary}
-    print(json.dumps(line))
+            "note": "vs_baseline: over the MI355X figure for this shape (967 TFLOPS, "
+                    "FlyDSL PR #860), context only; workloads: [TFLOPS, mean ms]",
+            "workloads": compact_workloads(secondary),
+            "roofline_by_workload": workload_rooflines(secondary, peaks)}
+    print(json.dumps(line, separators=(",", ":")))
+
+
+def r4(v):
+    """v rounded to 4 significant digits (the JSON line stays short)."""
+    if v is None or not isinstance(v, float) or v == 0.0 or not math.isfinite(v):
+        return v
+    return float(f"{v:.4g}")
+
+
+def compact_workloads(secondary):
+    """{name: [TFLOPS, mean ms]} of the secondary workloads (errors as text)."""
+    out = {}
+    for name, r in secondary.items():
+        if "error" in r:
+            out[name] = r["error"][:80]
+            continue
+        m = statistics.mean(r["ms"])
+        ent = [r4(r["flop"] / (m * 1e-3) / 1e12), r4(m)]
+        if "ms_pack_then_conv" in r:   # channel-major: the pack + conv_fwd alternative
+            ent.append(r4(statistics.mean(r["ms_pack_then_conv"])))
+        out[name] = ent
+    return out
+
+
+def workload_rooflines(secondary, peaks):
+    """Roofline entries of the fp8 conv (and its amax + pack), the temporal
+    conv and the patch embedding: achieved over the measured peak of the
+    kernel's own dtype (e4m3: 2x the bf16 burst, the nominal ratio), and the
+    pack's achieved bytes over the measured copy bandwidth."""
+    out = {}
+    bf16 = peaks["bf16_tflops"]
+    for name, peak in (("fp8_conv3d_1x3x3", 2.0 * bf16), ("temporal_3x1x1_bf16_big", bf16),
+                       ("patch_embed_bf16", bf16)):
+        r = secondary.get(name)
+        if not r or "error" in r:
+            continue
+        m = statistics.mean(r["ms"])
+        a = r["flop"] / (m * 1e-3) / 1e12
+        ent = {"bound": "tensor", "achieved": r4(a), "peak": r4(peak), "frac": r4(a / peak),
+               "ms": r4(m), "ms_median": r4(statistics.median(r["ms"]))}
+        if "ms_with_pack" in r:
+            mp = statistics.mean(r["ms_with_pack"])
+            pk = statistics.mean(r["ms_pack"])
+            gbs = r["pack_bytes"] / (pk * 1e-3) / 1e9
+            ent.update({"with_pack_tflops": r4(r["flop"] / (mp * 1e-3) / 1e12),
+                        "with_pack_ms": r4(mp),
+                        "pack": {"bound": "hbm", "achieved_gbs": r4(gbs), "ms": r4(pk),
+                                 "peak_gbs": peaks["hbm_gbs"],
+                                 "frac": r4(gbs / peaks["hbm_gbs"])}})
+        out[name] = ent
+    return out
 
 
 def main():

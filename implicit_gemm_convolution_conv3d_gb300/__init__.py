@@ -14,6 +14,7 @@ conv2d/conv1d wrapper commit does.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -39,6 +40,16 @@ CLASS_NAMES = {0: "generic", 1: "temporal", 2: "point_gemm", 3: "patch_gemm"}
 CONV_ACT_NONE, CONV_ACT_RELU, CONV_ACT_SILU, CONV_ACT_GELU = 0, 1, 2, 3
 ACT_CODES = {"none": CONV_ACT_NONE, "relu": CONV_ACT_RELU, "silu": CONV_ACT_SILU,
              "gelu": CONV_ACT_GELU}
+
+# conv_overrides (include/conv3d.h), field order as declared there
+OVERRIDE_FIELDS = ("tile_n", "k_bytes", "stages", "group_m", "splits", "pair", "msub", "slices",
+                   "epilogue", "hw_major", "two_phase", "repack", "dy_in_place", "pdl",
+                   "weight_groups", "ncdhw_in_place", "pack_lanes", "log")
+
+
+class _Overrides(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int) for f in OVERRIDE_FIELDS]
+
 
 _I64_5 = ctypes.c_int64 * 5
 _I32_3 = ctypes.c_int * 3
@@ -115,6 +126,14 @@ def load_library(path: str = LIB_PATH):
         lib.pack_fp8_workspace_size.restype = ctypes.c_size_t
         lib.pack_ncdhw_bf16_to_ndhwc_fp8.argtypes = [vp, i64p, vp, vp, vp, ctypes.c_size_t, vp]
         lib.pack_ncdhw_bf16_to_ndhwc_fp8.restype = ctypes.c_int
+        lib.conv_fwd_workspace_size.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int]
+        lib.conv_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.conv_get_device_status_stream.argtypes = [vp, i32p]
+        lib.conv_get_device_status_stream.restype = ctypes.c_int
+        lib.conv_default_overrides.argtypes = [ctypes.POINTER(_Overrides)]
+        lib.conv_default_overrides.restype = None
+        lib.conv_set_overrides.argtypes = [ctypes.POINTER(_Overrides)]
+        lib.conv_set_overrides.restype = ctypes.c_int
         lib.conv_get_device_status.argtypes = [i32p]
         lib.conv_get_device_status.restype = ctypes.c_int
         lib.conv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -207,6 +226,16 @@ def conv_fwd_ncdhw_plan(x_shape, w_shape, stride=1, pad=0, dil=1,
             "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
 
 
+def conv_fwd_workspace_size(x_shape, w_shape, stride=1, pad=0, dil=1,
+                            dtype: int = CONV_DTYPE_BF16) -> int:
+    """Workspace bytes conv_fwd uses for this problem on the current device
+    (0: none needed, or the problem is invalid / unsupported)."""
+    lib = load_library()
+    return int(lib.conv_fwd_workspace_size(_I64_5(*x_shape), _I64_5(*w_shape),
+                                           _I32_3(*_triple(stride)), _I32_3(*_triple(pad)),
+                                           _I32_3(*_triple(dil)), int(dtype)))
+
+
 def conv_fwd_kernel_launches(x_shape, w_shape, stride=1, pad=0, dil=1,
                              dtype: int = CONV_DTYPE_BF16, workspace_bytes: int = 0) -> int:
     """Kernels one conv_fwd call launches for this problem and workspace."""
@@ -219,6 +248,52 @@ def conv_fwd_kernel_launches(x_shape, w_shape, stride=1, pad=0, dil=1,
     return int(n.value)
 
 
+_current_overrides: dict = {}
+
+
+def set_overrides(**fields) -> dict:
+    """Install plan / path overrides for every later call (conv_set_overrides);
+    no arguments restores the library's own choices.  Fields are those of
+    conv_overrides; ``tile="BN,BK,stages,group_m,splits"`` is shorthand for
+    the first five (0 or -1 in it keeps the plan's value).  Returns the
+    overrides that were installed before."""
+    global _current_overrides
+    lib = load_library()
+    vals = dict(fields)
+    tile = vals.pop("tile", None)
+    if tile is not None:
+        for name, v in zip(OVERRIDE_FIELDS[:5], str(tile).split(",")):
+            v = int(v)
+            vals[name] = v if v > 0 else -1
+    unknown = set(vals) - set(OVERRIDE_FIELDS)
+    if unknown:
+        raise ValueError(f"unknown override fields {sorted(unknown)}")
+    o = _Overrides()
+    lib.conv_default_overrides(ctypes.byref(o))
+    for k, v in vals.items():
+        setattr(o, k, -1 if v is None else int(v))
+    _check(lib.conv_set_overrides(ctypes.byref(o)), "conv_set_overrides")
+    old, _current_overrides = _current_overrides, {k: v for k, v in vals.items() if v is not None}
+    return old
+
+
+@contextlib.contextmanager
+def overrides(**fields):
+    """Context manager: the given overrides on top of those already installed,
+    restored on exit (for sweeps and tests)."""
+    merged = dict(_current_overrides)
+    tile = fields.pop("tile", None)
+    if tile is not None:
+        for name, v in zip(OVERRIDE_FIELDS[:5], str(tile).split(",")):
+            merged[name] = int(v) if int(v) > 0 else None
+    merged.update(fields)
+    old = set_overrides(**merged)
+    try:
+        yield
+    finally:
+        set_overrides(**old)
+
+
 def conv_set_wait_limit_ns(ns: int) -> None:
     load_library().conv_set_wait_limit_ns(int(ns))
 
@@ -228,6 +303,16 @@ def conv_get_device_status() -> int:
     lib = load_library()
     v = ctypes.c_int(0)
     _check(lib.conv_get_device_status(ctypes.byref(v)), "conv_get_device_status")
+    return int(v.value)
+
+
+def conv_get_device_status_stream(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """After the work queued on ``stream`` (default: the current stream),
+    read and clear the device status word; synchronises that stream only."""
+    lib = load_library()
+    v = ctypes.c_int(0)
+    _check(lib.conv_get_device_status_stream(_stream_handle(stream), ctypes.byref(v)),
+           "conv_get_device_status_stream")
     return int(v.value)
 
 
@@ -546,5 +631,6 @@ __all__ = [
     "conv3d", "conv2d", "conv1d", "load_library", "ConvError", "LIB_PATH",
     "conv_fwd_from_host", "conv_fwd_kernel_launches", "conv_fwd_ncdhw",
     "conv_fwd_ncdhw_plan", "conv_bwd_point_workspace_bytes", "conv_bwd_data_point",
-    "conv_bwd_weight_point",
+    "conv_bwd_weight_point", "conv_fwd_workspace_size", "conv_get_device_status_stream",
+    "set_overrides", "overrides",
 ]

@@ -8,7 +8,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include <cstdlib>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -621,10 +620,10 @@ cudaError_t launch_pack(const void* in, long long N, long long C, long long S, v
         // warp tile: 32 channels x 128 positions for e4m3 output (each
         // channel row read 256 bytes at a time; measured 1.63 against 1.68 ms
         // for amax + pack of the 3.5 GB fp8 workload activation), 64 x 64
-        // for bf16 output (1.17 against 1.39 ms); CONV3D_PACK_LC=2/4 overrides
-        const char* lc_env = std::getenv("CONV3D_PACK_LC");
+        // for bf16 output (1.17 against 1.39 ms); the pack_lanes override sets it
         int lc = fp8 ? 2 : 4;
-        if (lc_env && (lc_env[0] == '2' || lc_env[0] == '4')) lc = lc_env[0] - '0';
+        const int lanes = overrides().pack_lanes;
+        if (lanes == 2 || lanes == 4) lc = lanes;
         const long long c_tiles = (C + 16 * lc - 1) / (16 * lc);
         const long long s_tiles = (S + 256 / lc - 1) / (256 / lc);
         const long long tiles = N * c_tiles * s_tiles;   // one warp per tile

@@ -112,6 +112,11 @@ int device_info(DeviceInfo** out) {
 
 unsigned long long g_wait_ns = 2000000000ull;
 
+// ------------------------------------------------------------ overrides
+static_assert(sizeof(Overrides) == sizeof(conv_overrides), "override layouts differ");
+std::mutex g_ovr_mutex;
+Overrides g_ovr = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+
 // ------------------------------------------------------------ geometry
 struct Geo {
     long long N, D, H, W, C, K, T, R, S;
@@ -218,17 +223,13 @@ const TileEntry* lookup_tile(int fp8, int cls, const Geo& g, long long M) {
     return nullptr;
 }
 
-// CONV3D_FORCE_TILE="BN,BK,stages,group_m,splits" (0 keeps the default) -- for sweeps.
-void force_tile(int* bn, int* bk, int* st, int* grp, int* spl) {
-    const char* s = std::getenv("CONV3D_FORCE_TILE");
-    if (!s || !*s) return;
-    int v[5] = {0, 0, 0, 0, 0};
-    std::sscanf(s, "%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4]);
-    if (v[0] > 0) *bn = v[0];
-    if (v[1] > 0) *bk = v[1];
-    if (v[2] > 0) *st = v[2];
-    if (v[3] > 0) *grp = v[3];
-    if (v[4] > 0) *spl = v[4];
+// Tile overrides (conv_set_overrides): a field above 0 replaces the plan's value.
+void force_tile(const Overrides& o, int* bn, int* bk, int* st, int* grp, int* spl) {
+    if (o.tile_n > 0) *bn = o.tile_n;
+    if (o.k_bytes > 0) *bk = o.k_bytes;
+    if (o.stages > 0) *st = o.stages;
+    if (o.group_m > 0) *grp = o.group_m;
+    if (o.splits > 0) *spl = o.splits;
 }
 
 bool gemm_amode(int amode) { return amode == AM_GEMM_TMA || amode == AM_GEMM_GATHER; }
@@ -292,6 +293,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         return CONV_ERR_INVALID;
     }
     std::memset(P, 0, sizeof *P);
+    const Overrides ov = overrides();
     P->fp8 = dtype == CONV_DTYPE_FP8_E4M3;
     P->elt = P->fp8 ? 1 : 2;
     const long long elt = P->elt;
@@ -316,12 +318,11 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         // collapses (3x the DRAM reads, 1.8x the time on the 3x1x1 workload).
         // There, when the workspace holds an NDHWC copy, x is packed into it
         // first (6.4 ms against 8.7 ms in place on that workload).
-        // CONV3D_NCDHW_INPLACE=1 keeps in-place reads.
+        // The ncdhw_in_place override keeps in-place reads.
         const size_t xcopy =
             static_cast<size_t>((g.N * g.C * g.D * g.H * g.W * elt + 255) / 256 * 256);
-        const char* ip = std::getenv("CONV3D_NCDHW_INPLACE");
         if (g.T > 1 && g.D * g.H * g.W * elt > kInPlaceChannelBytes && g.C % 16 == 0 &&
-            ws_avail >= xcopy && !(ip && ip[0] == '1')) {
+            ws_avail >= xcopy && ov.ncdhw_in_place != 1) {
             P->ncdhw_pack = 1;
             P->repack_bytes = xcopy;
         } else {
@@ -339,10 +340,9 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         rg = point_output ? g.T * g.R * g.S * g.C : g.C;
         P->g_row_bytes = rg * elt;
         P->tma_row_bytes = P->g_row_bytes;
-        const char* ph = std::getenv("CONV3D_PHASES");
         if (P->g_row_bytes % 16 == 0) {
             P->amode = AM_GEMM_TMA;
-        } else if (P->g_row_bytes % 16 == 8 && P->M >= 2 && !(ph && ph[0] == '1') &&
+        } else if (P->g_row_bytes % 16 == 8 && P->M >= 2 && ov.two_phase != 0 &&
                    ws_avail >= 2 * static_cast<size_t>((g.K * (P->g_row_bytes + 8) + 255) / 256 * 256)) {
             // rows of g_row_bytes = 16q + 8: even rows start 16-byte aligned, odd
             // rows 8 bytes past a boundary.  Two row phases, each a TMA-tiled
@@ -365,8 +365,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
             const long long pitch = (P->g_row_bytes + 15) / 16 * 16;
             const size_t a_bytes = static_cast<size_t>((P->M * pitch + 255) / 256 * 256);
             const size_t b_bytes = static_cast<size_t>((g.K * pitch + 255) / 256 * 256);
-            const char* e = std::getenv("CONV3D_REPACK");
-            if (ws_avail >= a_bytes + b_bytes && !(e && e[0] == '0')) {
+            if (ws_avail >= a_bytes + b_bytes && ov.repack != 0) {
                 P->amode = AM_GEMM_TMA;
                 P->repack = 1;
                 P->repack_bytes = a_bytes + b_bytes;
@@ -448,7 +447,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         pair_pref = e->pair;
         msub_pref = e->msub;
     }
-    force_tile(&BN, &BK, &stages, &group_m, &splits);
+    force_tile(ov, &BN, &BK, &stages, &group_m, &splits);
     // MN-major A boxes are 64 channel rows of 128 bytes: 128- or 256-byte k-steps
     if (P->a_ncdhw && BK < 128) BK = 128;
     if (BN < 32 || BN > 256 || BN % 32 != 0 || !(BK == 32 || BK == 64 || BK == 128 || BK == 256) ||
@@ -517,7 +516,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     // CTA pairs (tcgen05 cta_group::2): a cluster of two CTAs computes a
     // 256-row unit, each SM holding half of the B tile, which halves the B
     // bytes each SM stores and feeds to the tensor core.  Used when the
-    // problem has whole waves of such units; CONV3D_PAIR=0/1 overrides.
+    // problem has whole waves of such units; the pair override decides otherwise.
     P->pair = 0;
     if (P->amode != AM_GEMM_GATHER && splits == 1 && BN >= 64 && num_sms % 2 == 0) {
         const long long pm = P->cls == CONV_CLASS_TEMPORAL
@@ -525,7 +524,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
                                  : (P->M + 2 * kBM - 1) / (2 * kBM);
         int want = pm * P->n_tiles >= 2LL * num_sms ? 1 : 0;
         if (pair_pref >= 0) want = pair_pref;
-        if (const char* e = std::getenv("CONV3D_PAIR")) want = (e[0] == '1') ? 1 : 0;
+        if (ov.pair >= 0) want = ov.pair ? 1 : 0;
         if (want) {
             P->pair = 1;
             set_m_tiles(2 * kBM);
@@ -542,7 +541,7 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
                                  : (P->M + rows - 1) / rows;
         int want = (P->k_steps >= 384 && mt * P->n_tiles >= 2LL * (num_sms >> P->pair)) ? 2 : 1;
         if (msub_pref > 0) want = msub_pref;
-        if (const char* e = std::getenv("CONV3D_MSUB")) want = (e[0] == '2') ? 2 : 1;
+        if (ov.msub > 0) want = ov.msub == 2 ? 2 : 1;
         if (want == 2) {
             P->msub = 2;
             set_m_tiles(rows);
@@ -560,11 +559,11 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     // compiled copy of its code out of the staged epilogues (their code size
     // is what the short point-output kernels are sensitive to).
     P->epi_mode = splits > 1 || act != kActNone ? 0 : (g.K % 8 == 0 ? 1 : (g.K % 2 == 0 ? 2 : 0));
-    // CONV3D_EPI=tma / staged / direct overrides the epilogue kind (for sweeps)
-    if (const char* e = act != kActNone ? nullptr : std::getenv("CONV3D_EPI")) {
-        if (e[0] == 't' && splits == 1 && g.K % 8 == 0) P->epi_mode = 1;
-        if (e[0] == 's' && splits == 1 && g.K % 2 == 0) P->epi_mode = 2;
-        if (e[0] == 'd') P->epi_mode = 0;
+    // the epilogue override (1 TMA, 2 staged, 3 direct) where the shape allows it
+    if (act == kActNone) {
+        if (ov.epilogue == 1 && splits == 1 && g.K % 8 == 0) P->epi_mode = 1;
+        if (ov.epilogue == 2 && splits == 1 && g.K % 2 == 0) P->epi_mode = 2;
+        if (ov.epilogue == 3) P->epi_mode = 0;
     }
     P->epi_bytes = P->epi_mode ? kEpiStageBytes : 0u;
     // pipeline depth from the shared-memory budget (a pair CTA holds half of B)
@@ -594,15 +593,14 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
     // starts its CTAs together, so units sharing weight slices stay in step
     // and find them in L2 (one persistent launch drifts apart over ~44 waves:
     // 27 GB of DRAM traffic per launch against 13 GB sliced on the 3x3x3
-    // video conv, 1.6-4.5% faster under the power cap).  CONV3D_SLICES=n
-    // overrides (1: one launch).
+    // video conv, 1.6-4.5% faster under the power cap).  The slices override
+    // sets the count (1: one launch).
     P->slices = 1;
     if (!gemm_amode(P->amode) && splits == 1) {
         const long long wave = P->grid >> P->pair;
         const long long nb = P->m_tiles / (wave / gcd_ll(wave, P->n_tiles));
         if (P->k_steps >= 384 && nb >= 4) P->slices = static_cast<int>(std::min<long long>(nb, 32));
-        if (const char* e = std::getenv("CONV3D_SLICES"))
-            P->slices = std::max(1, std::min(32, std::atoi(e)));
+        if (ov.slices > 0) P->slices = std::min(32, ov.slices);
     }
     return CONV_OK;
 }
@@ -790,9 +788,8 @@ void fill_params(const Geo& g, const Plan& P, const void* x, const void* w, void
     k.HW = P.HW;
     k.hw_tiles = P.hw_tiles;
     // temporal units of one wave share input planes in L2 when H*W-tile
-    // major; CONV3D_HWMAJOR=0 keeps output row order
-    const char* hm = std::getenv("CONV3D_HWMAJOR");
-    k.hw_major = (P.cls == CONV_CLASS_TEMPORAL && !(hm && hm[0] == '0')) ? 1 : 0;
+    // major; the hw_major override 0 keeps output row order
+    k.hw_major = (P.cls == CONV_CLASS_TEMPORAL && overrides().hw_major != 0) ? 1 : 0;
     k.m_tiles = P.m_tiles;
     k.n_tiles = P.n_tiles;
     k.splits = P.splits;
@@ -1088,6 +1085,11 @@ size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
 
 void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof t_last_error, "%s", msg); }
 
+Overrides overrides() {
+    std::lock_guard<std::mutex> lk(g_ovr_mutex);
+    return g_ovr;
+}
+
 int* device_status_ptr() {
     DeviceInfo* d = nullptr;
     if (device_info(&d) != CONV_OK) return nullptr;
@@ -1114,6 +1116,35 @@ const char* conv_status_string(int status) {
 }
 
 void conv_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns; }
+
+void conv_default_overrides(conv_overrides* o) {
+    if (!o) return;
+    const Overrides d = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    std::memcpy(o, &d, sizeof d);
+}
+
+int conv_set_overrides(const conv_overrides* o) {
+    Overrides v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (o) std::memcpy(&v, o, sizeof v);
+    auto in = [](int x, int lo, int hi) { return x == -1 || (x >= lo && x <= hi); };
+    const bool ok =
+        (v.tile_n == -1 || (v.tile_n >= 32 && v.tile_n <= 256 && v.tile_n % 32 == 0)) &&
+        (v.k_bytes == -1 || v.k_bytes == 32 || v.k_bytes == 64 || v.k_bytes == 128 ||
+         v.k_bytes == 256) &&
+        in(v.stages, 1, 64) && in(v.group_m, 1, 1 << 20) && in(v.splits, 1, 1 << 20) &&
+        in(v.pair, 0, 1) && in(v.msub, 1, 2) && in(v.slices, 1, 32) && in(v.epilogue, 1, 3) &&
+        in(v.hw_major, 0, 1) && in(v.two_phase, 0, 1) && in(v.repack, 0, 1) &&
+        in(v.dy_in_place, 0, 1) && in(v.pdl, 0, 1) && in(v.weight_groups, 0, 1) &&
+        in(v.ncdhw_in_place, 0, 1) && (v.pack_lanes == -1 || v.pack_lanes == 2 || v.pack_lanes == 4) &&
+        in(v.log, 0, 1);
+    if (!ok) {
+        set_error("override value out of range");
+        return CONV_ERR_INVALID;
+    }
+    std::lock_guard<std::mutex> lk(g_ovr_mutex);
+    g_ovr = v;
+    return CONV_OK;
+}
 
 int conv_out_dims(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
                   const int pad[3], const int dil[3], int64_t out_dims[5]) {
@@ -1378,7 +1409,7 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
     fill_params(g, P, x, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
     k.act = act;
 
-    if (std::getenv("CONV3D_LOG")) {
+    if (overrides().log == 1) {
         std::fprintf(stderr,
                      "conv_fwd: class=%d amode=%d fp8=%d M=%lld K=%d BN=%d BK=%d stages=%d "
                      "splits=%d k_steps=%d tiles=%dx%d grid=%d smem=%zu tmem=%u epi=%u pair=%d msub=%d "
@@ -1487,8 +1518,8 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         const long long wave = P.grid >> P.pair;
         const long long units0 = static_cast<long long>(bounds[1] - bounds[0]) * P.n_tiles;
         const long long waves0 = units0 % wave == 0 ? units0 / wave : 0;
-        const char* ws = std::getenv("CONV3D_WSPLIT");
-        if (waves0 >= 2 && waves0 <= kMaxWGroups && P.n_tiles % waves0 == 0 && !(ws && ws[0] == '0')) {
+        if (waves0 >= 2 && waves0 <= kMaxWGroups && P.n_tiles % waves0 == 0 &&
+            overrides().weight_groups != 0) {
             wgroups = static_cast<int>(waves0);
             gtiles = P.n_tiles / wgroups;
         }
@@ -1542,7 +1573,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
             const long long units = static_cast<long long>(k.m_tiles) * k.n_tiles;
             const int grid = P.pair ? 2 * static_cast<int>(std::min<long long>(units, P.grid / 2))
                                     : static_cast<int>(std::min<long long>(units, P.grid));
-            if (std::getenv("CONV3D_LOG"))
+            if (overrides().log == 1)
                 std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) n-tiles "
                              "[%d, %d) rows [%lld, %lld) x prefix %zu B grid %d\n", i, mt0, mt1,
                              k.n_tile0, k.n_tile0 + k.n_tiles, row_lo, row_hi, x_done, grid);
@@ -1731,8 +1762,7 @@ int conv_bwd_weight_point(const void* x, const void* dy, const int64_t x_dims[5]
     // the reduction runs over the batch: dy^T [K, Np] and x^T [J, Np], rows
     // zero-padded to Np (a multiple of 8 elements, 16 bytes)
     const long long Np = (N + 7) / 8 * 8;
-    const char* amn = std::getenv("CONV3D_AMN");
-    if (K % 8 == 0 && !(amn && amn[0] == '0')) {
+    if (K % 8 == 0 && overrides().dy_in_place != 0) {
         // dy's rows are 16-byte multiples: the GEMM reads dy in place as an
         // MN-major A; only x is transposed
         const size_t head = round256(J * Np * 2);
@@ -1758,6 +1788,34 @@ int conv_bwd_weight_point(const void* x, const void* dy, const int64_t x_dims[5]
     const int one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
     return conv_fwd(wsb, xi, wsb + dyt, wi, one, zero, one, CONV_DTYPE_BF16, nullptr, nullptr, dw,
                     wsb + head, workspace_bytes - head, stream);
+}
+
+size_t conv_fwd_workspace_size(const int64_t x_dims[5], const int64_t w_dims[5],
+                               const int stride[3], const int pad[3], const int dil[3],
+                               int dtype) {
+    size_t bytes = 0;
+    if (conv_fwd_plan(x_dims, w_dims, stride, pad, dil, dtype, 0, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, nullptr, &bytes) != CONV_OK)
+        return 0;
+    return bytes;
+}
+
+int conv_get_device_status_stream(cudaStream_t stream, int* device_status) {
+    if (!device_status) {
+        set_error("null argument");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    // read, then clear, in stream order after the stream's earlier work
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dev->status, 0, sizeof(int), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status read on the stream");
+    *device_status = v;
+    return CONV_OK;
 }
 
 int conv_get_device_status(int* device_status) {

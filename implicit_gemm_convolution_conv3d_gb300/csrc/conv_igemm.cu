@@ -28,7 +28,6 @@
 // drains its copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_bf16.h>
 
-#include <cstdlib>
 #include <type_traits>
 
 #include "internal.h"
@@ -953,9 +952,8 @@ cudaError_t launch_one(const TMaps* tm, const KParams& p, int grid, size_t smem,
     cudaLaunchAttribute attr[2];
     int n = 0;
     // the set-up (barriers, TMEM, descriptor prefetch) may overlap the tail
-    // of the previous kernel in the stream; CONV3D_PDL=0 turns this off
-    const char* pdl = std::getenv("CONV3D_PDL");
-    if (!(pdl && pdl[0] == '0')) {
+    // of the previous kernel in the stream; the pdl override 0 turns this off
+    if (overrides().pdl != 0) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;

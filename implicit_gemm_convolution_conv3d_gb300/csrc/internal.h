@@ -169,6 +169,14 @@ cudaError_t launch_pack(const void* in, long long N, long long C, long long S, v
 
 int* device_status_ptr();   // device address of the status word (current device)
 
+// The process's plan / path overrides (conv_set_overrides), copied under a
+// lock; every field -1 keeps the library's own choice.
+struct Overrides {
+    int tile_n, k_bytes, stages, group_m, splits, pair, msub, slices, epilogue, hw_major,
+        two_phase, repack, dy_in_place, pdl, weight_groups, ncdhw_in_place, pack_lanes, log;
+};
+Overrides overrides();
+
 // Record a failure description for conv_last_error() on the calling thread.
 void set_last_error(const char* msg);
 

@@ -28,8 +28,11 @@
  *     keeps only a per-device status word, per-process host state
  *     (function pointers, device attributes) and, once conv_fwd_from_host
  *     has run on a device, two copy streams and a set of events there.
+ *     That per-device state lives until the process exits: after
+ *     cudaDeviceReset on a device, do not use the library on that device
+ *     again in the same process.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do
- *     not synchronise the host, except conv_get_device_status.
+ *     not synchronise the host, except conv_get_device_status(_stream).
  *   - Every function returns a conv_status; no exception crosses the ABI.
  *     On any non-OK return nothing has been launched (conv_fwd_from_host:
  *     see there).
@@ -91,6 +94,18 @@ int conv_fwd_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int st
                   const int pad[3], const int dil[3], int dtype, int num_sms, int* cls,
                   int* tile_n, int* k_bytes, int* stages, int* splits, int* ctas,
                   size_t* workspace_bytes);
+
+/* Bytes of device workspace conv_fwd uses for this problem on the current
+ * device: the workspace_bytes conv_fwd_plan reports (split-K partials,
+ * aligned operand copies of a point-output GEMM, the gathered rows of the
+ * patch class).  0 when the plan needs none, and also when the problem is
+ * invalid or unsupported or no GPU is usable (conv_fwd_plan returns the
+ * status, conv_last_error describes it).  Needs a GPU.  The split-K rule it
+ * sizes follows FlyDSL PR #860's split-K commits (split the reduction when
+ * the output tiles leave the GPU under-filled). */
+size_t conv_fwd_workspace_size(const int64_t x_dims[5], const int64_t w_dims[5],
+                               const int stride[3], const int pad[3], const int dil[3],
+                               int dtype);
 
 /* Number of kernels conv_fwd launches for this problem and workspace size on
  * the current device (operand copies / patch gather, the convolution's
@@ -314,7 +329,9 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
  * passes x, w, the scales and out.
  *   - A problem whose split-K partials need more than
  *     CONV_NOALLOC_SCRATCH_BYTES is rejected with CONV_ERR_INVALID
- *     (conv_last_error says how many bytes it needed).
+ *     (conv_last_error says how many bytes it needed), rather than run
+ *     without split-K: a caller gets conv_fwd's plan or an error, never a
+ *     silently slower plan.
  *   - Operand copies that conv_fwd makes in its workspace (aligned copies of
  *     a point-output GEMM's operands, the gathered rows of the patch class)
  *     go to the array too when they fit; the optional ones are skipped
@@ -322,7 +339,10 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
  *     is rejected with CONV_ERR_INVALID.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the process, like
+ *     the library's other per-device state (status word, copy streams): after
+ *     cudaDeviceReset on a device, do not use the library on that device
+ *     again in the same process.
  *   - Every call on a device shares the one array, which keeps the last
  *     call's contents.  Each call overwrites the partials it reads, so
  *     nothing needs clearing; but calls whose kernels overlap on the GPU
@@ -333,11 +353,54 @@ int conv_fwd_noalloc(const void* x, const int64_t x_dims[5], const void* w,
                      const int dil[3], int dtype, const float* scale_x, const float* scale_w,
                      void* out, cudaStream_t stream);
 
+/* Plan and path overrides, for tile sweeps, A/B measurements and tests;
+ * none is needed in normal use.  Every field set to -1 keeps the library's
+ * own choice (conv_default_overrides fills a struct that way).  Nothing is
+ * read from the environment: only conv_set_overrides changes these. */
+typedef struct {
+    int tile_n;          /* tile columns: 32..256, a multiple of 32 */
+    int k_bytes;         /* bytes of one row per k-step: 32, 64, 128 or 256 */
+    int stages;          /* shared-memory pipeline depth */
+    int group_m;         /* raster group: consecutive m-tiles per group (>= 1) */
+    int splits;          /* split-K factor (>= 1) */
+    int pair;            /* 0: single CTAs, 1: CTA pairs (cta_group::2) */
+    int msub;            /* row sub-tiles per unit sharing each B stage: 1 or 2 */
+    int slices;          /* launches of whole waves a long reduction is cut into (>= 1) */
+    int epilogue;        /* 1: TMA tensor stores, 2: staged 8/4-byte stores, 3: direct */
+    int hw_major;        /* temporal class: 0 output-row order, 1 H*W-tile-major order */
+    int two_phase;       /* point-output GEMM: 0 turns off the two-row-phase form */
+    int repack;          /* point-output GEMM: 0 turns off the aligned operand copies */
+    int dy_in_place;     /* backward weights: 0 transposes dy instead of reading it in place */
+    int pdl;             /* 0: launches without programmatic dependent launch */
+    int weight_groups;   /* conv_fwd_from_host: 0 keeps the first slice in one launch */
+    int ncdhw_in_place;  /* conv_fwd_ncdhw: 1 always reads x in place (no packed copy) */
+    int pack_lanes;      /* pack kernels: 2 or 4 lanes per position (warp-tile shape) */
+    int log;             /* 1: print each plan and slice to stderr */
+} conv_overrides;
+
+/* Fills *o with -1 in every field (the library's own choices). */
+void conv_default_overrides(conv_overrides* o);
+
+/* Installs *o for every later call in the process; NULL restores the
+ * defaults.  Returns CONV_ERR_INVALID (and keeps the previous overrides) for
+ * a value outside a field's range.  Calls already enqueued are not
+ * affected; calls running concurrently on other threads see either the old
+ * or the new set. */
+int conv_set_overrides(const conv_overrides* o);
+
 /* Reads and clears the current device's status word, after synchronising
  * the device.  *device_status receives CONV_OK, or CONV_ERR_TIMEOUT if a
  * kernel gave up on a bounded wait since the last call.  Returns
  * CONV_ERR_CUDA if the synchronisation or copy failed. */
 int conv_get_device_status(int* device_status);
+
+/* conv_get_device_status in the order of one stream: after the work queued
+ * on `stream` so far, reads and clears the current device's status word
+ * and synchronises that stream only (not the device).  The word is shared
+ * by every stream of the device, so a timeout recorded by a kernel on
+ * another stream is reported (and cleared) here too.  Returns CONV_ERR_CUDA
+ * if the copy or the synchronisation failed. */
+int conv_get_device_status_stream(cudaStream_t stream, int* device_status);
 
 /* Upper bound, in nanoseconds, on every spin-wait inside the kernels
  * (default 2e9 = 2 s).  A kernel that waits longer records CONV_ERR_TIMEOUT

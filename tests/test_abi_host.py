@@ -40,6 +40,19 @@ def test_header_declares_the_abi():
         assert must in names
 
 
+def test_workspace_size_without_a_gpu_is_zero_with_a_reason(pkg):
+    """conv_fwd_workspace_size plans for the current device: with no GPU it
+    answers 0 and leaves the reason in conv_last_error (no launch, no fault)."""
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU tests compare the size with conv_fwd_plan")
+    lib = pkg.load_library()
+    i64, i32 = ctypes.c_int64 * 5, ctypes.c_int * 3
+    n = lib.conv_fwd_workspace_size(i64(1, 4, 8, 8, 16), i64(32, 3, 3, 3, 16), i32(1, 1, 1),
+                                    i32(1, 1, 1), i32(1, 1, 1), 0)
+    assert n == 0
+    assert lib.conv_last_error().decode() != ""
+
+
 def test_library_exports_every_declared_symbol(pkg):
     lib = ctypes.CDLL(pkg.LIB_PATH)
     missing = [n for n in _declared_functions() if not hasattr(lib, n)]
@@ -123,22 +136,24 @@ def test_plan_tiles_are_legal(pkg):
             assert 1 <= p["ctas"] <= 148
 
 
-def test_forced_wide_k_step_plans(pkg, monkeypatch):
+def test_forced_wide_k_step_plans(pkg):
     """256-byte k-steps: accepted for every TMA operand mode, the reduction is
     cut into ceil(row bytes / 256) chunks, and the pipeline fits in shared
     memory; other k-step widths are rejected as invalid overrides."""
     sms = 148
-    monkeypatch.setenv("CONV3D_FORCE_TILE", "128,256,0,1,1")
-    for xs, ws, st, pa, cls in [((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, "generic"),
+    with pkg.overrides(tile="128,256,0,1,1"):
+        plans = [(pkg.conv_fwd_plan(xs, ws, st, pa, 1, 0, sms), cls) for xs, ws, st, pa, cls in [((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, "generic"),
                                 ((1, 5, 10, 50, 200), (200, 3, 1, 1, 200), 1, (1, 0, 0), "temporal"),
-                                ((600, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, "point_gemm")]:
-        p = pkg.conv_fwd_plan(xs, ws, st, pa, 1, 0, sms)
+                                ((600, 1, 4, 4, 16), (160, 1, 4, 4, 16), (1, 4, 4), 0, "point_gemm")]]
+    for p, cls in plans:
         assert p["class"] == cls and p["k_bytes"] == 256 and p["stages"] >= 2
         assert (128 * 256 + 128 * 256) * p["stages"] + 1280 <= 232448
-    monkeypatch.setenv("CONV3D_FORCE_TILE", "128,512,0,1,1")
     with pytest.raises(pkg.ConvError) as e:
-        pkg.conv_fwd_plan((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, 1, 0, sms)
+        with pkg.overrides(tile="128,512,0,1,1"):
+            pass
     assert e.value.status == pkg.CONV_ERR_INVALID
+    # a rejected set leaves the previous overrides (none) in place
+    assert pkg.conv_fwd_plan((1, 6, 10, 12, 200), (96, 3, 3, 3, 200), 1, 1, 1, 0, sms)["k_bytes"] != 256
 
 
 def test_invalid_and_unsupported_arguments(pkg):

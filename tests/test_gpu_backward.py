@@ -114,14 +114,11 @@ def test_backward_odd_extents(pkg):
 @pytest.mark.parametrize("amn", ["0", "1"])
 def test_backward_weight_both_operand_paths(pkg, amn):
     """dW with dy read in place as an MN-major operand (K % 8 == 0, the default)
-    and through the transposed copy (CONV3D_AMN=0): both against the oracle,
+    and through the transposed copy (the dy_in_place override 0): both against the oracle,
     with split-K and without (a workspace holding only the copies)."""
-    import os
     xs, K = (700, 1, 14, 14, 3), 256
     x, w, dy, ws, st = _operands(xs, K, 14)
-    old = os.environ.get("CONV3D_AMN")
-    os.environ["CONV3D_AMN"] = amn
-    try:
+    with pkg.overrides(dy_in_place=int(amn)):
         for small in (False, True):
             wsp = None
             if small:
@@ -133,8 +130,3 @@ def test_backward_weight_both_operand_paths(pkg, amn):
             assert pkg.conv_get_device_status() == 0
             assert_close(as_f64(dw), oracle.conv3d_bwd_weight(bits16(x), bits16(dy), ws, st),
                          f"wgrad amn={amn} small_ws={small}")
-    finally:
-        if old is None:
-            os.environ.pop("CONV3D_AMN", None)
-        else:
-            os.environ["CONV3D_AMN"] = old

@@ -4,8 +4,6 @@ tails and cover every dispatch class (im2col implicit GEMM, temporal T x 1 x 1,
 point-output / pointwise GEMM by TMA and by row gather), with and without
 split-K, plus forced tile shapes, exact delta filters, the 2-D / 1-D wrappers
 and NaN-prefilled canary guards."""
-import contextlib
-import os
 
 import numpy as np
 import pytest
@@ -27,17 +25,10 @@ def pkg():
     return p
 
 
-@contextlib.contextmanager
 def forced_tile(spec):
-    old = os.environ.get("CONV3D_FORCE_TILE")
-    os.environ["CONV3D_FORCE_TILE"] = spec
-    try:
-        yield
-    finally:
-        if old is None:
-            os.environ.pop("CONV3D_FORCE_TILE", None)
-        else:
-            os.environ["CONV3D_FORCE_TILE"] = old
+    """Plan override: tile "BN,BK,stages,group_m,splits" (0 keeps the plan's)."""
+    import implicit_gemm_convolution_conv3d_gb300 as p
+    return p.overrides(tile=spec)
 
 
 def _inputs(xs, ws, seed):
@@ -244,31 +235,9 @@ PAIR_CASES = [
 @pytest.mark.parametrize("case", PAIR_CASES, ids=[str(i) for i in range(len(PAIR_CASES))])
 def test_cta_pair_kernel(pkg, case):
     xs, ws, st, pa, di, spec = case
-    old = os.environ.get("CONV3D_PAIR")
-    os.environ["CONV3D_PAIR"] = "1"
-    try:
-        with forced_tile(spec):
-            _run_and_check(pkg, xs, ws, st, pa, di, seed=90 + PAIR_CASES.index(case),
-                           split_k=False, what=f"pair {case}")
-    finally:
-        if old is None:
-            os.environ.pop("CONV3D_PAIR", None)
-        else:
-            os.environ["CONV3D_PAIR"] = old
-
-
-@contextlib.contextmanager
-def env_vars(**kv):
-    old = {k: os.environ.get(k) for k in kv}
-    os.environ.update({k: str(v) for k, v in kv.items()})
-    try:
-        yield
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
+    with pkg.overrides(pair=1), forced_tile(spec):
+        _run_and_check(pkg, xs, ws, st, pa, di, seed=90 + PAIR_CASES.index(case),
+                       split_k=False, what=f"pair {case}")
 
 
 # Two row sub-tiles per unit sharing each B stage, with and without CTA pairs.
@@ -285,7 +254,7 @@ MSUB_CASES = [
 @pytest.mark.parametrize("pair", [0, 1])
 def test_two_row_subtiles(pkg, case, pair):
     xs, ws, st, pa, di, spec = case
-    with env_vars(CONV3D_MSUB=2, CONV3D_PAIR=pair), forced_tile(spec):
+    with pkg.overrides(msub=2, pair=pair), forced_tile(spec):
         _run_and_check(pkg, xs, ws, st, pa, di, seed=120 + MSUB_CASES.index(case),
                        split_k=False, what=f"msub2 pair={pair} {case}")
 
@@ -314,7 +283,7 @@ WIDE_K_PLANS = [(0, 1, "128,256,0,0,1"), (1, 1, "224,256,0,0,1"), (0, 2, "96,256
 def test_wide_k_steps(pkg, case, plan):
     xs, ws, st, pa, di = case
     pair, msub, spec = plan
-    with env_vars(CONV3D_MSUB=msub, CONV3D_PAIR=pair), forced_tile(spec):
+    with pkg.overrides(msub=msub, pair=pair), forced_tile(spec):
         assert pkg.conv_fwd_plan(xs, ws, st, pa, di)["k_bytes"] == 256
         _run_and_check(pkg, xs, ws, st, pa, di, seed=140 + WIDE_K_CASES.index(case),
                        split_k=True, what=f"bk256 pair={pair} msub={msub} {spec} {case}")
@@ -353,8 +322,8 @@ def test_point_gemm_two_phases(pkg, case, split_k):
     ref = oracle_conv(x, w, pkg._triple(st), pkg._triple(pa), pkg._triple(di))
     assert_close(as_f64(y), ref, f"two-phase {case} split={split_k}")
     if split_k:
-        # the same problem through the full operand repack (CONV3D_PHASES=1)
-        with env_vars(CONV3D_PHASES=1):
+        # the same problem through the full operand repack (two_phase=0)
+        with pkg.overrides(two_phase=0):
             y1 = pkg.conv_fwd(x, w, st, pa, di)
             torch.cuda.synchronize()
         assert_close(as_f64(y1), ref, f"repack {case}")
@@ -363,7 +332,7 @@ def test_point_gemm_two_phases(pkg, case, split_k):
 @pytest.mark.parametrize("pair", [0, 1])
 def test_point_gemm_two_phases_forced_pair(pkg, pair):
     xs, ws = (1100, 1, 14, 14, 3), (256, 1, 14, 14, 3)
-    with env_vars(CONV3D_PAIR=pair), forced_tile("128,128,0,1,1"):
+    with pkg.overrides(pair=pair), forced_tile("128,128,0,1,1"):
         _run_and_check(pkg, xs, ws, (1, 14, 14), 0, 1, seed=170, split_k=True,
                        what=f"two-phase pair={pair}")
 
@@ -495,7 +464,7 @@ def test_sliced_launches_are_bit_identical(pkg, case, slices):
     xs, ws, st, pa, di = case
     x, w = _inputs(xs, ws, 230)
     one = pkg.conv_fwd(x, w, st, pa, di, split_k=False)
-    with env_vars(CONV3D_SLICES=slices):
+    with pkg.overrides(slices=slices):
         sl = pkg.conv_fwd(x, w, st, pa, di, split_k=False)
         n = pkg.conv_fwd_kernel_launches(xs, ws, st, pa, di, 0, 0)
     torch.cuda.synchronize()

@@ -137,18 +137,10 @@ def test_fp8_conv_wide_k_steps(pkg, case, plan):
     x = cw.randn_bf16(xs, 400 + FP8_CASES.index(case), 1.0, "cuda")
     w = cw.randn_bf16(ws, 500 + FP8_CASES.index(case), 1.0 / np.sqrt(crs), "cuda")
     qx, sx, qw, sw = _fp8_operands(pkg, x, w)
-    old = {k: os.environ.get(k) for k in ("CONV3D_FORCE_TILE", "CONV3D_PAIR")}
-    os.environ.update({"CONV3D_FORCE_TILE": spec, "CONV3D_PAIR": str(pair)})
-    try:
+    with pkg.overrides(tile=spec, pair=pair):
         assert pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), st, pa, di, 1)["k_bytes"] == 256
         y = pkg.conv_fwd(qx, qw, st, pa, di, scale_x=sx, scale_w=sw)
         torch.cuda.synchronize()
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
     assert pkg.conv_get_device_status() == 0
     ref = oracle.conv3d(bytes8(qx), bytes8(qw), pkg._triple(st), pkg._triple(pa), pkg._triple(di),
                         sx.item(), sw.item())

@@ -34,20 +34,6 @@ def pkg():
     return p
 
 
-@contextlib.contextmanager
-def _env(kv):
-    old = {k: os.environ.get(k) for k in kv}
-    os.environ.update({k: str(v) for k, v in kv.items()})
-    try:
-        yield
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-
-
 def _out_len(n, f, s, p, d):
     return (n + 2 * p - d * (f - 1) - 1) // s + 1
 
@@ -102,9 +88,9 @@ def _draw_plan(rng):
     stages = int(rng.choice([0, 0, 2, 3, 4, 6]))
     group = int(rng.choice([1, 2, 4, 8]))
     splits = int(rng.choice([1, 1, 2, 3, 5]))
-    return {"CONV3D_FORCE_TILE": f"{bn},{bk},{stages},{group},{splits}",
-            "CONV3D_PAIR": int(rng.integers(0, 2)), "CONV3D_MSUB": int(rng.integers(1, 3)),
-            "CONV3D_SLICES": int(rng.choice([1, 1, 2, 3]))}
+    return {"tile": f"{bn},{bk},{stages},{group},{splits}",
+            "pair": int(rng.integers(0, 2)), "msub": int(rng.integers(1, 3)),
+            "slices": int(rng.choice([1, 1, 2, 3]))}
 
 
 def _case(i):
@@ -149,14 +135,14 @@ def test_random_problem_random_plan(pkg, i):
         assert e.status == pkg.CONV_ERR_UNSUPPORTED
         pytest.skip(f"shape outside coverage: {e}")
     env = plan
-    with _env(env):
+    with pkg.overrides(**env):
         try:
             p = pkg.conv_fwd_plan(xs, ws, st, pa, di, dtype)
         except pkg.ConvError:
             env, p = {}, None
     bias, act = _epilogue(i, ws[0])
     bias_t = torch.from_numpy(bias).cuda() if bias is not None else None
-    with _env(env):
+    with pkg.overrides(**env):
         if p is None:
             p = pkg.conv_fwd_plan(xs, ws, st, pa, di, dtype)
         y = pkg.conv_fwd(x, w, st, pa, di, scale_x=sx, scale_w=sw, bias=bias_t, act=act)

@@ -127,27 +127,27 @@ def test_host_pipeline_unsliced_plans(pkg, case):
 
 
 @pytest.mark.parametrize("bn", [128, 64])
-def test_host_pipeline_first_slice_split_over_weight_groups(pkg, capfd, bn, monkeypatch):
+def test_host_pipeline_first_slice_split_over_weight_groups(pkg, capfd, bn):
     """Eight (or sixteen) column tiles: the first slice runs as one wave per
     group of column tiles, each after its weight rows have landed.  The result
     equals conv_fwd's bit for bit, and the weights arrive whole on the
-    device; with the split turned off (CONV3D_WSPLIT=0) the bits are the
+    device; with the split turned off (weight_groups=0) the bits are the
     same."""
     xs, ws = (1, 8, 48, 48, 64), (1024, 3, 3, 3, 64)
     x, w = _operands(xs, ws, 40 + bn)
-    monkeypatch.setenv("CONV3D_FORCE_TILE", f"{bn},0,0,0,0")
-    monkeypatch.setenv("CONV3D_LOG", "1")
-    hout = _run(pkg, x, w, 1, 1, 1, 0)
-    log = capfd.readouterr().err
-    ref = pkg.conv_fwd(x, w, 1, 1, 1, split_k=False)
-    torch.cuda.synchronize()
+    with pkg.overrides(tile=f"{bn},0,0,0,0", log=1):
+        hout = _run(pkg, x, w, 1, 1, 1, 0)
+        log = capfd.readouterr().err
+        ref = pkg.conv_fwd(x, w, 1, 1, 1, split_k=False)
+        torch.cuda.synchronize()
+        plan_ctas = pkg.conv_fwd_plan(xs, ws, 1, 1, 1)["ctas"]
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
     chunk0 = [ln for ln in log.splitlines() if ln.startswith("conv_fwd_from_host: chunk 0 ")]
     n_tiles = 1024 // bn
-    if pkg.conv_fwd_plan(xs, ws, 1, 1, 1)["ctas"] % 2 == 0:
+    if plan_ctas % 2 == 0:
         assert len(chunk0) >= 2, log   # split over weight groups
         assert chunk0[0].split("n-tiles ")[1].startswith("[0, ")
         assert not chunk0[0].split("n-tiles ")[1].startswith(f"[0, {n_tiles})")
-    monkeypatch.setenv("CONV3D_WSPLIT", "0")
-    hout2 = _run(pkg, x, w, 1, 1, 1, 0)
+    with pkg.overrides(tile=f"{bn},0,0,0,0", weight_groups=0):
+        hout2 = _run(pkg, x, w, 1, 1, 1, 0)
     assert torch.equal(hout2.view(torch.int16), hout.view(torch.int16))

@@ -29,20 +29,6 @@ def pkg():
     return p
 
 
-@contextlib.contextmanager
-def _env(kv):
-    old = {k: os.environ.get(k) for k in kv}
-    os.environ.update({k: str(v) for k, v in kv.items()})
-    try:
-        yield
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-
-
 # (x NCDHW, K, T, temporal stride, pad, dilation)
 CASES = [
     ((1, 64, 6, 8, 16), 32, 3, 1, 1, 1),       # H*W = 128: one tile row per plane
@@ -135,10 +121,10 @@ def _random_plan(rng):
     bk = int(rng.choice([128, 256]))
     stages = int(rng.choice([0, 2, 3, 4]))
     splits = int(rng.choice([1, 1, 2, 3]))
-    return {"CONV3D_FORCE_TILE": f"{bn},{bk},{stages},{int(rng.choice([1, 4]))},{splits}",
-            "CONV3D_PAIR": int(rng.integers(0, 2)), "CONV3D_MSUB": int(rng.integers(1, 3)),
-            "CONV3D_SLICES": int(rng.choice([1, 2, 3])),
-            "CONV3D_HWMAJOR": int(rng.integers(0, 2))}
+    return {"tile": f"{bn},{bk},{stages},{int(rng.choice([1, 4]))},{splits}",
+            "pair": int(rng.integers(0, 2)), "msub": int(rng.integers(1, 3)),
+            "slices": int(rng.choice([1, 2, 3])),
+            "hw_major": int(rng.integers(0, 2))}
 
 
 @pytest.mark.parametrize("i", range(24))
@@ -152,14 +138,14 @@ def test_ncdhw_random_plans(pkg, i):
     env = _random_plan(rng)
     x, w = _operands(xs, K, T, 100 + i)
     plan = None
-    with _env(env):
+    with pkg.overrides(**env):
         try:
             plan = pkg.conv_fwd_ncdhw_plan(xs, tuple(w.shape), st, pa, di)
         except pkg.ConvError:   # a forced tile this shape cannot take: default plan
             pass
     if plan is None:
         env, plan = {}, pkg.conv_fwd_ncdhw_plan(xs, tuple(w.shape), st, pa, di)
-    with _env(env):
+    with pkg.overrides(**env):
         y = pkg.conv_fwd_ncdhw(x, w, st, pa, di)
         torch.cuda.synchronize()
     assert pkg.conv_get_device_status() == 0
@@ -232,13 +218,13 @@ def test_ncdhw_packed_copy_matches_oracle(pkg, i):
 
 
 def test_ncdhw_small_workspace_reads_in_place(pkg):
-    """Without room for the NDHWC copy (or with CONV3D_NCDHW_INPLACE=1) the
+    """Without room for the NDHWC copy (or with the ncdhw_in_place override) the
     same problem reads x in place; both against the oracle."""
     xs, K, T, st, pa, di = _geometry(PIPE_CASES[0])
     x, w = _operands(xs, K, T, 310)
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     a = pkg.conv_fwd_ncdhw(x, w, st, pa, di, workspace=ws)
-    with _env({"CONV3D_NCDHW_INPLACE": 1}):
+    with pkg.overrides(ncdhw_in_place=1):
         b = pkg.conv_fwd_ncdhw(x, w, st, pa, di)
     torch.cuda.synchronize()
     assert pkg.conv_get_device_status() == 0
