@@ -305,6 +305,222 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const __nv_bfloat16* __
     }
 }
 
+// ----------------------------------------------------------------- TMA-fed pack
+// The pack for C % 8 == 0 and D*H*W % 8 == 0 with the activation arriving by
+// TMA.  Per image the input is a [C, S] matrix (S = D*H*W positions); a tile
+// is 128 channel rows x 256 positions: 512 contiguous bytes of each row, one
+// TMA box {256, 128, 1} (out-of-range rows and positions read as zeros and
+// are not stored).  One producer thread keeps `stages` tiles in flight in a
+// shared-memory ring (full / empty mbarriers), so the bytes in flight sit in
+// shared memory, not in registers.  Sixteen converter warps transpose each
+// tile in units of 8 channels x 8 positions, one unit per thread: eight
+// 16-byte row reads -- conflict-free, the 8 lanes of a quarter-warp read 8
+// consecutive 16-byte pieces of one row -- then each position's 8 channels
+// leave as one 8-byte (e4m3) or 16-byte (bf16) store.  Persistent grid;
+// tiles are walked channels-fastest, so the CTAs running together write all
+// channels of the same output positions (whole output rows leave L2
+// together) while each reads 512-byte pieces of its channel rows.
+constexpr int kTmaPackPos = 256;
+constexpr int kTmaPackConvWarps = 16;
+constexpr int kTmaPackThreads = (kTmaPackConvWarps + 1) * 32;
+constexpr unsigned long long kPackDrainCycles = 2000000000ull;
+
+template <int FP8>
+struct TmaPackShape {
+    static constexpr int kC = 128;                                  // channels per tile
+    static constexpr uint32_t kStageBytes = kC * kTmaPackPos * 2;   // bf16 input tile
+};
+
+// Bounded mbarrier wait of the pack kernel: false once the abort flag is set
+// or the limit (SM cycles at 2 per ns) passes, recording the timeout.
+__device__ __noinline__ bool pack_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       int* status, unsigned long long limit_ns) {
+    const long long t0 = clock64();
+    const long long limit = static_cast<long long>(limit_ns > (1ull << 61) ? (1ull << 61) : limit_ns) * 2;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1u;
+            atomicExch(status, 4);   // CONV_ERR_TIMEOUT
+            return false;
+        }
+    }
+    return true;
+}
+
+// x / scale correctly rounded, from y = 1/scale correctly rounded (computed
+// once): q0 = x*y, r = x - scale*q0 (exact by one FMA), q = q0 + r*y rounded
+// once.  This is the FMA correction step of Markstein's division scheme
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34(1), 1990): with y the
+// correctly rounded reciprocal it returns the correctly rounded quotient
+// while no intermediate underflows.  Three instructions where an IEEE
+// division takes about three times as many; the pack uses it for scales of
+// at least 2^-60 whose significand is not all ones (quotients that matter
+// for e4m3 then keep every intermediate far from underflow) and divides
+// otherwise.  It runs on |x| and puts x's sign back: for x = -0 the FMAs'
+// exact zero sums would give +0 where the division gives -0 (another e4m3
+// code).  The exhaustive codec tests compare its codes with the oracle's
+// division for every bf16 pattern.
+__device__ __forceinline__ float quot_corrected(float x, float scale, float y) {
+    const float xa = fabsf(x);
+    const float q0 = __fmul_rn(xa, y);
+    const float r = __fmaf_rn(-scale, q0, xa);
+    const float q = __fmaf_rn(r, y, q0);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// One converter unit of the TMA-fed pack: 8 channel rows x 8 positions of the
+// tile in shared memory (v: row k's 8 positions) to 8 output positions.
+template <int FP8, bool CORR>
+__device__ __forceinline__ void pack_unit_store(const uint4 (&v)[8], long long n, long long s0,
+                                                long long c, long long C, long long S, void* out,
+                                                float scale, float rscale) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const long long s = s0 + i;
+        if (s >= S) break;
+        // element i of each channel row: word i/2, low or high half
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t ww = (i >> 1) == 0 ? v[k].x : (i >> 1) == 1 ? v[k].y
+                              : (i >> 1) == 2 ? v[k].z : v[k].w;
+            w[k] = (i & 1) ? (ww >> 16) : (ww & 0xFFFFu);
+        }
+        const long long o = (n * S + s) * C + c;
+        if (FP8) {
+            uint32_t q[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t b = 0;
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float x0 = __uint_as_float(w[4 * h + e] << 16);
+                    const float x1 = __uint_as_float(w[4 * h + e + 1] << 16);
+                    const float a0 = CORR ? quot_corrected(x0, scale, rscale) : x0 / scale;
+                    const float a1 = CORR ? quot_corrected(x1, scale, rscale) : x1 / scale;
+                    const __nv_fp8x2_storage_t q2 =
+                        __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+                    b |= static_cast<uint32_t>(q2) << (8 * e);
+                }
+                q[h] = b;
+            }
+            *reinterpret_cast<uint2*>(static_cast<unsigned char*>(out) + o) = make_uint2(q[0], q[1]);
+        } else {
+            *reinterpret_cast<uint4*>(static_cast<unsigned short*>(out) + o) =
+                make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16),
+                           w[6] | (w[7] << 16));
+        }
+    }
+}
+
+template <int FP8>
+__global__ void __launch_bounds__(kTmaPackThreads, 1)
+    pack_tma_kernel(const __grid_constant__ CUtensorMap in_map, long long C, long long S,
+                    void* __restrict__ out, const unsigned int* amax_bits, float* scale_out,
+                    long long c_tiles, long long s_tiles, long long tiles, int stages, int* status,
+                    unsigned long long wait_ns) {
+    using Shape = TmaPackShape<FP8>;
+    griddep_launch_dependents();   // the conv reading this output waits for completion
+    extern __shared__ unsigned char pack_smem[];
+    const uint32_t raw = smem_u32(pack_smem);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t full0 = base + static_cast<uint32_t>(stages) * Shape::kStageBytes;
+    const uint32_t empty0 = full0 + 8u * stages;
+    volatile uint32_t* abort_flag =
+        reinterpret_cast<volatile uint32_t*>(pack_smem + (empty0 + 8u * stages - raw));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kTmaPackConvWarps);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+        prefetch_tmap(&in_map);
+    }
+    // e4m3: quotients by the scale through its reciprocal and one correction
+    // step, except for tiny scales or an all-ones significand (IEEE division)
+    float scale = 1.0f, rscale = 1.0f;
+    bool corr = false;
+    if (FP8) {
+        scale = fp8_scale_of(amax_bits);
+        rscale = __frcp_rn(scale);
+        corr = scale >= 8.6736174e-19f &&   // 2^-60
+               (__float_as_uint(scale) & 0x7FFFFFu) != 0x7FFFFFu;
+        if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = scale;
+    }
+    __syncthreads();   // the barriers are initialised before any thread uses them
+    long long issued = 0;
+    if (warp == kTmaPackConvWarps) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+                if (!pack_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, status, wait_ns)) break;
+                const long long ct = t % c_tiles, rest = t / c_tiles;
+                const long long st = rest % s_tiles, n = rest / s_tiles;
+                mbar_arrive_expect_tx(full0 + 8 * stage, Shape::kStageBytes);
+                tma_load_3d(base + stage * Shape::kStageBytes, &in_map, full0 + 8 * stage,
+                            static_cast<int>(st * kTmaPackPos), static_cast<int>(ct * Shape::kC),
+                            static_cast<int>(n));
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------ converters
+        // quarter-warp = 8 consecutive 8-position blocks of one 8-channel group
+        const int pb = (warp & 3) * 8 + (lane & 7);          // position block, 0..31
+        const int cg = (warp >> 2) * 4 + (lane >> 3);        // channel group, 0..15
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+            if (!pack_wait(full0 + 8 * stage, phase, abort_flag, status, wait_ns)) break;
+            const long long ct = t % c_tiles, rest = t / c_tiles;
+            const long long st = rest % s_tiles, n = rest / s_tiles;
+            const long long s0 = st * kTmaPackPos + pb * 8;
+            const unsigned char* tile = pack_smem + (base - raw) + stage * Shape::kStageBytes;
+            {
+                const long long c = ct * Shape::kC + cg * 8;
+                uint4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = *reinterpret_cast<const uint4*>(tile + (cg * 8 + k) * (kTmaPackPos * 2) +
+                                                            pb * 16);
+                if (c < C) {
+                    if (corr)
+                        pack_unit_store<FP8, true>(v, n, s0, c, C, S, out, scale, rscale);
+                    else
+                        pack_unit_store<FP8, false>(v, n, s0, c, C, S, out, scale, rscale);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag && warp == kTmaPackConvWarps && lane == 0) {
+        // boxes issued but never waited for land before the CTA leaves
+        for (long long i = issued > stages ? issued - stages : 0; i < issued; ++i) {
+            const uint32_t bar = full0 + 8 * static_cast<uint32_t>(i % stages);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(bar, static_cast<uint32_t>((i / stages) & 1)) &&
+                   clock64() - t0 < static_cast<long long>(kPackDrainCycles)) {
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- row repack
 // dst[r, 0:src_row_bytes) = src[r, :], dst[r, src_row_bytes:dst_row_bytes) = 0,
 // for two matrices in one launch (the point-output GEMM's A and B operands),
@@ -609,6 +825,44 @@ cudaError_t launch_amax_bf16(const void* in, long long n, unsigned int* amax_bit
     if (blocks < 1) blocks = 1;
     amax_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(in), n, amax_bits);
+    return cudaGetLastError();
+}
+
+int pack_tma_stages(int fp8, int smem_optin) {
+    const uint32_t sb = fp8 ? TmaPackShape<1>::kStageBytes : TmaPackShape<0>::kStageBytes;
+    const int fit = static_cast<int>((static_cast<long long>(smem_optin) - 1024 - 256) / sb);
+    return fit < 2 ? 0 : (fit > 8 ? 8 : fit);
+}
+
+cudaError_t launch_pack_tma(const CUtensorMap* in_map, long long N, long long C, long long S,
+                            void* out, int fp8, const unsigned int* amax_bits, float* scale_out,
+                            int num_sms, int smem_optin, int* status, unsigned long long wait_ns,
+                            cudaStream_t stream) {
+    const int stages = pack_tma_stages(fp8, smem_optin);
+    if (stages < 2 || C % 8 || S % 8) return cudaErrorInvalidValue;
+    const long long tc = fp8 ? TmaPackShape<1>::kC : TmaPackShape<0>::kC;
+    const long long c_tiles = (C + tc - 1) / tc;
+    const long long s_tiles = (S + kTmaPackPos - 1) / kTmaPackPos;
+    const long long tiles = N * c_tiles * s_tiles;
+    const long long grid = tiles < num_sms ? tiles : num_sms;
+    const uint32_t sb = fp8 ? TmaPackShape<1>::kStageBytes : TmaPackShape<0>::kStageBytes;
+    const size_t smem = 1024 + static_cast<size_t>(stages) * sb + 16u * stages + 16;
+    cudaError_t e;
+    if (fp8) {
+        e = cudaFuncSetAttribute(pack_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        pack_tma_kernel<1><<<static_cast<unsigned>(grid), kTmaPackThreads, smem, stream>>>(
+            *in_map, C, S, out, amax_bits, scale_out, c_tiles, s_tiles, tiles, stages, status,
+            wait_ns);
+    } else {
+        e = cudaFuncSetAttribute(pack_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        pack_tma_kernel<0><<<static_cast<unsigned>(grid), kTmaPackThreads, smem, stream>>>(
+            *in_map, C, S, out, amax_bits, scale_out, c_tiles, s_tiles, tiles, stages, status,
+            wait_ns);
+    }
     return cudaGetLastError();
 }
 

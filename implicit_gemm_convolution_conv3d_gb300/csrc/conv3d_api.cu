@@ -631,6 +631,32 @@ int encode_tiled(CUtensorMap* m, int fp8, int rank, const void* ptr, const cuuin
     return CONV_OK;
 }
 
+// The NCDHW -> NDHWC pack of x [N, C, S] (S = D*H*W): by the TMA-fed kernel
+// when C and S are multiples of 8 (the box rows need 16-byte pitches) and
+// its ring fits, else by the register-blocked / generic kernels (also when
+// the pack_lanes override asks for the register-blocked warp tile).
+cudaError_t pack_launch(const void* in, long long N, long long C, long long S, void* out, int fp8,
+                        const unsigned int* amax_bits, float* scale_out, const DeviceInfo* dev,
+                        cudaStream_t stream) {
+    const int lanes = overrides().pack_lanes;
+    if (C % 8 == 0 && S % 8 == 0 && lanes != 2 && lanes != 4 &&
+        pack_tma_stages(fp8, dev->smem_optin) >= 2 && load_entry_points() && N <= 0x7FFFFFFFll) {
+        CUtensorMap m;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(C),
+                                    static_cast<cuuint64_t>(N)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(S) * 2, static_cast<cuuint64_t>(C * S) * 2};
+        const cuuint32_t box[3] = {256, 128, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (g_encode_tiled(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(in), dims,
+                           str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            return launch_pack_tma(&m, N, C, S, out, fp8, amax_bits, scale_out, dev->num_sms,
+                                   dev->smem_optin, dev->status, g_wait_ns, stream);
+    }
+    return launch_pack(in, N, C, S, out, fp8, amax_bits, scale_out, dev->num_sms, stream);
+}
+
 // Output map for the TMA-store epilogue: [M, K] bf16 rows (or, for the
 // temporal class, [N*Do planes, H*W, K] so stores clip at each plane's edge),
 // 32x32 boxes with the 64-byte swizzle the epilogue writes.
@@ -1317,8 +1343,7 @@ int ncdhw_via_copy(const Geo& g, const Plan& P, DeviceInfo* dev, const void* x, 
     KParams k;
     fill_params(g, P, xc, w, out, workspace, scale_x, scale_w, bias, dev->status, &k);
     k.act = act;
-    cudaError_t e = launch_pack(x, g.N, g.C, g.D * g.H * g.W, xc, 0, nullptr, nullptr,
-                                dev->num_sms, stream);
+    cudaError_t e = pack_launch(x, g.N, g.C, g.D * g.H * g.W, xc, 0, nullptr, nullptr, dev, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     if ((e = launch_units(P, tm, k, stream)) != cudaSuccess)
         return cuda_fail(e, "conv kernel launch");
@@ -1626,8 +1651,7 @@ int pack_ncdhw_bf16_to_ndhwc(const void* in, const int64_t dims[5], void* out,
     int rc = device_info(&dev);
     if (rc) return rc;
     const long long S = dims[2] * dims[3] * dims[4];
-    cudaError_t e = launch_pack(in, dims[0], dims[1], S, out, 0, nullptr, nullptr, dev->num_sms,
-                                stream);
+    cudaError_t e = pack_launch(in, dims[0], dims[1], S, out, 0, nullptr, nullptr, dev, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return CONV_OK;
 }
@@ -1665,7 +1689,7 @@ int pack_ncdhw_bf16_to_ndhwc_fp8(const void* in, const int64_t dims[5], void* ou
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     e = launch_amax_bf16(in, n, amax, dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-    e = launch_pack(in, dims[0], dims[1], S, out, 1, amax, scale_out, dev->num_sms, stream);
+    e = pack_launch(in, dims[0], dims[1], S, out, 1, amax, scale_out, dev, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return CONV_OK;
 }

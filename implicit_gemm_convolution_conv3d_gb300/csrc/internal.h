@@ -167,6 +167,15 @@ cudaError_t launch_pack(const void* in, long long N, long long C, long long S, v
                         int fp8, const unsigned int* amax_bits, float* scale_out, int num_sms,
                         cudaStream_t stream);
 
+// TMA-fed pack (C % 8 == 0, S % 8 == 0): in_map is the bf16 input as a 3-D
+// tensor {S, C, N} with a box of {256, 128, 1} and no swizzle.  pack_tma_stages gives the shared-memory ring depth for the
+// device's per-block limit (0: the kernel does not fit).
+int pack_tma_stages(int fp8, int smem_optin);
+cudaError_t launch_pack_tma(const CUtensorMap* in_map, long long N, long long C, long long S,
+                            void* out, int fp8, const unsigned int* amax_bits, float* scale_out,
+                            int num_sms, int smem_optin, int* status, unsigned long long wait_ns,
+                            cudaStream_t stream);
+
 int* device_status_ptr();   // device address of the status word (current device)
 
 // The process's plan / path overrides (conv_set_overrides), copied under a

@@ -76,6 +76,72 @@ def test_pack_fp8_codec_exhaustive(pkg, amax):
     assert np.array_equal(bytes8(q), ref_q)
 
 
+@pytest.mark.parametrize("amax", [448.0, 3.0, 1e-3, 2.0 ** -7, 1.7e38])
+def test_pack_fp8_codec_exhaustive_both_kernels(pkg, amax):
+    """The same exhaustive patterns in a 128-channel tensor whose position
+    count is a multiple of 8: the TMA-fed pack and the register-blocked pack
+    (the pack_lanes override) each equal the oracle byte for byte."""
+    pats = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = pats[np.isfinite(pats) & (np.abs(pats) <= np.float32(amax))]
+    amax_bf16 = np.float32(torch.tensor(amax).to(torch.bfloat16).float().item())
+    vals = np.concatenate([vals, np.array([amax_bf16, -amax_bf16], dtype=np.float32)])
+    C = 128
+    S = (vals.size + C - 1) // C
+    S = (S + 7) // 8 * 8
+    flat = np.zeros(S * C, dtype=np.float32)
+    flat[:vals.size] = np.random.default_rng(5).permutation(vals)
+    xb = torch.from_numpy(flat).to(torch.bfloat16).view(1, C, 1, 1, S).cuda()
+    ref_q, ref_s = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(xb))
+    for lanes in (None, 2):
+        with pkg.overrides(pack_lanes=lanes):
+            q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb)
+            torch.cuda.synchronize()
+        assert np.float32(s.item()).tobytes() == np.float32(ref_s).tobytes()
+        assert np.array_equal(bytes8(q), ref_q), f"pack_lanes={lanes}"
+
+
+_AMAX_SWEEP = [float(v) for v in np.exp(np.random.default_rng(41).uniform(np.log(1e-30),
+                                                                          np.log(1e30), 40))]
+
+
+@pytest.mark.parametrize("amax", _AMAX_SWEEP, ids=[f"{a:.3g}" for a in _AMAX_SWEEP])
+def test_pack_fp8_codec_many_scales(pkg, amax):
+    """Every finite bf16 pattern up to amax, for 40 seeded amax values over 60
+    decades: the default (TMA-fed) pack's codes, whatever quotient it uses,
+    equal the oracle's division byte for byte."""
+    pats = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    amax_bf16 = np.float32(torch.tensor(amax).to(torch.bfloat16).float().item())
+    vals = pats[np.isfinite(pats) & (np.abs(pats) <= amax_bf16)]
+    vals = np.concatenate([vals, np.array([amax_bf16, -amax_bf16], dtype=np.float32)])
+    C = 64
+    S = ((vals.size + C - 1) // C + 7) // 8 * 8
+    flat = np.zeros(S * C, dtype=np.float32)
+    flat[:vals.size] = vals
+    xb = torch.from_numpy(flat).to(torch.bfloat16).view(1, C, 1, 1, S).cuda()
+    q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb)
+    torch.cuda.synchronize()
+    ref_q, ref_s = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(xb))
+    assert np.float32(s.item()).tobytes() == np.float32(ref_s).tobytes()
+    assert np.array_equal(bytes8(q), ref_q)
+
+
+@pytest.mark.parametrize("shape", [(2, 200, 3, 17, 24), (1, 1024, 3, 40, 90), (3, 8, 1, 1, 8),
+                                   (1, 136, 2, 1, 260)])
+def test_pack_tma_partial_tiles(pkg, shape):
+    """Tensors whose channels and positions leave partial TMA tiles (200 of 128
+    / 64 channels, 1224 of 256 positions, one 8-channel tile, 520 positions):
+    both packs equal the oracle."""
+    x = cw.randn_bf16(shape, 302, 2.0, "cuda")
+    ref_b = oracle.pack_ncdhw_to_ndhwc_bf16(bits16(x))
+    ref_q, ref_s = oracle.pack_ncdhw_to_ndhwc_fp8(bits16(x))
+    y = pkg.pack_ncdhw_bf16_to_ndhwc(x)
+    q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(y), ref_b)
+    assert np.float32(s.item()).tobytes() == np.float32(ref_s).tobytes()
+    assert np.array_equal(bytes8(q), ref_q)
+
+
 def test_pack_fp8_all_zero_tensor(pkg):
     x = torch.zeros((1, 32, 2, 2, 2), dtype=torch.bfloat16, device="cuda")
     q, s = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(x)

@@ -89,6 +89,34 @@ def test_video_conv3d_sampled(pkg):
     _check_sampled(y, bits16(x), bits16(w), idx, wl)
 
 
+def test_video_conv3d_from_host_full_size(pkg):
+    """The measured end-to-end path at the headline size: conv_fwd_from_host
+    with its default slicing (whole-wave slices, the first split over weight
+    groups) from pinned host operands equals conv_fwd bit for bit over the
+    whole output, and the oracle on >= 1M sampled outputs."""
+    wl = cw.BY_NAME["video_conv3d_bf16"]
+    x, w = cw.make_inputs(wl, "cuda")
+    y = pkg.conv_fwd(x, w, wl.stride, wl.pad, wl.dil)
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    wh = torch.empty(w.shape, dtype=w.dtype, pin_memory=True)
+    xh.copy_(x)
+    wh.copy_(w)
+    hout = torch.empty(y.shape, dtype=torch.bfloat16, pin_memory=True)
+    hout.fill_(float("nan"))
+    xd, wd = torch.empty_like(x), torch.empty_like(w)
+    outd = torch.full(y.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkg.conv_fwd_from_host(xh, wh, wl.stride, wl.pad, wl.dil, out_host=hout, x_dev=xd,
+                           w_dev=wd, out_dev=outd)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    assert torch.equal(hout.view(torch.int16), y.cpu().view(torch.int16))
+    plan = pkg.conv_fwd_plan(wl.x_shape, wl.w_shape, wl.stride, wl.pad, wl.dil)
+    idx = _sample(tuple(y.shape), wl, plan["tile_n"])
+    got = hout.view(-1)[torch.from_numpy(idx)].float().double().numpy()
+    ref = oracle.conv3d_points(bits16(x), bits16(w), idx, wl.stride, wl.pad, wl.dil)
+    assert_close(got, ref, "video_conv3d_bf16 from host")
+
+
 def test_fp8_workload_pack_exact_and_conv_sampled(pkg):
     wl = cw.BY_NAME["fp8_conv3d_1x3x3"]
     x, w = cw.make_inputs(wl, "cuda")          # bf16 NCDHW, bf16 KCTRS
