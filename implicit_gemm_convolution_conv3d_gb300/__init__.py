@@ -126,6 +126,12 @@ def load_library(path: str = LIB_PATH):
         lib.pack_fp8_workspace_size.restype = ctypes.c_size_t
         lib.pack_ncdhw_bf16_to_ndhwc_fp8.argtypes = [vp, i64p, vp, vp, vp, ctypes.c_size_t, vp]
         lib.pack_ncdhw_bf16_to_ndhwc_fp8.restype = ctypes.c_int
+        lib.conv_fwd_ncdhw_fp8.argtypes = [vp, i64p, vp, i64p, i32p, i32p, i32p, vp, vp, vp, vp,
+                                           vp, ctypes.c_size_t, vp]
+        lib.conv_fwd_ncdhw_fp8.restype = ctypes.c_int
+        lib.conv_fwd_ncdhw_fp8_workspace_size.argtypes = [i64p, i64p, i32p, i32p, i32p,
+                                                          ctypes.POINTER(ctypes.c_size_t)]
+        lib.conv_fwd_ncdhw_fp8_workspace_size.restype = ctypes.c_int
         lib.conv_fwd_workspace_size.argtypes = [i64p, i64p, i32p, i32p, i32p, ctypes.c_int]
         lib.conv_fwd_workspace_size.restype = ctypes.c_size_t
         lib.conv_get_device_status_stream.argtypes = [vp, i32p]
@@ -421,6 +427,59 @@ def conv_fwd_ncdhw(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
     return out
 
 
+def conv_fwd_ncdhw_fp8_workspace_size(x_shape, w_shape, stride=1, pad=0, dil=1) -> int:
+    """Preferred workspace bytes of conv_fwd_ncdhw_fp8 (x_shape = N, C, D, H, W)."""
+    lib = load_library()
+    b = ctypes.c_size_t(0)
+    _check(lib.conv_fwd_ncdhw_fp8_workspace_size(
+        _I64_5(*x_shape), _I64_5(*w_shape), _I32_3(*_triple(stride)), _I32_3(*_triple(pad)),
+        _I32_3(*_triple(dil)), ctypes.byref(b)), "conv_fwd_ncdhw_fp8_workspace_size")
+    return int(b.value)
+
+
+def conv_fwd_ncdhw_fp8(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
+                       scale_w: Optional[torch.Tensor] = None,
+                       scale_x: Optional[torch.Tensor] = None,
+                       bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """e4m3 conv of a bf16 channel-major activation quantised while it is
+    loaded: x NCDHW [N,C,D,H,W] bf16, w e4m3 KTRSC [K,1,R,S,C] with its fp32
+    scale -> (out NDHWC [N,D,H,W,K] bf16, scale_x fp32[1] = amax(x)/448)."""
+    lib = load_library()
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError("x must be [N,C,D,H,W] and w [K,T,R,S,C]")
+    if x.dtype != torch.bfloat16 or w.dtype != torch.float8_e4m3fn:
+        raise TypeError("conv_fwd_ncdhw_fp8 takes bf16 x and float8_e4m3fn w")
+    for s in (scale_w, scale_x):
+        if s is not None and (s.dtype != torch.float32 or s.numel() < 1):
+            raise TypeError("scales must be float32 device tensors")
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (w.shape[0],)):
+        raise TypeError("bias must be a float32 device tensor of shape [K]")
+    _require_cuda(x, w, scale_w, scale_x, bias, out, workspace)
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    n, c, d, h, wd = (int(v) for v in x.shape)
+    od = conv_out_dims((n, d, h, wd, c), tuple(w.shape), st, pa, di)
+    if out is None:
+        out = torch.empty(od, dtype=torch.bfloat16, device=x.device)
+    elif tuple(out.shape) != od or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 {od}")
+    if scale_x is None:
+        scale_x = torch.empty(1, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(conv_fwd_ncdhw_fp8_workspace_size(tuple(x.shape), tuple(w.shape),
+                                                                  st, pa, di),
+                                dtype=torch.uint8, device=x.device)
+    rc = lib.conv_fwd_ncdhw_fp8(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
+                                _I32_3(*st), _I32_3(*pa), _I32_3(*di), _ptr(scale_w),
+                                scale_x.data_ptr(), _ptr(bias), out.data_ptr(),
+                                workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    _check(rc, "conv_fwd_ncdhw_fp8")
+    return out, scale_x
+
+
 def conv_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
                      scale_x: Optional[torch.Tensor] = None,
                      scale_w: Optional[torch.Tensor] = None, out: torch.Tensor = None,
@@ -632,5 +691,5 @@ __all__ = [
     "conv_fwd_from_host", "conv_fwd_kernel_launches", "conv_fwd_ncdhw",
     "conv_fwd_ncdhw_plan", "conv_bwd_point_workspace_bytes", "conv_bwd_data_point",
     "conv_bwd_weight_point", "conv_fwd_workspace_size", "conv_get_device_status_stream",
-    "set_overrides", "overrides",
+    "set_overrides", "overrides", "conv_fwd_ncdhw_fp8", "conv_fwd_ncdhw_fp8_workspace_size",
 ]

@@ -21,8 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libconv3d.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["conv_igemm.cu", "aux_kernels.cu", "conv3d_api.cu", "conv_noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "tile_table.h"]
+SOURCES = ["conv_igemm.cu", "aux_kernels.cu", "conv3d_api.cu", "conv_noalloc.cu", "conv_fused_q.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "tile_table.h", "kernel_common.cuh"]
 
 
 def nvcc_path() -> str:

@@ -10,6 +10,7 @@
 
 
 #include "internal.h"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace c3d {
@@ -110,10 +111,6 @@ constexpr int kPackC = 64;
 constexpr int kPackS = 64;
 constexpr int kPitch = kPackS + 2;   // bf16 elements per smem row (33 words: no bank conflicts)
 
-__device__ __forceinline__ float fp8_scale_of(const unsigned int* amax_bits) {
-    const float amax = __uint_as_float(*amax_bits);
-    return amax == 0.0f ? 1.0f : amax / 448.0f;   // IEEE division (no fast-math)
-}
 
 template <int FP8>
 __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restrict__ in,
@@ -348,28 +345,6 @@ __device__ __noinline__ bool pack_wait(uint32_t bar, uint32_t parity, volatile u
     return true;
 }
 
-// x / scale correctly rounded, from y = 1/scale correctly rounded (computed
-// once): q0 = x*y, r = x - scale*q0 (exact by one FMA), q = q0 + r*y rounded
-// once.  This is the FMA correction step of Markstein's division scheme
-// (P. Markstein, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Develop. 34(1), 1990): with y the
-// correctly rounded reciprocal it returns the correctly rounded quotient
-// while no intermediate underflows.  Three instructions where an IEEE
-// division takes about three times as many; the pack uses it for scales of
-// at least 2^-60 whose significand is not all ones (quotients that matter
-// for e4m3 then keep every intermediate far from underflow) and divides
-// otherwise.  It runs on |x| and puts x's sign back: for x = -0 the FMAs'
-// exact zero sums would give +0 where the division gives -0 (another e4m3
-// code).  The exhaustive codec tests compare its codes with the oracle's
-// division for every bf16 pattern.
-__device__ __forceinline__ float quot_corrected(float x, float scale, float y) {
-    const float xa = fabsf(x);
-    const float q0 = __fmul_rn(xa, y);
-    const float r = __fmaf_rn(-scale, q0, xa);
-    const float q = __fmaf_rn(r, y, q0);
-    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
-}
-
 // One converter unit of the TMA-fed pack: 8 channel rows x 8 positions of the
 // tile in shared memory (v: row k's 8 positions) to 8 output positions.
 template <int FP8, bool CORR>
@@ -396,13 +371,9 @@ __device__ __forceinline__ void pack_unit_store(const uint4 (&v)[8], long long n
                 uint32_t b = 0;
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
-                    const float x0 = __uint_as_float(w[4 * h + e] << 16);
-                    const float x1 = __uint_as_float(w[4 * h + e + 1] << 16);
-                    const float a0 = CORR ? quot_corrected(x0, scale, rscale) : x0 / scale;
-                    const float a1 = CORR ? quot_corrected(x1, scale, rscale) : x1 / scale;
-                    const __nv_fp8x2_storage_t q2 =
-                        __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
-                    b |= static_cast<uint32_t>(q2) << (8 * e);
+                    b |= quant_e4m3x2<CORR>(__uint_as_float(w[4 * h + e] << 16),
+                                            __uint_as_float(w[4 * h + e + 1] << 16), scale,
+                                            rscale) << (8 * e);
                 }
                 q[h] = b;
             }
@@ -447,8 +418,7 @@ __global__ void __launch_bounds__(kTmaPackThreads, 1)
     if (FP8) {
         scale = fp8_scale_of(amax_bits);
         rscale = __frcp_rn(scale);
-        corr = scale >= 8.6736174e-19f &&   // 2^-60
-               (__float_as_uint(scale) & 0x7FFFFFu) != 0x7FFFFFu;
+        corr = quot_corrected_ok(scale);
         if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = scale;
     }
     __syncthreads();   // the barriers are initialised before any thread uses them

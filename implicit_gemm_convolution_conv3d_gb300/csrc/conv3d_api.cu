@@ -1455,6 +1455,91 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
 
 }  // namespace
 
+namespace {
+
+// Workspace bytes before the kept strips of conv_fwd_ncdhw_fp8 (the amax word).
+constexpr size_t kFqScratchOffset = 256;
+
+struct FqPlan {
+    FQParams p;       // geometry, tiles and shared-memory layout (pointers unset)
+    int grid;
+    size_t smem;
+    size_t keep_bytes;   // scratch for the kept strips: grid x chunks x strip bytes
+};
+
+// The plan of conv_fwd_ncdhw_fp8: per-frame "same" filters, CTA pairs when
+// the problem has two waves of 256-row units, and the strip and weight ring
+// within the shared-memory budget.
+int fq_plan(const Geo& g, const DeviceInfo* dev, FqPlan* fp) {
+    // per-frame filters with "same" padding in H and W, unit stride and dilation
+    if (g.T != 1 || g.pd != 0 || g.sd != 1 || g.sh != 1 || g.sw != 1 || g.dd != 1 || g.dh != 1 ||
+        g.dw != 1 || g.R % 2 == 0 || g.S % 2 == 0 || g.ph != (g.R - 1) / 2 ||
+        g.pw != (g.S - 1) / 2) {
+        set_error("fused channel-major e4m3 conv: T = 1, odd R and S with pad (0, (R-1)/2, "
+                  "(S-1)/2), unit stride and dilation");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    if (g.C % 16 != 0) {
+        set_error("fused channel-major e4m3 conv: C must be a multiple of 16");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    if (g.H * (g.W + 2 * g.pw) > 0x3FFFFFFFll || g.N * g.D > 0x7FFFFFFFll) {
+        set_error("fused channel-major e4m3 conv: frame or frame count too large");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    const Overrides ov = overrides();
+    FQParams& p = fp->p;
+    std::memset(&p, 0, sizeof p);
+    p.N = static_cast<int>(g.N); p.C = static_cast<int>(g.C); p.D = static_cast<int>(g.D);
+    p.H = static_cast<int>(g.H); p.W = static_cast<int>(g.W); p.K = static_cast<int>(g.K);
+    p.R = static_cast<int>(g.R); p.S = static_cast<int>(g.S);
+    p.ph = g.ph; p.pw = g.pw;
+    p.Wp = p.W + 2 * p.pw;
+    p.HWp = p.H * p.Wp;
+    p.BN = ov.tile_n > 0 ? ov.tile_n : pick_bn(g.K);
+    p.n_tiles = static_cast<int>((g.K + p.BN - 1) / p.BN);
+    p.chunks = static_cast<int>((g.C + 127) / 128);
+    const long long mt_pair = (p.HWp + 255) / 256;
+    int pair = (g.N * g.D * mt_pair * p.n_tiles >= 2LL * dev->num_sms && dev->num_sms % 2 == 0) ? 1 : 0;
+    if (ov.pair >= 0) pair = (ov.pair && dev->num_sms % 2 == 0) ? 1 : 0;
+    p.pair = pair;
+    p.mt_frame = (p.HWp + (128 << pair) - 1) / (128 << pair);
+    const long long m_tiles = g.N * g.D * p.mt_frame;
+    if (m_tiles * p.n_tiles > 0x7FFFFFFFll) {
+        set_error("too many work units");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p.m_tiles = static_cast<int>(m_tiles);
+    // the strip: this CTA's 128 rows plus the taps' reach on both sides
+    const long long reach = static_cast<long long>(p.ph) * p.Wp + p.pw;
+    p.L = static_cast<int>((128 + 2 * reach + 31) / 32 * 32);
+    p.strip_bytes = static_cast<uint32_t>(8 * p.L * 16);
+    p.b_stage_bytes = static_cast<uint32_t>((p.BN >> pair) * 128);
+    const size_t strips = (2 * static_cast<size_t>(p.strip_bytes) + 1023) / 1024 * 1024;
+    const size_t fixed = 1024 + strips + 96 + 64;
+    if (static_cast<size_t>(dev->smem_optin) < fixed + 2 * (p.b_stage_bytes + 16)) {
+        set_error("fused channel-major e4m3 conv: the filter's strip does not fit in shared "
+                  "memory (frame too wide for the filter height)");
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p.b_stages = static_cast<int>(std::min<size_t>(
+        8, (static_cast<size_t>(dev->smem_optin) - fixed) / (p.b_stage_bytes + 16)));
+    if (ov.stages > 0) p.b_stages = std::max(2, std::min(p.b_stages, ov.stages));
+    fp->smem = fixed + static_cast<size_t>(p.b_stages) * (p.b_stage_bytes + 16);
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(2 * p.BN)) cols <<= 1;
+    p.tmem_cols = cols;
+    p.idesc = make_idesc(1, p.BN, 128 << pair);
+    // persistent CTAs (pairs) take whole m-tiles: every column tile in turn
+    fp->grid = pair ? 2 * static_cast<int>(std::min<long long>(m_tiles, dev->num_sms / 2))
+                    : static_cast<int>(std::min<long long>(m_tiles, dev->num_sms));
+    p.scratch_stride = static_cast<long long>(p.chunks) * p.strip_bytes;
+    fp->keep_bytes = static_cast<size_t>(fp->grid) * static_cast<size_t>(p.scratch_stride);
+    return CONV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* w_host,
@@ -1822,6 +1907,101 @@ size_t conv_fwd_workspace_size(const int64_t x_dims[5], const int64_t w_dims[5],
                       nullptr, nullptr, nullptr, &bytes) != CONV_OK)
         return 0;
     return bytes;
+}
+
+int conv_fwd_ncdhw_fp8_workspace_size(const int64_t x_dims[5], const int64_t w_dims[5],
+                                      const int stride[3], const int pad[3], const int dil[3],
+                                      size_t* bytes) {
+    if (!x_dims || !bytes) {
+        set_error("null argument");
+        return CONV_ERR_INVALID;
+    }
+    int64_t xd[5];
+    ndhwc_dims(x_dims, xd);
+    Geo g;
+    int rc = make_geo(xd, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    FqPlan fp;
+    if ((rc = fq_plan(g, dev, &fp))) return rc;
+    *bytes = kFqScratchOffset + (fp.p.n_tiles > 1 ? fp.keep_bytes : 0);
+    return CONV_OK;
+}
+
+int conv_fwd_ncdhw_fp8(const void* x, const int64_t x_dims[5], const void* w,
+                       const int64_t w_dims[5], const int stride[3], const int pad[3],
+                       const int dil[3], const float* scale_w, float* scale_x_out,
+                       const float* bias, void* out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+    if (!x_dims) {
+        set_error("null shape argument");
+        return CONV_ERR_INVALID;
+    }
+    int64_t xd[5];
+    ndhwc_dims(x_dims, xd);
+    Geo g;
+    int rc = make_geo(xd, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!x || !w || !out || !workspace) {
+        set_error("null tensor or workspace pointer");
+        return CONV_ERR_INVALID;
+    }
+    if (workspace_bytes < pack_fp8_workspace_size()) {
+        set_error("workspace smaller than pack_fp8_workspace_size()");
+        return CONV_ERR_INVALID;
+    }
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned16(workspace) ||
+        (scale_w && (reinterpret_cast<uintptr_t>(scale_w) & 3u)) ||
+        (scale_x_out && (reinterpret_cast<uintptr_t>(scale_x_out) & 3u)) ||
+        (bias && (reinterpret_cast<uintptr_t>(bias) & 3u))) {
+        set_error("device pointers must be 16-byte aligned");
+        return CONV_ERR_INVALID;
+    }
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    if (!load_entry_points()) {
+        set_error("cuTensorMapEncode* entry points unavailable");
+        return CONV_ERR_CUDA;
+    }
+    FqPlan fp;
+    if ((rc = fq_plan(g, dev, &fp))) return rc;
+    FQParams& p = fp.p;
+    unsigned int* amax = static_cast<unsigned int*>(workspace);
+    // the strips a CTA converts for an m-tile's first column tile are kept for
+    // the others in the workspace after the amax word, when it has room
+    if (p.n_tiles > 1 && workspace_bytes >= kFqScratchOffset + fp.keep_bytes)
+        p.scratch = static_cast<unsigned char*>(workspace) + kFqScratchOffset;
+    p.x = static_cast<const unsigned short*>(x);
+    p.amax_bits = amax;
+    p.scale_x_out = scale_x_out;
+    p.scale_w = scale_w;
+    p.bias = bias;
+    p.out = out;
+    p.status = dev->status;
+    p.wait_ns = g_wait_ns;
+    // the e4m3 weight [K, R*S, C] as {C, R*S, K}: boxes of 128 channel bytes x
+    // one tap x (BN >> pair) filters, 128-byte swizzle
+    CUtensorMap wm;
+    {
+        const cuuint64_t taps = static_cast<cuuint64_t>(g.R * g.S);
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C), taps, static_cast<cuuint64_t>(g.K)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(g.C), static_cast<cuuint64_t>(g.C) * taps};
+        const cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(p.BN >> p.pair)};
+        if ((rc = encode_tiled(&wm, 1, 3, w, dims, str, box, 128))) return rc;
+    }
+    if (overrides().log == 1)
+        std::fprintf(stderr, "conv_fwd_ncdhw_fp8: BN=%d pair=%d L=%d strip=%u b_stages=%d "
+                     "m_tiles=%d n_tiles=%d chunks=%d grid=%d smem=%zu keep=%d\n", p.BN, p.pair,
+                     p.L, p.strip_bytes, p.b_stages, p.m_tiles, p.n_tiles, p.chunks, fp.grid,
+                     fp.smem, p.scratch ? 1 : 0);
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    e = launch_amax_bf16(x, g.N * g.C * g.D * g.H * g.W, amax, dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "amax launch");
+    e = launch_fused_q(&wm, p, fp.grid, fp.smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused conv launch");
+    return CONV_OK;
 }
 
 int conv_get_device_status_stream(cudaStream_t stream, int* device_status) {

@@ -31,14 +31,13 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace c3d {
 
 namespace {
 
-constexpr int kStatusTimeout = 4;
-constexpr unsigned long long kDrainNs = 1000000000ull;
 
 struct Unit {
     int m_tile, n_tile, split;
@@ -87,40 +86,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     return r;
 }
 
-// The bound is counted in SM clock cycles (clock64 is a cheap SM-local
-// register; the global nanosecond timer is far slower to read and would sit on
-// every producer / MMA / epilogue hand-off).  Two cycles per nanosecond is the
-// SM clock's upper end, so at any lower clock the wall-clock bound only grows.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                       int* status, unsigned long long limit_ns) {
-    const long long t0 = clock64();
-    const long long limit_cycles = static_cast<long long>(limit_ns > (1ull << 61) ? (1ull << 61) : limit_ns) * 2;
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > limit_cycles) {
-            *abort_flag = 1u;
-            atomicExch(status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-// Bounded wait on phase `parity` of an mbarrier; false on timeout or abort.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         int* status, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, abort_flag, status, limit_ns);
-}
-
-// Cleanup wait: bounded by a fixed limit, ignores the abort flag.
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kDrainNs) return;
-    }
-}
-
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
     uint2 r;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr) : "memory");
@@ -132,37 +97,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Store 32 accumulator columns of one output row (bf16): v * scale + bias
-// (bias: the 32 columns' entries, or NULL).
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
-                                               float scale, const float* bias, int count,
-                                               bool vec_ok) {
-    auto val = [&](int i) {
-        return __uint_as_float(v[i]) * scale + (bias ? __ldg(bias + i) : 0.0f);
-    };
-    if (count == 32 && vec_ok) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 o;
-            o.x = pack_bf16x2(val(8 * i + 0), val(8 * i + 1));
-            o.y = pack_bf16x2(val(8 * i + 2), val(8 * i + 3));
-            o.z = pack_bf16x2(val(8 * i + 4), val(8 * i + 5));
-            o.w = pack_bf16x2(val(8 * i + 6), val(8 * i + 7));
-            d4[i] = o;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < count) dst[i] = __float2bfloat16_rn(val(i));
-    }
 }
 
 // The same with an activation after the bias: act(v * scale + bias).  Plans

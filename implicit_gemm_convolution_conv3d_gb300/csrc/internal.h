@@ -126,6 +126,45 @@ struct TMaps {
     CUtensorMap a[2], b[2], c[2];
 };
 
+// Parameters of the fused channel-major e4m3 convolution (conv_fused_q.cu):
+// bf16 x NCDHW read in place and quantised while the A operand is built.
+// Output rows are enumerated in padded-row coordinates: per (n, d) frame,
+// P = h * Wp + wp with Wp = W + 2*pw, image column w = wp - pw (rows with
+// wp outside [pw, pw + W) are computed and dropped).  Each CTA's 128 rows
+// read a strip of L padded positions around them; tap (r, s) is the strip
+// shifted by r*Wp + s positions.
+struct FQParams {
+    int N, C, D, H, W, K, R, S, ph, pw;
+    int Wp, HWp;          // padded row length, padded positions per frame
+    int mt_frame;         // m-tiles per frame (128 << pair rows each)
+    int m_tiles, n_tiles; // m_tiles = N * D * mt_frame
+    int chunks;           // ceil(C / 128): 128-channel reduction chunks
+    int BN;               // tile columns (multiple of 32, <= 256)
+    int b_stages;         // weight ring depth
+    int L;                // strip positions per CTA (multiple of 32)
+    uint32_t strip_bytes; // 8 slices x L x 16 bytes
+    uint32_t b_stage_bytes;
+    uint32_t idesc;       // tcgen05 instruction descriptor (e4m3 x e4m3, M, N)
+    uint32_t tmem_cols;
+    int pair;
+    unsigned char* scratch;        // per-CTA converted strips (blockIdx.x * scratch_stride), or NULL
+    long long scratch_stride;      // chunks * strip_bytes
+    const unsigned short* x;       // bf16 NCDHW
+    const unsigned int* amax_bits; // max |x| as binary32 bits (computed before)
+    float* scale_x_out;            // receives amax / 448 (or NULL)
+    const float* scale_w;
+    const float* bias;
+    void* out;                     // bf16 NDHWC
+    int* status;
+    unsigned long long wait_ns;
+};
+constexpr int kFqThreads = 448;   // warp 0 weights (TMA), 1 MMA, 2-5 epilogue, 6-13 converters
+
+// Launch the fused channel-major e4m3 convolution (w_map: the e4m3 KTRSC
+// weight as {C, R*S, K} with boxes {128, 1, BN >> pair}, 128-byte swizzle).
+cudaError_t launch_fused_q(const CUtensorMap* w_map, const FQParams& p, int grid, size_t smem,
+                           cudaStream_t stream);
+
 // Launch the implicit-GEMM kernel (AMODE x dtype) on grid/smem from the plan.
 cudaError_t launch_igemm(int amode, int fp8, const TMaps* maps, const KParams& p, int grid,
                          size_t smem, cudaStream_t stream);

@@ -191,6 +191,31 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 
 
+// non-tensor bulk copies (addresses 16-byte aligned, bytes a multiple of 16):
+// global -> this CTA's shared memory, completion counted on an mbarrier
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// shared -> global, in the thread's bulk async-group (bulk_commit, then
+// bulk_wait_read / bulk_wait_done)
+__device__ __forceinline__ void bulk_store_1d(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// wait until at most N committed bulk groups are still pending (writes done)
+template <int N>
+__device__ __forceinline__ void bulk_wait_done() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // bulk prefetch of [src, src+bytes) into L2 (src and bytes multiples of 16)
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -211,6 +211,49 @@ int conv_fwd_ncdhw(const void* x, const int64_t x_dims[5], const void* w, const 
                    const float* scale_x, const float* scale_w, const float* bias, void* out,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* e4m3 forward convolution of a bf16 channel-major (NCDHW) activation, the
+ * activation quantised while the kernel loads it -- no NCDHW -> NDHWC pack
+ * pass and no packed copy:
+ *   amax   = max |x| over the whole tensor (one read-only pass first)
+ *   scale  = amax / 448 (1.0 if amax == 0), written to *scale_x_out
+ *   q[n,c,d,h,w] = e4m3_satfinite_rn( fp32(x[n,c,d,h,w]) / scale )
+ *   out[n,d,h,w,k] = bf16_rn( scale * scale_w *
+ *       sum_{r,s,c} q[n, c, d, h+r-ph, w+s-pw] * w[k,0,r,s,c] + bias[k] )
+ * so the result is conv_fwd_bias of pack_ncdhw_bf16_to_ndhwc_fp8(x) (the
+ * same codes and scale) up to the fp32 summation order.
+ *   x          device, bf16 NCDHW [N,C,D,H,W]; x_dims = {N, C, D, H, W}
+ *   w          device, e4m3 KTRSC [K,1,R,S,C] (pack_ncdhw_bf16_to_ndhwc_fp8
+ *              of the bf16 KCTRS weight, which also gives scale_w)
+ *   scale_w    device fp32 or NULL (1.0); scale_x_out device fp32 or NULL
+ *   bias       device fp32 [K] or NULL
+ *   out        device, bf16 NDHWC [N,D,H,W,K]; fully overwritten
+ *   workspace  device, >= pack_fp8_workspace_size() bytes (the amax word);
+ *              with conv_fwd_ncdhw_fp8_workspace_size() bytes the converted
+ *              strips are kept for the other column tiles (faster; same result)
+ * Coverage: T = 1, odd R and S with pad = (0, (R-1)/2, (S-1)/2), unit
+ * stride and dilation, C % 16 == 0; anything else CONV_ERR_UNSUPPORTED.
+ * Each CTA converts, per 128-channel chunk, a strip of its output rows plus
+ * the filter's reach into e4m3 in shared memory once; every tap reads the
+ * strip in place, shifted.  A CTA (pair) computes all column tiles of an
+ * m-tile in turn; with room in the workspace, the strips converted for the
+ * first column tile are copied out (bulk copies, L2-resident) and copied
+ * back for the others instead of being converted again.  Defined by: FlyDSL PR #860, the 3x1x1 unfold
+ * revert commit (a kernel reading NCDHW straight into the GEMM, without
+ * materialising A, left to future work) and the tiled bf16 -> fp8 pack
+ * commit (the quantisation it folds in). */
+int conv_fwd_ncdhw_fp8(const void* x, const int64_t x_dims[5], const void* w,
+                       const int64_t w_dims[5], const int stride[3], const int pad[3],
+                       const int dil[3], const float* scale_w, float* scale_x_out,
+                       const float* bias, void* out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Preferred workspace bytes of conv_fwd_ncdhw_fp8 for this problem on the
+ * current device (the amax word plus the kept strips: CTAs x 128-channel
+ * chunks x strip bytes).  Returns CONV_ERR_UNSUPPORTED when the conv would. */
+int conv_fwd_ncdhw_fp8_workspace_size(const int64_t x_dims[5], const int64_t w_dims[5],
+                                      const int stride[3], const int pad[3], const int dil[3],
+                                      size_t* bytes);
+
 /* conv_fwd_plan for conv_fwd_ncdhw (x_dims = {N, C, D, H, W}); the class is
  * always CONV_CLASS_TEMPORAL.  Host-only when num_sms > 0. */
 int conv_fwd_ncdhw_plan(const int64_t x_dims[5], const int64_t w_dims[5], const int stride[3],
