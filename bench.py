@@ -303,6 +303,23 @@ def run_workload(pkg, wl, device, steps, warmup, flush, with_e2e=True, with_bias
             pkg.pack_ncdhw_bf16_to_ndhwc_fp8(xb, out=ops["x"], scale=ops["sx"], workspace=pk_ws)
         res["ms_pack"] = Timer(steps, flush).run(pack_only)
         res["pack_bytes"] = xb.numel() * 2 * 2 + xb.numel()   # amax read, pack read, fp8 write
+        # the activation quantised while the conv loads it (amax pass + one
+        # kernel, no pack pass), for T = 1 "same" filters
+        try:
+            fws = torch.empty(pkg.conv_fwd_ncdhw_fp8_workspace_size(
+                tuple(xb.shape), tuple(ops["w"].shape), wl.stride, wl.pad, wl.dil),
+                dtype=torch.uint8, device=device)
+            fsx = torch.empty(1, dtype=torch.float32, device=device)
+
+            def fused():
+                pkg.conv_fwd_ncdhw_fp8(xb, ops["w"], wl.stride, wl.pad, wl.dil, scale_w=ops["sw"],
+                                       scale_x=fsx, out=out, workspace=fws)
+            for _ in range(warmup):
+                fused()
+            res["ms_fused"] = Timer(steps, flush).run(fused)
+            del fws
+        except pkg.ConvError:
+            pass
     if with_e2e:
         res["e2e"] = run_e2e(pkg, wl, ops, out, ws, steps, warmup, flush)
     del ops
@@ -627,6 +644,10 @@ def workload_rooflines(secondary, peaks):
             mp = statistics.mean(r["ms_with_pack"])
             pk = statistics.mean(r["ms_pack"])
             gbs = r["pack_bytes"] / (pk * 1e-3) / 1e9
+            if "ms_fused" in r:   # quantised while loaded: amax pass + fused conv
+                mf = statistics.mean(r["ms_fused"])
+                ent["fused_ncdhw_ms"] = r4(mf)
+                ent["fused_ncdhw_tflops"] = r4(r["flop"] / (mf * 1e-3) / 1e12)
             ent.update({"with_pack_tflops": r4(r["flop"] / (mp * 1e-3) / 1e12),
                         "with_pack_ms": r4(mp),
                         "pack": {"bound": "hbm", "achieved_gbs": r4(gbs), "ms": r4(pk),

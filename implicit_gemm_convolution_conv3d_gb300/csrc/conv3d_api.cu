@@ -1516,7 +1516,8 @@ int fq_plan(const Geo& g, const DeviceInfo* dev, FqPlan* fp) {
     p.strip_bytes = static_cast<uint32_t>(8 * p.L * 16);
     p.b_stage_bytes = static_cast<uint32_t>((p.BN >> pair) * 128);
     const size_t strips = (2 * static_cast<size_t>(p.strip_bytes) + 1023) / 1024 * 1024;
-    const size_t fixed = 1024 + strips + 96 + 64;
+    const size_t staging = (static_cast<size_t>(p.strip_bytes) + 1023) / 1024 * 1024;
+    const size_t fixed = 1024 + strips + staging + 160;
     if (static_cast<size_t>(dev->smem_optin) < fixed + 2 * (p.b_stage_bytes + 16)) {
         set_error("fused channel-major e4m3 conv: the filter's strip does not fit in shared "
                   "memory (frame too wide for the filter height)");
@@ -1533,7 +1534,8 @@ int fq_plan(const Geo& g, const DeviceInfo* dev, FqPlan* fp) {
     // persistent CTAs (pairs) take whole m-tiles: every column tile in turn
     fp->grid = pair ? 2 * static_cast<int>(std::min<long long>(m_tiles, dev->num_sms / 2))
                     : static_cast<int>(std::min<long long>(m_tiles, dev->num_sms));
-    p.scratch_stride = static_cast<long long>(p.chunks) * p.strip_bytes;
+    // two scratch slots per CTA: the m-tile being copied back and the next
+    p.scratch_stride = 2LL * p.chunks * p.strip_bytes;
     fp->keep_bytes = static_cast<size_t>(fp->grid) * static_cast<size_t>(p.scratch_stride);
     return CONV_OK;
 }
@@ -1925,7 +1927,7 @@ int conv_fwd_ncdhw_fp8_workspace_size(const int64_t x_dims[5], const int64_t w_d
     if ((rc = device_info(&dev))) return rc;
     FqPlan fp;
     if ((rc = fq_plan(g, dev, &fp))) return rc;
-    *bytes = kFqScratchOffset + (fp.p.n_tiles > 1 ? fp.keep_bytes : 0);
+    *bytes = kFqScratchOffset + fp.keep_bytes;
     return CONV_OK;
 }
 
@@ -1968,9 +1970,9 @@ int conv_fwd_ncdhw_fp8(const void* x, const int64_t x_dims[5], const void* w,
     if ((rc = fq_plan(g, dev, &fp))) return rc;
     FQParams& p = fp.p;
     unsigned int* amax = static_cast<unsigned int*>(workspace);
-    // the strips a CTA converts for an m-tile's first column tile are kept for
-    // the others in the workspace after the amax word, when it has room
-    if (p.n_tiles > 1 && workspace_bytes >= kFqScratchOffset + fp.keep_bytes)
+    // with room after the amax word, the converters work one m-tile ahead into
+    // a scratch there and every column tile copies the strips back
+    if (workspace_bytes >= kFqScratchOffset + fp.keep_bytes)
         p.scratch = static_cast<unsigned char*>(workspace) + kFqScratchOffset;
     p.x = static_cast<const unsigned short*>(x);
     p.amax_bits = amax;

@@ -53,7 +53,8 @@ namespace {
 
 constexpr int kFqConvWarps = 8;    // one per 16-channel slice of a 128-channel chunk
 constexpr int kFqEpiWarp0 = 2;
-constexpr int kFqConvWarp0 = 6;
+constexpr int kFqLoaderWarp = 6;
+constexpr int kFqConvWarp0 = 7;
 constexpr int kFqChunk = 128;      // channels (e4m3 bytes) per reduction chunk
 
 struct FqUnit {
@@ -85,10 +86,161 @@ __device__ __forceinline__ int floor_div(int a, int b) {
     return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
 }
 
+// store_row_bf16 with streaming (evict-first) stores: the output is written
+// once and never read here, so it should not push the scratch out of L2.
+__device__ __forceinline__ void store_row_bf16_stream(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                                      float scale, const float* bias, int count,
+                                                      bool vec_ok) {
+    auto val = [&](int i) {
+        return __uint_as_float(v[i]) * scale + (bias ? __ldg(bias + i) : 0.0f);
+    };
+    if (count == 32 && vec_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            __stcs(d4 + i, make_uint4(pack_bf16x2(val(8 * i + 0), val(8 * i + 1)),
+                                      pack_bf16x2(val(8 * i + 2), val(8 * i + 3)),
+                                      pack_bf16x2(val(8 * i + 4), val(8 * i + 5)),
+                                      pack_bf16x2(val(8 * i + 6), val(8 * i + 7))));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < count) dst[i] = __float2bfloat16_rn(val(i));
+    }
+}
+
 // Columns the unit's MMAs compute: BN, or the rest of K rounded up to 32.
 __device__ __forceinline__ int fq_cols(int nt, const FQParams& p) {
     const int rest = p.K - nt * p.BN;
     return rest >= p.BN ? p.BN : ((rest + 31) & ~31);
+}
+
+// One 16-channel slice (channels c0 .. c0+15) of a strip, converted to e4m3
+// in the shared-memory rows at dst0 (L rows of 16 bytes): strip row q holds
+// padded position Ps + q of frame (n, d); rows with no image position are
+// zeros.  Run by one warp.
+__device__ __forceinline__ void fq_convert_slice(const FQParams& p, uint32_t dst0, int c0, int Ps,
+                                                 int n, int d, int lane, float scale_x,
+                                                 float rscale, bool corr) {
+    const long long HW = static_cast<long long>(p.H) * p.W;
+    const bool vec_planes = (HW % 8) == 0;   // every channel plane 16-byte aligned
+    const int nch = min(16, p.C - c0);
+    // (1) strip rows that hold no image position (padding columns,
+    // rows outside the frame, or channels past C) are zeros
+    {
+        int h = floor_div(Ps + lane, p.Wp);
+        int wp = Ps + lane - h * p.Wp;
+        for (int qb = 0; qb < p.L; qb += 32) {
+            const int w = wp - p.pw;
+            if (!(h >= 0 && h < p.H && w >= 0 && w < p.W) || nch <= 0)
+                st_shared_v4(dst0 + static_cast<uint32_t>(qb + lane) * 16u, 0u, 0u, 0u,
+                             0u);
+            wp += 32;
+            while (wp >= p.Wp) {
+                wp -= p.Wp;
+                ++h;
+            }
+        }
+    }
+    // (2) the image rows the strip covers, 8 positions x 16
+    // channels per lane: one 16-byte load per channel plane (a
+    // warp reads 512 contiguous bytes of each), the 8 x 16
+    // transpose in registers, one 16-byte strip row per position.
+    // Needs 16-byte aligned planes (H*W % 8 == 0); otherwise (3).
+    if (nch > 0 && vec_planes) {
+        const int ha = max(0, floor_div(Ps, p.Wp));
+        const int hb = min(p.H - 1, floor_div(Ps + p.L - 1, p.Wp));
+        const long long fa = static_cast<long long>(ha) * p.W;
+        const long long fb = static_cast<long long>(hb + 1) * p.W;
+        const unsigned short* src0 =
+            p.x + ((static_cast<long long>(n) * p.C + c0) * p.D + d) * HW;
+        const long long cstride = static_cast<long long>(p.D) * HW;
+        for (long long f = (fa & ~7ll) + 8 * lane; f < fb; f += 256) {
+            // codes[e][j]: channels 4j .. 4j+3 of position f + e
+            uint32_t codes[8][4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 8 * half + i;
+                    v[i] = c < nch
+                               ? __ldcs(reinterpret_cast<const uint4*>(src0 + c * cstride + f))
+                               : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    // element e of each channel row: word e/2, low or high half
+                    float xv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t ww = (e >> 1) == 0 ? v[i].x : (e >> 1) == 1 ? v[i].y
+                                          : (e >> 1) == 2 ? v[i].z : v[i].w;
+                        xv[i] = __uint_as_float((e & 1) ? (ww & 0xFFFF0000u) : (ww << 16));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float* x4 = xv + 4 * j;
+                        codes[e][2 * half + j] =
+                            corr ? (quant_e4m3x2<true>(x4[0], x4[1], scale_x, rscale) |
+                                    (quant_e4m3x2<true>(x4[2], x4[3], scale_x, rscale) << 16))
+                                 : (quant_e4m3x2<false>(x4[0], x4[1], scale_x, rscale) |
+                                    (quant_e4m3x2<false>(x4[2], x4[3], scale_x, rscale) << 16));
+                    }
+                }
+            }
+            int h = static_cast<int>(f / p.W);
+            int w = static_cast<int>(f - static_cast<long long>(h) * p.W);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int q = h * p.Wp + w + p.pw - Ps;
+                if (f + e >= fa && f + e < fb && q >= 0 && q < p.L)
+                    st_shared_v4(dst0 + static_cast<uint32_t>(q) * 16u, codes[e][0],
+                                 codes[e][1], codes[e][2], codes[e][3]);
+                if (++w == p.W) {
+                    w = 0;
+                    ++h;
+                }
+            }
+        }
+    }
+    // (3) planes not 16-byte aligned: per strip row, 16 2-byte
+    // loads (lanes take consecutive rows, so a warp reads 64
+    // contiguous bytes of a plane per load)
+    if (nch > 0 && !vec_planes) {
+        const unsigned short* src0 =
+            p.x + ((static_cast<long long>(n) * p.C + c0) * p.D + d) * HW;
+        const long long cstride = static_cast<long long>(p.D) * HW;
+        int h = floor_div(Ps + lane, p.Wp);
+        int wp = Ps + lane - h * p.Wp;
+        for (int qb = 0; qb < p.L; qb += 32) {
+            const int w = wp - p.pw;
+            if (h >= 0 && h < p.H && w >= 0 && w < p.W) {
+                const unsigned short* src = src0 + static_cast<long long>(h) * p.W + w;
+                float xv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    xv[i] = __uint_as_float(
+                        (i < nch ? static_cast<uint32_t>(__ldg(src + i * cstride)) : 0u) << 16);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o[j] = corr ? (quant_e4m3x2<true>(xv[4 * j], xv[4 * j + 1], scale_x, rscale) |
+                                   (quant_e4m3x2<true>(xv[4 * j + 2], xv[4 * j + 3], scale_x,
+                                                       rscale) << 16))
+                                : (quant_e4m3x2<false>(xv[4 * j], xv[4 * j + 1], scale_x, rscale) |
+                                   (quant_e4m3x2<false>(xv[4 * j + 2], xv[4 * j + 3], scale_x,
+                                                        rscale) << 16));
+                st_shared_v4(dst0 + static_cast<uint32_t>(qb + lane) * 16u, o[0], o[1],
+                             o[2], o[3]);
+            }
+            wp += 32;
+            while (wp >= p.Wp) {
+                wp -= p.Wp;
+                ++h;
+            }
+        }
+    }
 }
 
 template <int PAIR>
@@ -98,21 +250,30 @@ __global__ void __launch_bounds__(kFqThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t strips = base;                                     // 2 strip buffers
-    const uint32_t ring = base + ((2u * p.strip_bytes + 1023u) & ~1023u);
+    const uint32_t staging = base + ((2u * p.strip_bytes + 1023u) & ~1023u);   // converters' rows
+    const uint32_t ring = staging + ((p.strip_bytes + 1023u) & ~1023u);
     const uint32_t bfull0 = ring + static_cast<uint32_t>(p.b_stages) * p.b_stage_bytes;
     const uint32_t bempty0 = bfull0 + 8u * p.b_stages;
     const uint32_t sfull0 = bempty0 + 8u * p.b_stages;
     const uint32_t sempty0 = sfull0 + 16u;
     const uint32_t tfull0 = sempty0 + 16u;
     const uint32_t tempty0 = tfull0 + 16u;
-    const uint32_t drain_bar = tempty0 + 16u;
-    const uint32_t lbar0 = drain_bar + 8u;   // per converter warp: strip slice reloads
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (lbar0 + 8u * kFqConvWarps - raw));
+    const uint32_t kready0 = tempty0 + 16u;   // ahead mode: scratch slot written / copied out
+    const uint32_t kfree0 = kready0 + 16u;
+    const uint32_t drain_bar = kfree0 + 16u;
+    const uint32_t lbar0 = drain_bar + 8u;   // the loader's strip copies
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (lbar0 + 8u - raw));
     // misc[0] TMEM base, misc[1] abort flag, misc[2] weight boxes issued, misc[3] consumed
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    // ahead mode: the converters work one m-tile ahead into the scratch and a
+    // loader copies strips back; otherwise they convert in place
+    const bool ahead = p.scratch != nullptr;
+    // the scratch strips are read back n_tiles times within about a unit's
+    // time: they are asked to outlive the streaming activation and output in L2
+    const uint64_t keep_pol = l2_policy_evict_last();
     const int unit0 = static_cast<int>(blockIdx.x) >> PAIR;
     const int ustride = static_cast<int>(gridDim.x) >> PAIR;
     const int taps = p.R * p.S;
@@ -124,13 +285,17 @@ __global__ void __launch_bounds__(kFqThreads, 1)
             mbar_init(bempty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(sfull0 + 8 * b, kFqConvWarps * (1 + PAIR));
+            // a strip is signalled by the loader (ahead mode) or by every
+            // converter warp, of both CTAs of a pair
+            mbar_init(sfull0 + 8 * b, (ahead ? 1 : kFqConvWarps) * (1 + PAIR));
             mbar_init(sempty0 + 8 * b, 1);
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, kEpiWarps * (1 + PAIR));
+            mbar_init(kready0 + 8 * b, kFqConvWarps);
+            mbar_init(kfree0 + 8 * b, 1);
         }
         mbar_init(drain_bar, 1);
-        for (int k = 0; k < kFqConvWarps; ++k) mbar_init(lbar0 + 8 * k, 1);
+        mbar_init(lbar0, 1);
         misc[1] = 0u;
         misc[2] = 0u;
         misc[3] = 0u;
@@ -195,8 +360,16 @@ __global__ void __launch_bounds__(kFqThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
+            // descriptors built once and stepped by encoded offsets (16-byte
+            // units): strip buffer, tap window (r * Wp + s rows), two slices
+            // per MMA; weight stage, 32 bytes per MMA
             const uint32_t lbo = static_cast<uint32_t>(p.L) * 16u;          // slice stride
-            const uint64_t bdesc0 = make_smem_desc(ring, 1024u, 2u);        // 128B swizzle
+            const uint64_t adesc0 = make_smem_desc(strips, 128u, 0u, lbo);   // no swizzle
+            const uint64_t bdesc0 = make_smem_desc(ring, 1024u, 2u);         // 128B swizzle
+            const uint32_t a_buf_step = p.strip_bytes >> 4;
+            const uint32_t a_kstep = (2u * lbo) >> 4;
+            const uint32_t b_stage_step = p.b_stage_bytes >> 4;
+            const int row_skip = p.Wp - p.S;   // window offset from (r, S) to (r + 1, 0)
             int stage = 0, acc_iter = 0, chunk_iter = 0;
             uint32_t phase = 0, consumed = 0;
             bool ok = true;
@@ -219,39 +392,37 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t strip = strips + static_cast<uint32_t>(sb) * p.strip_bytes;
-                    for (int r = 0; r < p.R && ok; ++r) {
-                        for (int s = 0; s < p.S; ++s) {
-                            if (!wait_bar(bfull0 + 8 * stage, phase, abort_flag, p.status,
-                                          p.wait_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            misc[3] = ++consumed;
-                            const uint32_t win = strip + static_cast<uint32_t>(r * p.Wp + s) * 16u;
-                            const uint64_t bd =
-                                bdesc0 + ((static_cast<uint64_t>(stage) * p.b_stage_bytes) >> 4);
+                    const uint64_t abuf = adesc0 + static_cast<uint64_t>(sb) * a_buf_step;
+                    int win = 0, s = 0;   // window offset of tap (r, s): r * Wp + s
+                    for (int tap = 0; tap < taps; ++tap) {
+                        if (!wait_bar(bfull0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        misc[3] = ++consumed;
+                        const uint64_t a = abuf + static_cast<uint64_t>(win);
+                        const uint64_t b = bdesc0 + static_cast<uint64_t>(stage) * b_stage_step;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {   // 32 channel bytes per MMA
-                                const uint64_t ad =
-                                    make_smem_desc(win + 2u * static_cast<uint32_t>(kk) * lbo, 128u,
-                                                   0u, lbo);
-                                const uint64_t b = bd + 2u * static_cast<uint32_t>(kk);
-                                if (PAIR)
-                                    tc_mma_f8_pair(d_tmem, ad, b, idesc, accum);
-                                else
-                                    tc_mma_f8(d_tmem, ad, b, idesc, accum);
-                                accum = 1u;
-                            }
+                        for (int kk = 0; kk < 4; ++kk) {   // 32 channel bytes per MMA
                             if (PAIR)
-                                tc_commit_pair(bempty0 + 8 * stage, 3);
+                                tc_mma_f8_pair(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc, accum);
                             else
-                                tc_commit(bempty0 + 8 * stage);
-                            if (++stage == p.b_stages) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
+                                tc_mma_f8(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc, accum);
+                            accum = 1u;
+                        }
+                        if (PAIR)
+                            tc_commit_pair(bempty0 + 8 * stage, 3);
+                        else
+                            tc_commit(bempty0 + 8 * stage);
+                        if (++stage == p.b_stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        ++win;
+                        if (++s == p.S) {
+                            s = 0;
+                            win += row_skip;
                         }
                     }
                     // the strip buffer is free in both CTAs once these MMAs have read it
@@ -270,7 +441,7 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                 ++acc_iter;
             }
         }
-    } else if (warp < kFqConvWarp0) {
+    } else if (warp < kFqEpiWarp0 + kEpiWarps) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;   // TMEM lane quarter this warp may read
         float scale = scale_x;
@@ -302,8 +473,9 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                 tmem_ld_wait();
                 const int n0 = t.nt * p.BN + 32 * j;
                 if (valid)
-                    store_row_bf16(out + orow * p.K + n0, v, scale,
-                                   p.bias ? p.bias + n0 : nullptr, min(32, p.K - n0), vec_out);
+                    store_row_bf16_stream(out + orow * p.K + n0, v, scale,
+                                          p.bias ? p.bias + n0 : nullptr, min(32, p.K - n0),
+                                          vec_out);
             }
             tc_fence_before();
             __syncwarp();
@@ -315,208 +487,139 @@ __global__ void __launch_bounds__(kFqThreads, 1)
             }
             ++acc_iter;
         }
+    } else if (warp == kFqLoaderWarp) {
+        // ------------------------------------------------------ strip loader
+        // (ahead mode): each chunk's converted strip comes back from this
+        // CTA's scratch slot of the m-tile, one bulk copy into a strip buffer
+        if (ahead && lane == 0) {
+            const uint32_t sfull_dst0 = PAIR ? mapa_shared(sfull0, 0) : sfull0;
+            const unsigned char* mine =
+                p.scratch + static_cast<long long>(blockIdx.x) * p.scratch_stride;
+            int chunk_iter = 0;
+            bool ok = true;
+            FqUnit t;
+            for (int i = 0; ok && fq_unit(i, unit0, ustride, p, t); ++i) {
+                const int j = i / p.n_tiles, slot = j & 1;
+                // the converters have written the m-tile's strips
+                if (t.nt == 0 && !wait_bar(kready0 + 8 * slot, static_cast<uint32_t>(j >> 1) & 1u,
+                                           abort_flag, p.status, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                for (int cc = 0; cc < p.chunks; ++cc, ++chunk_iter) {
+                    const int sb = chunk_iter & 1;
+                    const uint32_t s_phase = static_cast<uint32_t>(chunk_iter >> 1) & 1u;
+                    if (!wait_bar(sempty0 + 8 * sb, s_phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(lbar0, p.strip_bytes);
+                    bulk_load_1d_hint(strips + static_cast<uint32_t>(sb) * p.strip_bytes,
+                                      mine + (static_cast<long long>(slot) * p.chunks + cc) *
+                                                 p.strip_bytes,
+                                      p.strip_bytes, lbar0, keep_pol);
+                    load_pending = true;
+                    if (!wait_bar(lbar0, loads & 1u, abort_flag, p.status, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    load_pending = false;
+                    ++loads;
+                    if (PAIR)
+                        mbar_arrive_cluster(sfull_dst0 + 8 * sb);
+                    else
+                        mbar_arrive(sfull0 + 8 * sb);
+                }
+                // the slot's last strip has landed: the converters may refill it
+                if (ok && t.nt == p.n_tiles - 1) mbar_arrive(kfree0 + 8 * slot);
+            }
+        }
     } else {
         // ------------------------------------------------------ converters
         const int k = warp - kFqConvWarp0;   // 16-channel slice of each chunk
         const float rscale = __frcp_rn(scale_x);
         const bool corr = quot_corrected_ok(scale_x);
-        const long long HW = static_cast<long long>(p.H) * p.W;
-        const bool vec_planes = (HW % 8) == 0;   // every channel plane 16-byte aligned
-        const uint32_t sfull_dst0 = PAIR ? mapa_shared(sfull0, 0) : sfull0;
-        // converted strips kept for the m-tile's later column tiles
-        const bool reuse = p.scratch != nullptr && p.n_tiles > 1;
-        unsigned char* my_scratch =
-            reuse ? p.scratch + static_cast<long long>(blockIdx.x) * p.scratch_stride : nullptr;
-        int chunk_iter = 0;
         bool ok = true;
-        FqUnit t;
-        for (int i = 0; ok && fq_unit(i, unit0, ustride, p, t); ++i) {
-            const int n = t.frame / p.D, d = t.frame - n * p.D;
-            // first strip row: padded position P0 - ph * Wp - pw of this CTA's rows
-            const int Ps = t.mt * kTileM + static_cast<int>(rank) * 128 - (p.ph * p.Wp + p.pw);
-            for (int cc = 0; cc < p.chunks && ok; ++cc, ++chunk_iter) {
-                const int sb = chunk_iter & 1;
-                const uint32_t s_phase = static_cast<uint32_t>(chunk_iter >> 1) & 1u;
-                if (!wait_bar(sempty0 + 8 * sb, s_phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
+        if (ahead) {
+            // one m-tile ahead of the MMAs: m-tile j's strips into scratch
+            // slot j & 1, slice by slice through this warp's staging rows
+            unsigned char* mine = p.scratch + static_cast<long long>(blockIdx.x) * p.scratch_stride;
+            const uint32_t slice_bytes = static_cast<uint32_t>(p.L) * 16u;
+            const uint32_t stage = staging + static_cast<uint32_t>(k) * slice_bytes;
+            for (int j = 0; ok; ++j) {
+                const int g = unit0 + j * ustride;
+                if (g >= p.m_tiles) break;
+                const int frame = g / p.mt_frame, mt = g - frame * p.mt_frame;
+                const int n = frame / p.D, d = frame - n * p.D;
+                const int Ps = mt * kTileM + static_cast<int>(rank) * 128 - (p.ph * p.Wp + p.pw);
+                const int slot = j & 1;
+                // the loader has copied out the slot's previous m-tile
+                if (j >= 2 && !wait_bar(kfree0 + 8 * slot, static_cast<uint32_t>((j >> 1) - 1) & 1u,
+                                        abort_flag, p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }
-                const int c0 = cc * kFqChunk + k * 16;   // first channel of this slice
-                const uint32_t dst0 = strips + static_cast<uint32_t>(sb) * p.strip_bytes +
-                                      static_cast<uint32_t>(k) * static_cast<uint32_t>(p.L) * 16u;
-                const uint32_t slice_bytes = static_cast<uint32_t>(p.L) * 16u;
-                unsigned char* keep =
-                    reuse ? my_scratch + (static_cast<long long>(cc) * kFqConvWarps + k) * slice_bytes
-                          : nullptr;
-                // this warp's earlier bulk store from the buffer has finished reading it
-                if (reuse && lane == 0) bulk_wait_read<0>();
-                __syncwarp();
-                if (reuse && t.nt > 0) {
-                    // a later column tile of the m-tile: the slice converted for
-                    // the first one comes back from the scratch (L2)
-                    bool landed = true;
+                for (int cc = 0; cc < p.chunks; ++cc) {
+                    // the staging rows' previous bulk store has read them
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+                    fq_convert_slice(p, stage, cc * kFqChunk + k * 16, Ps, n, d, lane, scale_x,
+                                     rscale, corr);
+                    fence_proxy_async_smem();
+                    __syncwarp();
                     if (lane == 0) {
-                        bulk_wait_done<0>();   // the stores have reached memory
-                        mbar_arrive_expect_tx(lbar0 + 8 * k, slice_bytes);
-                        bulk_load_1d(dst0, keep, slice_bytes, lbar0 + 8 * k);
-                        landed = wait_bar(lbar0 + 8 * k, static_cast<uint32_t>(loads & 1),
-                                          abort_flag, p.status, p.wait_ns);
-                        load_pending = !landed;
+                        bulk_store_1d_hint(mine + ((static_cast<long long>(slot) * p.chunks + cc) *
+                                                       kFqConvWarps + k) * slice_bytes,
+                                           stage, slice_bytes, keep_pol);
+                        bulk_commit();
                     }
-                    ++loads;
-                    if (!__shfl_sync(0xffffffffu, landed ? 1 : 0, 0)) {
+                }
+                if (lane == 0) {
+                    bulk_wait_done<0>();   // the slot's slices are in memory
+                    mbar_arrive(kready0 + 8 * slot);
+                }
+                __syncwarp();
+            }
+        } else {
+            // in place: each chunk's slice straight into a strip buffer
+            const uint32_t sfull_dst0 = PAIR ? mapa_shared(sfull0, 0) : sfull0;
+            int chunk_iter = 0;
+            FqUnit t;
+            for (int i = 0; ok && fq_unit(i, unit0, ustride, p, t); ++i) {
+                const int n = t.frame / p.D, d = t.frame - n * p.D;
+                const int Ps = t.mt * kTileM + static_cast<int>(rank) * 128 - (p.ph * p.Wp + p.pw);
+                for (int cc = 0; cc < p.chunks; ++cc, ++chunk_iter) {
+                    const int sb = chunk_iter & 1;
+                    const uint32_t s_phase = static_cast<uint32_t>(chunk_iter >> 1) & 1u;
+                    if (!wait_bar(sempty0 + 8 * sb, s_phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
+                    fq_convert_slice(p,
+                                     strips + static_cast<uint32_t>(sb) * p.strip_bytes +
+                                         static_cast<uint32_t>(k) * static_cast<uint32_t>(p.L) * 16u,
+                                     cc * kFqChunk + k * 16, Ps, n, d, lane, scale_x, rscale, corr);
+                    // the strip's generic-proxy writes become visible to the
+                    // tensor core before the MMA issuer learns of them
+                    fence_proxy_async_smem();
+                    __syncwarp();
                     if (lane == 0) {
                         if (PAIR)
                             mbar_arrive_cluster(sfull_dst0 + 8 * sb);
                         else
                             mbar_arrive(sfull0 + 8 * sb);
                     }
-                    continue;
-                }
-                const int nch = min(16, p.C - c0);
-                // (1) strip rows that hold no image position (padding columns,
-                // rows outside the frame, or channels past C) are zeros
-                {
-                    int h = floor_div(Ps + lane, p.Wp);
-                    int wp = Ps + lane - h * p.Wp;
-                    for (int qb = 0; qb < p.L; qb += 32) {
-                        const int w = wp - p.pw;
-                        if (!(h >= 0 && h < p.H && w >= 0 && w < p.W) || nch <= 0)
-                            st_shared_v4(dst0 + static_cast<uint32_t>(qb + lane) * 16u, 0u, 0u, 0u,
-                                         0u);
-                        wp += 32;
-                        while (wp >= p.Wp) {
-                            wp -= p.Wp;
-                            ++h;
-                        }
-                    }
-                }
-                // (2) the image rows the strip covers, 8 positions x 16
-                // channels per lane: one 16-byte load per channel plane (a
-                // warp reads 512 contiguous bytes of each), the 8 x 16
-                // transpose in registers, one 16-byte strip row per position.
-                // Needs 16-byte aligned planes (H*W % 8 == 0); otherwise (3).
-                if (nch > 0 && vec_planes) {
-                    const int ha = max(0, floor_div(Ps, p.Wp));
-                    const int hb = min(p.H - 1, floor_div(Ps + p.L - 1, p.Wp));
-                    const long long fa = static_cast<long long>(ha) * p.W;
-                    const long long fb = static_cast<long long>(hb + 1) * p.W;
-                    const unsigned short* src0 =
-                        p.x + ((static_cast<long long>(n) * p.C + c0) * p.D + d) * HW;
-                    const long long cstride = static_cast<long long>(p.D) * HW;
-                    for (long long f = (fa & ~7ll) + 8 * lane; f < fb; f += 256) {
-                        // codes[e][j]: channels 4j .. 4j+3 of position f + e
-                        uint32_t codes[8][4];
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint4 v[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int c = 8 * half + i;
-                                v[i] = c < nch
-                                           ? __ldg(reinterpret_cast<const uint4*>(src0 + c * cstride + f))
-                                           : make_uint4(0u, 0u, 0u, 0u);
-                            }
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                // element e of each channel row: word e/2, low or high half
-                                float xv[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const uint32_t ww = (e >> 1) == 0 ? v[i].x : (e >> 1) == 1 ? v[i].y
-                                                      : (e >> 1) == 2 ? v[i].z : v[i].w;
-                                    xv[i] = __uint_as_float((e & 1) ? (ww & 0xFFFF0000u) : (ww << 16));
-                                }
-#pragma unroll
-                                for (int j = 0; j < 2; ++j) {
-                                    const float* x4 = xv + 4 * j;
-                                    codes[e][2 * half + j] =
-                                        corr ? (quant_e4m3x2<true>(x4[0], x4[1], scale_x, rscale) |
-                                                (quant_e4m3x2<true>(x4[2], x4[3], scale_x, rscale) << 16))
-                                             : (quant_e4m3x2<false>(x4[0], x4[1], scale_x, rscale) |
-                                                (quant_e4m3x2<false>(x4[2], x4[3], scale_x, rscale) << 16));
-                                }
-                            }
-                        }
-                        int h = static_cast<int>(f / p.W);
-                        int w = static_cast<int>(f - static_cast<long long>(h) * p.W);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int q = h * p.Wp + w + p.pw - Ps;
-                            if (f + e >= fa && f + e < fb && q >= 0 && q < p.L)
-                                st_shared_v4(dst0 + static_cast<uint32_t>(q) * 16u, codes[e][0],
-                                             codes[e][1], codes[e][2], codes[e][3]);
-                            if (++w == p.W) {
-                                w = 0;
-                                ++h;
-                            }
-                        }
-                    }
-                }
-                // (3) planes not 16-byte aligned: per strip row, 16 2-byte
-                // loads (lanes take consecutive rows, so a warp reads 64
-                // contiguous bytes of a plane per load)
-                if (nch > 0 && !vec_planes) {
-                    const unsigned short* src0 =
-                        p.x + ((static_cast<long long>(n) * p.C + c0) * p.D + d) * HW;
-                    const long long cstride = static_cast<long long>(p.D) * HW;
-                    int h = floor_div(Ps + lane, p.Wp);
-                    int wp = Ps + lane - h * p.Wp;
-                    for (int qb = 0; qb < p.L; qb += 32) {
-                        const int w = wp - p.pw;
-                        if (h >= 0 && h < p.H && w >= 0 && w < p.W) {
-                            const unsigned short* src = src0 + static_cast<long long>(h) * p.W + w;
-                            float xv[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                xv[i] = __uint_as_float(
-                                    (i < nch ? static_cast<uint32_t>(__ldg(src + i * cstride)) : 0u) << 16);
-                            uint32_t o[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                o[j] = corr ? (quant_e4m3x2<true>(xv[4 * j], xv[4 * j + 1], scale_x, rscale) |
-                                               (quant_e4m3x2<true>(xv[4 * j + 2], xv[4 * j + 3], scale_x,
-                                                                   rscale) << 16))
-                                            : (quant_e4m3x2<false>(xv[4 * j], xv[4 * j + 1], scale_x, rscale) |
-                                               (quant_e4m3x2<false>(xv[4 * j + 2], xv[4 * j + 3], scale_x,
-                                                                    rscale) << 16));
-                            st_shared_v4(dst0 + static_cast<uint32_t>(qb + lane) * 16u, o[0], o[1],
-                                         o[2], o[3]);
-                        }
-                        wp += 32;
-                        while (wp >= p.Wp) {
-                            wp -= p.Wp;
-                            ++h;
-                        }
-                    }
-                }
-                // the strip's generic-proxy writes become visible to the
-                // tensor core (and the bulk copy) before the MMA issuer learns of them
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (reuse) {
-                        bulk_store_1d(keep, dst0, slice_bytes);
-                        bulk_commit();
-                    }
-                    if (PAIR)
-                        mbar_arrive_cluster(sfull_dst0 + 8 * sb);
-                    else
-                        mbar_arrive(sfull0 + 8 * sb);
                 }
             }
         }
     }
 
-    if (warp >= kFqConvWarp0 && lane == 0 && p.scratch != nullptr) {
-        // the bulk stores have read their shared-memory source (and written)
-        // before the CTA leaves; a reload that was not seen landing lands first
-        bulk_wait_done<0>();
-        if (load_pending)
-            drain_wait(lbar0 + 8 * (warp - kFqConvWarp0), (loads - 1u) & 1u);
+    if (ahead && lane == 0) {
+        // the converters' bulk stores have read their staging rows (and
+        // written) before the CTA leaves; a strip reload that was not seen
+        // landing lands first
+        if (warp >= kFqConvWarp0) bulk_wait_done<0>();
+        if (warp == kFqLoaderWarp && load_pending) drain_wait(lbar0, loads & 1u);
     }
     __syncthreads();
     // in a pair, both CTAs finish their roles (and the peer's last remote

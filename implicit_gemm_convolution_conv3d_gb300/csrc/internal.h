@@ -148,7 +148,7 @@ struct FQParams {
     uint32_t tmem_cols;
     int pair;
     unsigned char* scratch;        // per-CTA converted strips (blockIdx.x * scratch_stride), or NULL
-    long long scratch_stride;      // chunks * strip_bytes
+    long long scratch_stride;      // 2 slots x chunks x strip_bytes
     const unsigned short* x;       // bf16 NCDHW
     const unsigned int* amax_bits; // max |x| as binary32 bits (computed before)
     float* scale_x_out;            // receives amax / 448 (or NULL)
@@ -158,7 +158,8 @@ struct FQParams {
     int* status;
     unsigned long long wait_ns;
 };
-constexpr int kFqThreads = 448;   // warp 0 weights (TMA), 1 MMA, 2-5 epilogue, 6-13 converters
+constexpr int kFqThreads = 480;   // warp 0 weights (TMA), 1 MMA, 2-5 epilogue, 6 strip loader,
+                                  // 7-14 converters
 
 // Launch the fused channel-major e4m3 convolution (w_map: the e4m3 KTRSC
 // weight as {C, R*S, K} with boxes {128, 1, BN >> pair}, 128-byte swizzle).

@@ -202,6 +202,31 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
         : "memory");
 }
 
+// L2 cache policy asking that lines stay resident ahead of others (for data
+// read again soon), for the cache-hinted bulk copies below
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_load_1d_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                                  uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_1d_hint(void* dst, uint32_t src, uint32_t bytes,
+                                                   uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                     dst),
+                 "r"(src), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+
 // shared -> global, in the thread's bulk async-group (bulk_commit, then
 // bulk_wait_read / bulk_wait_done)
 __device__ __forceinline__ void bulk_store_1d(void* dst, uint32_t src, uint32_t bytes) {

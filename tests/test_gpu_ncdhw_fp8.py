@@ -63,11 +63,12 @@ def _run(pkg, xs, ws, seed, bias=False, small_ws=False):
 
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 @pytest.mark.parametrize("pair", [0, 1])
-@pytest.mark.parametrize("small_ws", [False, True], ids=["kept-strips", "reconverted"])
+@pytest.mark.parametrize("small_ws", [False, True], ids=["ahead", "in-place"])
 def test_fused_quantising_loader_matches_oracle(pkg, case, pair, small_ws):
-    """With the preferred workspace the strips converted for an m-tile's first
-    column tile are copied back for the others; with only the amax word they
-    are converted again: the same values either way."""
+    """With the preferred workspace the converters work one m-tile ahead into
+    a scratch and the strips are copied back for every column tile; with only
+    the amax word they convert each chunk in place: the same values either
+    way."""
     xs, ws = case
     with pkg.overrides(pair=pair):
         _, _, _, _, y, ref, _ = _run(pkg, xs, ws, CASES.index(case), small_ws=small_ws)

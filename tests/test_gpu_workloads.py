@@ -124,7 +124,6 @@ def test_fp8_workload_pack_exact_and_conv_sampled(pkg):
     qw, sw = pkg.pack_ncdhw_bf16_to_ndhwc_fp8(w)
     torch.cuda.synchronize()
     xh = bits16(x)
-    del x
     ref_qx, ref_sx = oracle.pack_ncdhw_to_ndhwc_fp8(xh)
     del xh
     qx_h = bytes8(qx)
@@ -140,6 +139,16 @@ def test_fp8_workload_pack_exact_and_conv_sampled(pkg):
     plan = pkg.conv_fwd_plan(tuple(qx.shape), tuple(qw.shape), wl.stride, wl.pad, wl.dil, 1)
     idx = _sample(tuple(y.shape), wl, plan["tile_n"])
     _check_sampled(y, qx_h, qw_h, idx, wl, sx.item(), sw.item())
+    # the same conv with the activation quantised while it is loaded (no
+    # pack pass): the scale's bits and the sampled outputs against the
+    # oracle's pack and conv
+    del y, qx
+    torch.cuda.empty_cache()
+    yf, sxf = pkg.conv_fwd_ncdhw_fp8(x, qw, wl.stride, wl.pad, wl.dil, scale_w=sw)
+    torch.cuda.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    assert np.float32(sxf.item()).tobytes() == np.float32(ref_sx).tobytes()
+    _check_sampled(yf, qx_h, qw_h, idx, wl, sxf.item(), sw.item())
 
 
 def test_temporal_big_sampled(pkg):
