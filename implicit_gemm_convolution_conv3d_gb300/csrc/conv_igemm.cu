@@ -57,11 +57,10 @@ __device__ __forceinline__ int tile_cols(int n_tile, const KParams& p) {
 // (each is read by T output planes) in L2.
 __device__ __forceinline__ void temporal_tile(int m_tile, const KParams& p, int& plane, int& hwb) {
     if (p.hw_major) {
-        const int planes = p.N * p.Do;
-        hwb = m_tile / planes;
-        plane = m_tile - hwb * planes;
+        hwb = static_cast<int>(fdiv(static_cast<uint32_t>(m_tile), p.f_planes));
+        plane = m_tile - hwb * p.N * p.Do;
     } else {
-        plane = m_tile / p.hw_tiles;
+        plane = static_cast<int>(fdiv(static_cast<uint32_t>(m_tile), p.f_hw_tiles));
         hwb = m_tile - plane * p.hw_tiles;
     }
 }
@@ -74,15 +73,17 @@ __device__ __forceinline__ void temporal_tile(int m_tile, const KParams& p, int&
 __device__ __forceinline__ Unit decode_unit(int u, const KParams& p) {
     const int tiles = p.m_tiles * p.n_tiles;
     Unit r;
-    r.split = u / tiles;
+    r.split = static_cast<int>(fdiv(static_cast<uint32_t>(u), p.f_tiles));
     const int t = u - r.split * tiles;
     const int group = p.group_m * p.n_tiles;
-    const int g = t / group;
+    const int g = static_cast<int>(fdiv(static_cast<uint32_t>(t), p.f_group));
     const int first_m = g * p.group_m;
-    const int gm = min(p.group_m, p.m_tiles - first_m);
+    const int gm = min(p.group_m, p.m_tiles - first_m);   // the last group may be short
     const int local = t - g * group;
-    r.m_tile = p.m_tile0 + first_m + local % gm;
-    r.n_tile = p.n_tile0 + local / gm;
+    const int col = gm == p.group_m ? static_cast<int>(fdiv(static_cast<uint32_t>(local), p.f_gm))
+                                    : local / gm;
+    r.m_tile = p.m_tile0 + first_m + (local - col * gm);
+    r.n_tile = p.n_tile0 + col;
     return r;
 }
 
@@ -252,6 +253,17 @@ __device__ void gather_producer(const KParams& p, uint32_t tiles, uint32_t full0
 // adding encoded byte offsets (address field = bytes >> 4).  A 256-byte
 // k-step (KMMA = 8) holds each operand as two 128-byte-swizzled boxes, one
 // after the other; slices 4..7 read the second box.
+//
+// The tensor pipe queues only a couple of MMAs, so an issue blocks until the
+// pipe has room and the issuer runs in step with it: whatever the thread does
+// between two k-steps (the barrier wait, the commit, the loop) must fit in the
+// MMAs still queued, or the pipe idles.  With two or more slices per k-step
+// the next k-step's stage is therefore tested (without blocking) before the
+// last slice is issued, while the earlier slices are still executing: when it
+// has landed, the next k-step starts without a wait.  A stage still in flight
+// is waited for as usual after the commit (blocking there instead would hold
+// back this stage's release to the producer).  At the last k-step of a unit
+// the same slot decodes the next unit and tests its accumulator.
 template <int KMMA, int FP8, int PAIR, int MSUB>
 __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uint32_t full0,
                                            uint32_t empty0, uint32_t tfull0, uint32_t tempty0,
@@ -268,32 +280,70 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
     // msub row sub-tiles share each B stage; the TMEM holds 2/msub unit
     // accumulators (double-buffered when msub == 1)
     constexpr int nacc = 2 / MSUB;
+    constexpr bool kEarly = KMMA >= 2;
     const uint32_t sub_step = (static_cast<uint32_t>(kBM) * p.BK) >> 4;   // A sub-tile, encoded
     const uint32_t abox_step = (static_cast<uint32_t>(kBM) * 128u) >> 4;
     const uint32_t bbox_step = (static_cast<uint32_t>(p.BN >> PAIR) * 128u) >> 4;
+    const int ustride = static_cast<int>(gridDim.x) >> PAIR;
+    int u = static_cast<int>(blockIdx.x) >> PAIR;
+    if (u >= total_units) return;
+    Unit t = decode_unit(u, p);
     int stage = 0, acc_iter = 0;
     uint32_t phase = 0, consumed = 0;
-    for (int u = static_cast<int>(blockIdx.x) >> PAIR; u < total_units; u += gridDim.x >> PAIR) {
-        const Unit t = decode_unit(u, p);
+    bool stage_ready = false;   // the full barrier of `stage` was already waited for
+    bool acc_ready = false;     // the accumulator of `acc_iter` was already waited for
+    while (true) {
         const int ks0 = t.split * p.steps_per_split;
         const int ks1 = min(p.k_steps, ks0 + p.steps_per_split);
         const int acc = acc_iter % nacc;
-        const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
-        if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns)) return;
-        tc_fence_after();
+        if (!acc_ready) {
+            const uint32_t acc_phase = static_cast<uint32_t>(acc_iter / nacc) & 1u;
+            if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.status, p.wait_ns)) return;
+            tc_fence_after();
+        }
+        acc_ready = false;
         // the instruction descriptor's N (bits 17-22, N / 8) for this tile
         const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) |
                                (static_cast<uint32_t>(tile_cols(t.n_tile, p) >> 3) << 17);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MSUB * p.BN);
+        const int un = u + ustride;
+        Unit tn = t;
         uint32_t accum = 0u;
         for (int ks = ks0; ks < ks1; ++ks) {
-            if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) return;
-            tc_fence_after();
-            misc[3] = ++consumed;
-            const uint64_t off = static_cast<uint64_t>(stage) * stage_step;
+            if (!stage_ready) {
+                if (!wait_bar(full0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) return;
+                misc[3] = ++consumed;
+                tc_fence_after();
+            }
+            stage_ready = false;
+            int nstage = stage + 1;
+            uint32_t nphase = phase;
+            if (nstage == p.stages) {
+                nstage = 0;
+                nphase ^= 1u;
+            }
+            const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(stage) * stage_step);
             const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
 #pragma unroll
             for (int k = 0; k < KMMA; ++k) {
+                if (kEarly && k == KMMA - 1) {
+                    const bool last = ks + 1 == ks1;
+                    if (!last || un < total_units) {
+                        if (last) {
+                            tn = decode_unit(un, p);
+                            if (nacc == 2) {
+                                const int na = acc_iter + 1;
+                                const uint32_t na_phase = static_cast<uint32_t>(na / nacc) & 1u;
+                                acc_ready = mbar_test_wait(tempty0 + 8 * (na % nacc), na_phase ^ 1u);
+                            }
+                        }
+                        if (mbar_test_wait(full0 + 8 * nstage, nphase)) {
+                            misc[3] = ++consumed;
+                            stage_ready = true;
+                        }
+                        if (stage_ready || acc_ready) tc_fence_after();
+                    }
+                }
                 const int box = k >> 2, kin = k & 3;   // 128-byte box, 32-byte slice in it
                 const uint64_t b = bd + box * bbox_step + 2 * kin;
 #pragma unroll
@@ -319,16 +369,17 @@ __device__ __forceinline__ void mma_issuer(const KParams& p, uint32_t tiles, uin
                 tc_commit_pair(empty0 + 8 * stage, 3);
             else
                 tc_commit(empty0 + 8 * stage);
-            if (++stage == p.stages) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            stage = nstage;
+            phase = nphase;
         }
         if (PAIR)
             tc_commit_pair(tfull0 + 8 * acc, 3);
         else
             tc_commit(tfull0 + 8 * acc);
         ++acc_iter;
+        if (un >= total_units) break;
+        u = un;
+        t = kEarly ? tn : decode_unit(un, p);
     }
 }
 
@@ -373,20 +424,33 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
             if (AMODE == AM_IM2COL) {
                 const long long m0 =
                     static_cast<long long>(t.m_tile) * kTileM * MSUB + first;
-                const int ow = static_cast<int>(m0 % p.Wo);
-                const long long q1 = m0 / p.Wo;
-                const int oh = static_cast<int>(q1 % p.Ho);
-                const long long q2 = q1 / p.Ho;
-                const int od = static_cast<int>(q2 % p.Do);
-                an[sub] = static_cast<int>(q2 / p.Do);
+                int ow, oh, od;
+                if (p.rows32) {
+                    const uint32_t x = static_cast<uint32_t>(m0);
+                    const uint32_t q1 = fdiv(x, p.f_Wo);
+                    const uint32_t q2 = fdiv(q1, p.f_Ho);
+                    const uint32_t q3 = fdiv(q2, p.f_Do);
+                    ow = static_cast<int>(x - q1 * static_cast<uint32_t>(p.Wo));
+                    oh = static_cast<int>(q1 - q2 * static_cast<uint32_t>(p.Ho));
+                    od = static_cast<int>(q2 - q3 * static_cast<uint32_t>(p.Do));
+                    an[sub] = static_cast<int>(q3);
+                } else {
+                    ow = static_cast<int>(m0 % p.Wo);
+                    const long long q1 = m0 / p.Wo;
+                    oh = static_cast<int>(q1 % p.Ho);
+                    const long long q2 = q1 / p.Ho;
+                    od = static_cast<int>(q2 % p.Do);
+                    an[sub] = static_cast<int>(q2 / p.Do);
+                }
                 aw[sub] = ow * p.sw - p.pw;
                 ah[sub] = oh * p.sh - p.ph;
                 ad[sub] = od * p.sd - p.pd;
             } else if (AMODE == AM_TEMPORAL) {
                 int plane, hwb;
                 temporal_tile(t.m_tile, p, plane, hwb);
-                const int od = plane % p.Do;
-                an[sub] = plane / p.Do;
+                const int nn = static_cast<int>(fdiv(static_cast<uint32_t>(plane), p.f_Do));
+                const int od = plane - nn * p.Do;
+                an[sub] = nn;
                 ad[sub] = od * p.sd - p.pd;
                 ah[sub] = hwb * kTileM * MSUB + first;   // first H*W row
             } else {
@@ -395,9 +459,16 @@ __device__ __forceinline__ void tma_producer(const TMaps& tm, const KParams& p, 
         }
         // reduction order: channel chunk (outer), tap (t, r, s) inner.  The
         // position is decoded once per unit and then stepped incrementally.
-        int tap = ks0 % p.taps;
-        int c0 = (ks0 / p.taps) * bke;
-        int fs = tap % p.S, fr = (tap / p.S) % p.R, ft = tap / (p.S * p.R);
+        int tap = 0, c0 = 0, fs = 0, fr = 0, ft = 0;
+        if (ks0 > 0) {
+            const int chunk = static_cast<int>(fdiv(static_cast<uint32_t>(ks0), p.f_taps));
+            tap = ks0 - chunk * p.taps;
+            c0 = chunk * bke;
+            const int qs = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.f_S));
+            ft = static_cast<int>(fdiv(static_cast<uint32_t>(qs), p.f_R));
+            fs = tap - qs * p.S;
+            fr = qs - ft * p.R;
+        }
         int k0 = ks0 * bke;   // GEMM modes: first reduction element of the k-step
         for (int ks = ks0; ks < ks1; ++ks) {
             if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status, p.wait_ns)) {
@@ -906,8 +977,22 @@ cudaError_t launch_one(const TMaps* tm, const KParams& p, int grid, size_t smem,
 
 }  // namespace
 
-cudaError_t launch_igemm(int amode, int fp8, const TMaps* tm, const KParams& p, int grid,
+cudaError_t launch_igemm(int amode, int fp8, const TMaps* tm, const KParams& kp, int grid,
                          size_t smem, cudaStream_t stream) {
+    KParams p = kp;
+    const auto u32 = [](long long v) { return static_cast<uint32_t>(v < 1 ? 1 : v); };
+    p.f_tiles = make_fastdiv(u32(static_cast<long long>(p.m_tiles) * p.n_tiles));
+    p.f_group = make_fastdiv(u32(static_cast<long long>(p.group_m) * p.n_tiles));
+    p.f_gm = make_fastdiv(u32(p.group_m));
+    p.f_planes = make_fastdiv(u32(static_cast<long long>(p.N) * p.Do));
+    p.f_hw_tiles = make_fastdiv(u32(p.hw_tiles));
+    p.f_Do = make_fastdiv(u32(p.Do));
+    p.f_Ho = make_fastdiv(u32(p.Ho));
+    p.f_Wo = make_fastdiv(u32(p.Wo));
+    p.f_taps = make_fastdiv(u32(p.taps));
+    p.f_S = make_fastdiv(u32(p.S));
+    p.f_R = make_fastdiv(u32(p.R));
+    p.rows32 = p.M + 4 * kBM < (1ll << 31) ? 1 : 0;
     const int key = (amode * 2 + (fp8 ? 1 : 0)) * 2 + (p.pair ? 1 : 0);
     switch (key) {
 #define C3D_CASE(AM, F8, PR) \

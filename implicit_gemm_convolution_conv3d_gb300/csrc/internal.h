@@ -66,6 +66,28 @@ constexpr int kGatherThreads = 128;    // producer threads of AM_GEMM_GATHER
 constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;              // one warp's 32x32 bf16 chunk
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 2 * kEpiChunkBytes;   // double-buffered
 
+// Division by a launch constant d (1 <= d <= 2^31) as a multiply-high, an add
+// and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, section 4): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, floor(x / d) = (umulhi(x, m) + x) >> l for
+// every 32-bit x, the sum taken in 33 bits.  The kernels' per-unit index
+// arithmetic (unit -> tile, row -> output position, k-step -> tap) divides
+// by these instead of issuing integer divisions.
+struct FastDiv {
+    uint32_t d, mul, shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d < 1u ? 1u : d, 1u, 0u};
+    while ((1ull << f.shift) < f.d) ++f.shift;
+    f.mul = static_cast<uint32_t>((((1ull << 32) * ((1ull << f.shift) - f.d)) / f.d) + 1ull);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv& f) {
+    return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(x, f.mul)) + x) >> f.shift);
+}
+
 struct KParams {
     // convolution geometry (A coordinates)
     int N, D, H, W, C;
@@ -118,6 +140,12 @@ struct KParams {
     const float* bias;  // fp32 [K] added after the scales, or NULL
     int* status;        // device status word
     unsigned long long wait_ns;
+    // divisors of the per-unit index arithmetic, filled at launch from the
+    // fields above (set_divisors): units per split, units per raster group,
+    // group_m, temporal planes (N * Do) and H*W tiles, Do, Ho, Wo, taps, S, R;
+    // rows32: every row index (plus a tile) fits in 31 bits
+    FastDiv f_tiles, f_group, f_gm, f_planes, f_hw_tiles, f_Do, f_Ho, f_Wo, f_taps, f_S, f_R;
+    int rows32;
 };
 
 // The tensor maps of one launch: A, B and the output for each row phase
