@@ -175,9 +175,17 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: bf16 or float8_e4m3fn")
 
 
-def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+# the current stream's raw handle without building a Stream object (torch's
+# own accessor where it exists; the public API otherwise)
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: Optional[int] = None):
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_current_stream is not None and device is not None:
+        return ctypes.c_void_p(_raw_current_stream(device))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -280,6 +288,7 @@ def set_overrides(**fields) -> dict:
         setattr(o, k, -1 if v is None else int(v))
     _check(lib.conv_set_overrides(ctypes.byref(o)), "conv_set_overrides")
     old, _current_overrides = _current_overrides, {k: v for k, v in vals.items() if v is not None}
+    _shape_cache.clear()   # plans (and so workspace sizes) may change with the overrides
     return old
 
 
@@ -322,6 +331,40 @@ def conv_get_device_status_stream(stream: Optional[torch.cuda.Stream] = None) ->
     return int(v.value)
 
 
+# ------------------------------------------------------------------ per-shape cache
+# A forward call's output dims, its marshalled shape arguments and (when the
+# caller gives no workspace) the plan's workspace size depend only on the
+# shapes, stride / pad / dilation, dtype and device (and on the overrides,
+# whose change clears the cache), so they are computed once per problem.
+# A stale size could not change a result: the library plans within the
+# workspace it is given.
+
+class _FwdShape:
+    __slots__ = ("od", "xd", "wd", "st", "pa", "di", "need")
+
+    def __init__(self, x_shape, w_shape, st, pa, di):
+        self.od = conv_out_dims(x_shape, w_shape, st, pa, di)
+        self.xd, self.wd = _I64_5(*x_shape), _I64_5(*w_shape)
+        self.st, self.pa, self.di = _I32_3(*st), _I32_3(*pa), _I32_3(*di)
+        self.need = None
+
+
+_shape_cache: dict = {}
+_SHAPE_CACHE_MAX = 256
+
+
+def _fwd_shape(x: torch.Tensor, w: torch.Tensor, stride, pad, dil, dtype: int) -> _FwdShape:
+    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
+    key = (tuple(x.shape), tuple(w.shape), st, pa, di, dtype, x.device.index)
+    e = _shape_cache.get(key)
+    if e is None:
+        e = _FwdShape(key[0], key[1], st, pa, di)
+        if len(_shape_cache) >= _SHAPE_CACHE_MAX:
+            _shape_cache.clear()
+        _shape_cache[key] = e
+    return e
+
+
 # ------------------------------------------------------------------ device calls
 
 def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
@@ -337,7 +380,7 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
     and none is given (``split_k=False`` runs without)."""
     if act not in ACT_CODES:
         raise ValueError(f"act must be one of {sorted(ACT_CODES)}")
-    lib = load_library()
+    lib = _lib or load_library()
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x must be [N,D,H,W,C] and w [K,T,R,S,C]")
     dtype = _dtype_code(x)
@@ -349,36 +392,36 @@ def conv_fwd(x: torch.Tensor, w: torch.Tensor, stride=1, pad=0, dil=1,
     if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (w.shape[0],)):
         raise TypeError("bias must be a float32 device tensor of shape [K]")
     _require_cuda(x, w, scale_x, scale_w, out, workspace, bias)
-    st, pa, di = _triple(stride), _triple(pad), _triple(dil)
-    od = conv_out_dims(tuple(x.shape), tuple(w.shape), st, pa, di)
+    e = _fwd_shape(x, w, stride, pad, dil, dtype)
     if out is None:
-        out = torch.empty(od, dtype=torch.bfloat16, device=x.device)
-    elif tuple(out.shape) != od or out.dtype != torch.bfloat16:
-        raise ValueError(f"out must be bf16 {od}")
+        out = torch.empty(e.od, dtype=torch.bfloat16, device=x.device)
+    elif tuple(out.shape) != e.od or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 {e.od}")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     elif split_k:
-        need = conv_fwd_plan(tuple(x.shape), tuple(w.shape), st, pa, di, dtype)["workspace_bytes"]
-        if need:
-            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-            ws_ptr, ws_bytes = workspace.data_ptr(), need
+        if e.need is None:
+            e.need = conv_fwd_plan(tuple(x.shape), tuple(w.shape), stride, pad, dil,
+                                   dtype)["workspace_bytes"]
+        if e.need:
+            workspace = torch.empty(e.need, dtype=torch.uint8, device=x.device)
+            ws_ptr, ws_bytes = workspace.data_ptr(), e.need
     if act != "none":
-        rc = lib.conv_fwd_bias_act(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(),
-                                   _I64_5(*w.shape), _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype,
-                                   _ptr(scale_x), _ptr(scale_w), _ptr(bias), ACT_CODES[act],
-                                   out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
+        rc = lib.conv_fwd_bias_act(x.data_ptr(), e.xd, w.data_ptr(), e.wd, e.st, e.pa, e.di,
+                                   dtype, _ptr(scale_x), _ptr(scale_w), _ptr(bias),
+                                   ACT_CODES[act], out.data_ptr(), ws_ptr, ws_bytes,
+                                   _stream_handle(stream, x.device.index))
         _check(rc, "conv_fwd_bias_act")
     elif bias is None:
-        rc = lib.conv_fwd(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
-                          _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
-                          _ptr(scale_w), out.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
+        rc = lib.conv_fwd(x.data_ptr(), e.xd, w.data_ptr(), e.wd, e.st, e.pa, e.di, dtype,
+                          _ptr(scale_x), _ptr(scale_w), out.data_ptr(), ws_ptr, ws_bytes,
+                          _stream_handle(stream, x.device.index))
         _check(rc, "conv_fwd")
     else:
-        rc = lib.conv_fwd_bias(x.data_ptr(), _I64_5(*x.shape), w.data_ptr(), _I64_5(*w.shape),
-                               _I32_3(*st), _I32_3(*pa), _I32_3(*di), dtype, _ptr(scale_x),
-                               _ptr(scale_w), bias.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes,
-                               _stream_handle(stream))
+        rc = lib.conv_fwd_bias(x.data_ptr(), e.xd, w.data_ptr(), e.wd, e.st, e.pa, e.di, dtype,
+                               _ptr(scale_x), _ptr(scale_w), bias.data_ptr(), out.data_ptr(),
+                               ws_ptr, ws_bytes, _stream_handle(stream, x.device.index))
         _check(rc, "conv_fwd_bias")
     return out
 

@@ -818,16 +818,15 @@ cudaError_t launch_pack_tma(const CUtensorMap* in_map, long long N, long long C,
     const uint32_t sb = fp8 ? TmaPackShape<1>::kStageBytes : TmaPackShape<0>::kStageBytes;
     const size_t smem = 1024 + static_cast<size_t>(stages) * sb + 16u * stages + 16;
     cudaError_t e;
+    static std::atomic<int> smem_set[2][kMaxDevices];
     if (fp8) {
-        e = cudaFuncSetAttribute(pack_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        e = ensure_dynamic_smem(pack_tma_kernel<1>, smem, smem_set[1]);
         if (e != cudaSuccess) return e;
         pack_tma_kernel<1><<<static_cast<unsigned>(grid), kTmaPackThreads, smem, stream>>>(
             *in_map, C, S, out, amax_bits, scale_out, c_tiles, s_tiles, tiles, stages, status,
             wait_ns);
     } else {
-        e = cudaFuncSetAttribute(pack_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        e = ensure_dynamic_smem(pack_tma_kernel<0>, smem, smem_set[0]);
         if (e != cudaSuccess) return e;
         pack_tma_kernel<0><<<static_cast<unsigned>(grid), kTmaPackThreads, smem, stream>>>(
             *in_map, C, S, out, amax_bits, scale_out, c_tiles, s_tiles, tiles, stages, status,

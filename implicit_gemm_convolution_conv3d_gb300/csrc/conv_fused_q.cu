@@ -662,8 +662,8 @@ template <int PAIR>
 cudaError_t launch_fq(const CUtensorMap* w_map, const FQParams& p, int grid, size_t smem,
                       cudaStream_t stream) {
     auto kern = conv_fused_q_kernel<PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);

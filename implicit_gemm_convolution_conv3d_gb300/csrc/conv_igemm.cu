@@ -945,8 +945,8 @@ template <int AM, int F8, int PAIR>
 cudaError_t launch_one(const TMaps* tm, const KParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
     auto kern = conv_igemm_kernel<AM, F8, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     const int threads = (AM == AM_GEMM_GATHER) ? 320 : 192;
     cudaLaunchConfig_t cfg = {};

@@ -2,6 +2,7 @@
 // library (conv3d_api.cu) and the kernel translation units.  Not part of the
 // public ABI.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -86,6 +87,30 @@ inline FastDiv make_fastdiv(uint32_t d) {
 
 __device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv& f) {
     return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(x, f.mul)) + x) >> f.shift);
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) only when this kernel has
+// not yet been allowed `smem` bytes on the current device: `slots` (one per
+// kernel, static in its launcher) remembers the largest size set on each
+// device, so repeated launches (22 per call on long reductions) skip the
+// driver call.  The attribute belongs to the device context, so a
+// cudaDeviceReset invalidates it like the library's other per-device state.
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel kern, size_t smem, std::atomic<int>* slots) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int want = static_cast<int>(smem);
+    if (dev >= 0 && dev < kMaxDevices && slots[dev].load(std::memory_order_acquire) >= want)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        int cur = slots[dev].load(std::memory_order_relaxed);
+        while (cur < want && !slots[dev].compare_exchange_weak(cur, want, std::memory_order_acq_rel)) {
+        }
+    }
+    return e;
 }
 
 struct KParams {

@@ -266,3 +266,26 @@ def test_ncdhw_plan_coverage(pkg):
     with pytest.raises(pkg.ConvError) as e:   # C of x (dim 1) against w
         pkg.conv_fwd_ncdhw_plan((1, 64, 4, 8, 8), (32, 3, 1, 1, 32), 1, 0, 1, 0, sms)
     assert e.value.status == pkg.CONV_ERR_INVALID
+
+
+def test_forward_shape_cache(pkg):
+    """The binding computes a problem's output dims and marshalled shape
+    arguments once: the same shapes and conv parameters return the same
+    entry, any difference a new one, and installing overrides (which can
+    change plans and so workspace sizes) empties the cache."""
+    x = torch.empty((2, 5, 9, 11, 64), dtype=torch.bfloat16)
+    w = torch.empty((96, 3, 3, 3, 64), dtype=torch.bfloat16)
+    e1 = pkg._fwd_shape(x, w, 1, 1, 1, 0)
+    assert e1 is pkg._fwd_shape(x, w, (1, 1, 1), [1, 1, 1], 1, 0)
+    assert e1.od == pkg.conv_out_dims(tuple(x.shape), tuple(w.shape), 1, 1, 1) == (2, 5, 9, 11, 96)
+    assert tuple(e1.xd) == tuple(x.shape) and tuple(e1.wd) == tuple(w.shape)
+    e2 = pkg._fwd_shape(x, w, 2, 1, 1, 0)
+    assert e2 is not e1 and e2.od == (2, 3, 5, 6, 96)
+    assert pkg._fwd_shape(x, w, 1, 1, 1, 1) is not e1          # dtype is part of the key
+    assert pkg._fwd_shape(x, w, 1, 1, 1, 0) is e1
+    try:
+        pkg.set_overrides(stages=3)
+        assert pkg._fwd_shape(x, w, 1, 1, 1, 0) is not e1
+    finally:
+        pkg.set_overrides()
+    assert pkg._fwd_shape(x, w, 1, 1, 1, 0) is not e1   # cleared again by the reset

@@ -491,3 +491,27 @@ def test_kernel_launch_counts(pkg):
     n = pkg.conv_fwd_kernel_launches(video.x_shape, video.w_shape, video.stride, video.pad,
                                      video.dil, 0, 0)
     assert n > 4   # the long reduction runs in slices of whole waves
+
+
+def test_launches_on_the_current_stream(pkg):
+    """With no stream argument the kernels go to the caller's current stream:
+    queued behind a ~50 ms spin on a side stream made current, the output is
+    still untouched once the default stream has drained, and correct once
+    the side stream has."""
+    xs, ws = (2, 5, 9, 11, 64), (96, 3, 3, 3, 64)
+    x = cw.randn_bf16(xs, 1200, 1.0, "cuda")
+    w = cw.randn_bf16(ws, 1201, 1.0 / np.sqrt(27 * 64), "cuda")
+    ref = pkg.conv_fwd(x, w, 1, 1, 1)
+    out = torch.full(ref.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws_t = torch.empty(max(16, pkg.conv_fwd_workspace_size(xs, ws, 1, 1, 1)), dtype=torch.uint8,
+                       device="cuda")
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(100_000_000)            # ~50 ms of SM cycles on the side stream
+        pkg.conv_fwd(x, w, 1, 1, 1, out=out, workspace=ws_t)
+    torch.cuda.default_stream().synchronize()
+    assert torch.isnan(out.float()).all(), "the conv did not wait for the side stream"
+    side.synchronize()
+    assert pkg.conv_get_device_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
