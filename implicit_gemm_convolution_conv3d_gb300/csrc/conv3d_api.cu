@@ -1514,10 +1514,20 @@ int fq_plan(const Geo& g, const DeviceInfo* dev, FqPlan* fp) {
     const long long reach = static_cast<long long>(p.ph) * p.Wp + p.pw;
     p.L = static_cast<int>((128 + 2 * reach + 31) / 32 * 32);
     p.strip_bytes = static_cast<uint32_t>(8 * p.L * 16);
-    p.b_stage_bytes = static_cast<uint32_t>((p.BN >> pair) * 128);
     const size_t strips = (2 * static_cast<size_t>(p.strip_bytes) + 1023) / 1024 * 1024;
     const size_t staging = (static_cast<size_t>(p.strip_bytes) + 1023) / 1024 * 1024;
     const size_t fixed = 1024 + strips + staging + 160;
+    // two taps per weight stage (eight MMAs per barrier round instead of
+    // four: the single issuing thread spends a fixed cost per round -- wait,
+    // fence, commit -- that four 128-cycle MMAs do not cover) when three such
+    // stages fit; the k_bytes override forces one (128) or two (256)
+    const uint32_t tap_bytes = static_cast<uint32_t>((p.BN >> pair) * 128);
+    const size_t avail = static_cast<size_t>(dev->smem_optin) > fixed
+                             ? static_cast<size_t>(dev->smem_optin) - fixed : 0;
+    p.tap_group = (g.R * g.S >= 2 && avail / (2 * tap_bytes + 16) >= 3) ? 2 : 1;
+    if (ov.k_bytes == 128) p.tap_group = 1;
+    if (ov.k_bytes == 256 && g.R * g.S >= 2) p.tap_group = 2;
+    p.b_stage_bytes = static_cast<uint32_t>(p.tap_group) * tap_bytes;
     if (static_cast<size_t>(dev->smem_optin) < fixed + 2 * (p.b_stage_bytes + 16)) {
         set_error("fused channel-major e4m3 conv: the filter's strip does not fit in shared "
                   "memory (frame too wide for the filter height)");
@@ -1982,21 +1992,24 @@ int conv_fwd_ncdhw_fp8(const void* x, const int64_t x_dims[5], const void* w,
     p.out = out;
     p.status = dev->status;
     p.wait_ns = g_wait_ns;
-    // the e4m3 weight [K, R*S, C] as {C, R*S, K}: boxes of 128 channel bytes x
-    // one tap x (BN >> pair) filters, 128-byte swizzle
+    // the e4m3 weight [K, R*S, C] as {C, K, R*S}: boxes of 128 channel bytes x
+    // (BN >> pair) filters x tap_group taps, 128-byte swizzle, so a stage is
+    // tap_group blocks of (BN >> pair) rows x 128 bytes (taps past R*S, in the
+    // last group of an odd count, read as zeros)
     CUtensorMap wm;
     {
         const cuuint64_t taps = static_cast<cuuint64_t>(g.R * g.S);
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C), taps, static_cast<cuuint64_t>(g.K)};
-        const cuuint64_t str[2] = {static_cast<cuuint64_t>(g.C), static_cast<cuuint64_t>(g.C) * taps};
-        const cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(p.BN >> p.pair)};
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C), static_cast<cuuint64_t>(g.K), taps};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(g.C) * taps, static_cast<cuuint64_t>(g.C)};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(p.BN >> p.pair),
+                                   static_cast<cuuint32_t>(p.tap_group)};
         if ((rc = encode_tiled(&wm, 1, 3, w, dims, str, box, 128))) return rc;
     }
     if (overrides().log == 1)
         std::fprintf(stderr, "conv_fwd_ncdhw_fp8: BN=%d pair=%d L=%d strip=%u b_stages=%d "
-                     "m_tiles=%d n_tiles=%d chunks=%d grid=%d smem=%zu keep=%d\n", p.BN, p.pair,
-                     p.L, p.strip_bytes, p.b_stages, p.m_tiles, p.n_tiles, p.chunks, fp.grid,
-                     fp.smem, p.scratch ? 1 : 0);
+                     "tap_group=%d m_tiles=%d n_tiles=%d chunks=%d grid=%d smem=%zu keep=%d\n",
+                     p.BN, p.pair, p.L, p.strip_bytes, p.b_stages, p.tap_group, p.m_tiles,
+                     p.n_tiles, p.chunks, fp.grid, fp.smem, p.scratch ? 1 : 0);
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     e = launch_amax_bf16(x, g.N * g.C * g.D * g.H * g.W, amax, dev->num_sms, stream);

@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(kFqThreads, 1)
             for (int i = 0; ok && fq_unit(i, unit0, ustride, p, t); ++i) {
                 const int n0 = t.nt * p.BN + static_cast<int>(rank) * (fq_cols(t.nt, p) >> PAIR);
                 for (int cc = 0; cc < p.chunks && ok; ++cc) {
-                    for (int tap = 0; tap < taps; ++tap) {
+                    // one box per group of tap_group consecutive taps
+                    for (int tap = 0; tap < taps; tap += p.tap_group) {
                         if (!wait_bar(bempty0 + 8 * stage, phase ^ 1u, abort_flag, p.status,
                                       p.wait_ns)) {
                             ok = false;
@@ -342,11 +343,11 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                             if (rank == 0) mbar_arrive_expect_tx(fb, 2u * p.b_stage_bytes);
                             fb = mapa_shared(fb, 0);
                             tma_load_3d_pair(ring + stage * p.b_stage_bytes, &w_map, fb,
-                                             cc * kFqChunk, tap, n0);
+                                             cc * kFqChunk, n0, tap);
                         } else {
                             mbar_arrive_expect_tx(fb, p.b_stage_bytes);
                             tma_load_3d(ring + stage * p.b_stage_bytes, &w_map, fb, cc * kFqChunk,
-                                        tap, n0);
+                                        n0, tap);
                         }
                         misc[2] = ++issued;
                         if (++stage == p.b_stages) {
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(kFqThreads, 1)
             const uint32_t a_buf_step = p.strip_bytes >> 4;
             const uint32_t a_kstep = (2u * lbo) >> 4;
             const uint32_t b_stage_step = p.b_stage_bytes >> 4;
+            const uint32_t b_tap_step = (p.b_stage_bytes / p.tap_group) >> 4;   // one tap's block
             const int row_skip = p.Wp - p.S;   // window offset from (r, S) to (r + 1, 0)
             int stage = 0, acc_iter = 0, chunk_iter = 0;
             uint32_t phase = 0, consumed = 0;
@@ -394,22 +396,33 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                     tc_fence_after();
                     const uint64_t abuf = adesc0 + static_cast<uint64_t>(sb) * a_buf_step;
                     int win = 0, s = 0;   // window offset of tap (r, s): r * Wp + s
-                    for (int tap = 0; tap < taps; ++tap) {
+                    for (int tap0 = 0; tap0 < taps; tap0 += p.tap_group) {
+                        // one weight stage: tap_group taps (fewer in the last
+                        // group of an odd count), each a block of filter rows
                         if (!wait_bar(bfull0 + 8 * stage, phase, abort_flag, p.status, p.wait_ns)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         misc[3] = ++consumed;
-                        const uint64_t a = abuf + static_cast<uint64_t>(win);
-                        const uint64_t b = bdesc0 + static_cast<uint64_t>(stage) * b_stage_step;
+                        const int ntap = min(p.tap_group, taps - tap0);
+                        uint64_t b = bdesc0 + static_cast<uint64_t>(stage) * b_stage_step;
+                        for (int j = 0; j < ntap; ++j, b += b_tap_step) {
+                            const uint64_t a = abuf + static_cast<uint64_t>(win);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {   // 32 channel bytes per MMA
-                            if (PAIR)
-                                tc_mma_f8_pair(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc, accum);
-                            else
-                                tc_mma_f8(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc, accum);
-                            accum = 1u;
+                            for (int kk = 0; kk < 4; ++kk) {   // 32 channel bytes per MMA
+                                if (PAIR)
+                                    tc_mma_f8_pair(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc,
+                                                   accum);
+                                else
+                                    tc_mma_f8(d_tmem, a + kk * a_kstep, b + 2u * kk, idesc, accum);
+                                accum = 1u;
+                            }
+                            ++win;
+                            if (++s == p.S) {
+                                s = 0;
+                                win += row_skip;
+                            }
                         }
                         if (PAIR)
                             tc_commit_pair(bempty0 + 8 * stage, 3);
@@ -418,11 +431,6 @@ __global__ void __launch_bounds__(kFqThreads, 1)
                         if (++stage == p.b_stages) {
                             stage = 0;
                             phase ^= 1u;
-                        }
-                        ++win;
-                        if (++s == p.S) {
-                            s = 0;
-                            win += row_skip;
                         }
                     }
                     // the strip buffer is free in both CTAs once these MMAs have read it

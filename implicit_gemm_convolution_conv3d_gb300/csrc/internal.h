@@ -194,9 +194,10 @@ struct FQParams {
     int chunks;           // ceil(C / 128): 128-channel reduction chunks
     int BN;               // tile columns (multiple of 32, <= 256)
     int b_stages;         // weight ring depth
+    int tap_group;        // filter taps per weight stage (1 or 2): one barrier round each
     int L;                // strip positions per CTA (multiple of 32)
     uint32_t strip_bytes; // 8 slices x L x 16 bytes
-    uint32_t b_stage_bytes;
+    uint32_t b_stage_bytes; // tap_group x (BN >> pair) x 128 bytes
     uint32_t idesc;       // tcgen05 instruction descriptor (e4m3 x e4m3, M, N)
     uint32_t tmem_cols;
     int pair;
@@ -215,7 +216,9 @@ constexpr int kFqThreads = 480;   // warp 0 weights (TMA), 1 MMA, 2-5 epilogue, 
                                   // 7-14 converters
 
 // Launch the fused channel-major e4m3 convolution (w_map: the e4m3 KTRSC
-// weight as {C, R*S, K} with boxes {128, 1, BN >> pair}, 128-byte swizzle).
+// weight as {C, K, R*S} with boxes {128, BN >> pair, tap_group}, 128-byte
+// swizzle: a stage holds tap_group consecutive taps' filter rows, one
+// (BN >> pair) x 128-byte block per tap).
 cudaError_t launch_fused_q(const CUtensorMap* w_map, const FQParams& p, int grid, size_t smem,
                            cudaStream_t stream);
 

@@ -64,15 +64,18 @@ def _run(pkg, xs, ws, seed, bias=False, small_ws=False):
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 @pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("small_ws", [False, True], ids=["ahead", "in-place"])
-def test_fused_quantising_loader_matches_oracle(pkg, case, pair, small_ws):
+@pytest.mark.parametrize("k_bytes", [128, 256], ids=["tap", "two-taps"])
+def test_fused_quantising_loader_matches_oracle(pkg, case, pair, small_ws, k_bytes):
     """With the preferred workspace the converters work one m-tile ahead into
     a scratch and the strips are copied back for every column tile; with only
     the amax word they convert each chunk in place: the same values either
-    way."""
+    way.  Weight stages hold one filter tap or two (the last group of an odd
+    tap count half empty)."""
     xs, ws = case
-    with pkg.overrides(pair=pair):
+    with pkg.overrides(pair=pair, k_bytes=k_bytes):
         _, _, _, _, y, ref, _ = _run(pkg, xs, ws, CASES.index(case), small_ws=small_ws)
-    assert_close(as_f64(y), ref, f"fused e4m3 NCDHW {case} pair={pair} small_ws={small_ws}")
+    assert_close(as_f64(y), ref,
+                 f"fused e4m3 NCDHW {case} pair={pair} small_ws={small_ws} k_bytes={k_bytes}")
 
 
 def test_fused_with_bias_and_against_pack_then_conv(pkg):
