@@ -123,3 +123,30 @@ def test_fused_unsupported_shapes(pkg, ws, stride, pad):
     with pytest.raises(pkg.ConvError) as e:
         pkg.conv_fwd_ncdhw_fp8(x, qw, 1, (0, 1, 1), 1)
     assert e.value.status == pkg.CONV_ERR_UNSUPPORTED
+
+
+def _fuzz_cases(n=16, seed=20261):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        N, D = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        C = 16 * int(rng.integers(1, 11))                 # up to 160: partial 128-channel chunks
+        H, W = int(rng.integers(1, 25)), int(rng.integers(1, 25))
+        K = 32 * int(rng.integers(1, 9))                  # up to 256: partial column tiles
+        R, S = (int(v) for v in rng.choice([1, 3, 5], size=2))
+        cases.append(((N, C, D, H, W), (K, C, 1, R, S), int(rng.integers(0, 2)),
+                      int(rng.choice([128, 256])), bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_fused_loader_fuzz(pkg, i):
+    """Seeded random problems (N, D up to 2 / 3, C up to 160, H and W 1..24,
+    K up to 256, 1 / 3 / 5-tap filter rows and columns), each with a random
+    CTA-pair choice, one or two taps per weight stage and either workspace
+    mode, against the oracle's pack + conv."""
+    xs, ws, pair, k_bytes, small_ws = _fuzz_cases()[i]
+    with pkg.overrides(pair=pair, k_bytes=k_bytes):
+        _, _, _, _, y, ref, _ = _run(pkg, xs, ws, 100 + i, small_ws=small_ws)
+    assert_close(as_f64(y), ref, f"fuzz {i}: x {xs} w {ws} pair={pair} k_bytes={k_bytes} "
+                                 f"small_ws={small_ws}")
