@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,11 +76,15 @@ def load_peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the library's sources without their // comments and blank
+    lines: changes to the code (not to its comments) void measured counters."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "implicit_gemm_convolution_conv3d_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            text = open(os.path.join(csrc, f), encoding="utf-8").read()
+            code = [re.sub(r"//.*$", "", line).rstrip() for line in text.split("\n")]
+            h.update(f.encode() + b"\0" + "\n".join(c for c in code if c).encode())
     return h.hexdigest()[:16]
 
 

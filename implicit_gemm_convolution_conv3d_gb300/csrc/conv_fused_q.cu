@@ -20,25 +20,31 @@
 // is stored K-major without swizzle: 8 slices of 16 channels (one per 16-byte
 // core-matrix column), each slice L rows of 16 bytes (SBO 128 bytes between
 // 8-row groups, LBO L * 16 bytes between slices).  Each input element is
-// converted about L / 128 times (1.5 for a 3x3 filter on a 90-wide frame)
+// converted about L / 128 times (2.5 for a 3x3 filter on a 90-wide frame)
 // instead of once per tap, and rows with wp outside the image (2 of every
 // Wp) are computed and dropped.
 //
-// Warp roles (448 threads):
-//   warp 0      TMA producer of the e4m3 KTRSC weight: per (chunk, tap) one
-//               box of 128 channel bytes x (BN >> pair) filters, 128-byte
-//               swizzle, into a ring (full / empty mbarriers);
+// Warp roles (480 threads):
+//   warp 0      TMA producer of the e4m3 KTRSC weight: per chunk and group of
+//               tap_group consecutive taps one box of 128 channel bytes x
+//               (BN >> pair) filters x tap_group taps, 128-byte swizzle, into
+//               a ring (full / empty mbarriers);
 //   warp 1      TMEM allocation; lane 0 issues tcgen05.mma kind::f8f6f4
-//               (cta_group::2 for CTA pairs) for each tap of each chunk;
+//               (cta_group::2 for CTA pairs): per weight stage the four MMAs
+//               of each of its taps, then one commit;
 //   warps 2..5  epilogue: tcgen05.ld -> scale_x * scale_w (+ bias) -> bf16 ->
 //               16-byte stores of the valid rows; overlaps the next unit;
-//   warps 6..13 converters: warp k builds slice k (16 channels) of the next
-//               chunk's strip into one of two strip buffers: each lane takes 8
-//               consecutive image positions of the frame rows the strip
-//               covers, loads them from the 16 channel planes (16-byte loads,
-//               512 contiguous bytes of a plane per warp), quantises them to
-//               e4m3 and writes each position's 16 channel bytes to its strip
-//               row; strip rows with no image position are zeroed.
+//   warp 6      strip loader (with a scratch): copies each converted strip
+//               back from this CTA's scratch for every column tile;
+//   warps 7..14 converters: warp k builds slice k (16 channels) of a chunk's
+//               strip -- one m-tile ahead into the scratch through a staging
+//               buffer when there is one, else in place in a strip buffer --:
+//               each lane takes 8 consecutive image positions of the frame
+//               rows the strip covers, loads them from the 16 channel planes
+//               (16-byte loads, 512 contiguous bytes of a plane per warp),
+//               quantises them to e4m3 and writes each position's 16 channel
+//               bytes to its strip row; strip rows with no image position are
+//               zeroed.
 // Every wait is bounded; on expiry the kernel records CONV_ERR_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
