@@ -87,7 +87,8 @@ def _all_bf16_as_f32():
 def test_encode_matches_torch_inside_finite_range(scale):
     vals = _all_bf16_as_f32()
     finite = np.isfinite(vals)
-    q = (vals[finite] / np.float32(scale)).astype(np.float32)
+    with np.errstate(over="ignore"):    # large values over a small scale: inf, dropped below
+        q = (vals[finite] / np.float32(scale)).astype(np.float32)
     keep = np.abs(q) < 464.0            # torch's cast is non-saturating beyond this
     q = q[keep]
     ref = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
