@@ -402,7 +402,9 @@ int conv_fwd_noalloc(const void* x, const int64_t x_dims[5], const void* w,
  * read from the environment: only conv_set_overrides changes these. */
 typedef struct {
     int tile_n;          /* tile columns: 32..256, a multiple of 32 */
-    int k_bytes;         /* bytes of one row per k-step: 32, 64, 128 or 256 */
+    int k_bytes;         /* bytes of one row per k-step: 32, 64, 128 or 256
+                            (conv_fwd_ncdhw_fp8: 128 / 256 = one / two filter
+                            taps per weight stage) */
     int stages;          /* shared-memory pipeline depth */
     int group_m;         /* raster group: consecutive m-tiles per group (>= 1) */
     int splits;          /* split-K factor (>= 1) */
