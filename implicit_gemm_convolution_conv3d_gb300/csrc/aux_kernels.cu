@@ -694,6 +694,41 @@ __global__ void __launch_bounds__(256) patch_gather_kernel(
     }
 }
 
+// The same gather with one thread per output word (problems whose word
+// counts fit in 32 bits): word w of `a` is row m = w / pitch, word i of it;
+// i < T*R*seg reads segment (t, r) = divmod(i / seg, R) at offset i % seg of
+// patch (n, od, oh, ow), the rest is the zero tail.  The indices come from
+// multiply-shift divisors set on the host (FastDiv), so a thread spends a few
+// instructions per 16-byte word; consecutive threads store consecutive
+// words (whole rows per warp instruction) and read the patch's contiguous
+// S*C-element segments.
+struct GatherFlat {
+    FastDiv f_pitch, f_seg, f_r, f_wo, f_ho, f_do;
+    uint32_t total, row_words, T, R, H, D, Wrow, seg;
+};
+
+template <typename Word>
+__global__ void __launch_bounds__(256) patch_gather_flat_kernel(const Word* __restrict__ x,
+                                                                Word* __restrict__ a, GatherFlat g) {
+    griddep_launch_dependents();
+    const uint32_t step = gridDim.x * blockDim.x;
+    for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < g.total; w += step) {
+        const uint32_t m = fdiv(w, g.f_pitch);
+        const uint32_t i = w - m * g.f_pitch.d;
+        Word v = zero_word<Word>();
+        if (i < g.row_words) {
+            const uint32_t sid = fdiv(i, g.f_seg), off = i - sid * g.seg;
+            const uint32_t t = fdiv(sid, g.f_r), r = sid - t * g.R;
+            const uint32_t q1 = fdiv(m, g.f_wo), ow = m - q1 * g.f_wo.d;
+            const uint32_t q2 = fdiv(q1, g.f_ho), oh = q1 - q2 * g.f_ho.d;
+            const uint32_t n = fdiv(q2, g.f_do), od = q2 - n * g.f_do.d;
+            const uint32_t plane = (n * g.D + od * g.T + t) * g.H + oh * g.R + r;
+            v = __ldg(x + static_cast<size_t>(plane) * g.Wrow + ow * g.seg + off);
+        }
+        a[w] = v;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
@@ -702,6 +737,48 @@ cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D
                                 cudaStream_t stream) {
     const long long M = N * Do * Ho * Wo;
     const long long seg_b = static_cast<long long>(S) * C * elt, row_b = W * C * elt;
+    // one thread per word when every index fits in 32 bits: 16-, 4-, 2- or
+    // 1-byte words, whichever divides the segment, row and pitch bytes
+    const int wb = (seg_b % 16 == 0 && row_b % 16 == 0 && pitch_bytes % 16 == 0) ? 16
+                   : (seg_b % 4 == 0 && row_b % 4 == 0 && pitch_bytes % 4 == 0) ? 4
+                   : elt;
+    const long long total_w = M * (pitch_bytes / wb);
+    const long long x_words = N * D * H * (row_b / wb);
+    if (total_w > 0 && total_w < (1ll << 31) && x_words < (1ll << 31) && row_b % wb == 0 &&
+        seg_b % wb == 0 && pitch_bytes % wb == 0) {
+        GatherFlat g;
+        g.total = static_cast<uint32_t>(total_w);
+        g.seg = static_cast<uint32_t>(seg_b / wb);
+        g.row_words = static_cast<uint32_t>(static_cast<long long>(T) * R * g.seg);
+        g.T = static_cast<uint32_t>(T);
+        g.R = static_cast<uint32_t>(R);
+        g.H = static_cast<uint32_t>(H);
+        g.D = static_cast<uint32_t>(D);
+        g.Wrow = static_cast<uint32_t>(row_b / wb);
+        g.f_pitch = make_fastdiv(static_cast<uint32_t>(pitch_bytes / wb));
+        g.f_seg = make_fastdiv(g.seg);
+        g.f_r = make_fastdiv(g.R);
+        g.f_wo = make_fastdiv(static_cast<uint32_t>(Wo));
+        g.f_ho = make_fastdiv(static_cast<uint32_t>(Ho));
+        g.f_do = make_fastdiv(static_cast<uint32_t>(Do));
+        long long blk = (total_w + 255) / 256;
+        const long long cap = static_cast<long long>(num_sms) * 8;
+        if (blk > cap) blk = cap;
+        const unsigned grid = static_cast<unsigned>(blk < 1 ? 1 : blk);
+        if (wb == 16)
+            patch_gather_flat_kernel<uint4><<<grid, 256, 0, stream>>>(
+                static_cast<const uint4*>(x), static_cast<uint4*>(a), g);
+        else if (wb == 4)
+            patch_gather_flat_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+                static_cast<const uint32_t*>(x), static_cast<uint32_t*>(a), g);
+        else if (wb == 2)
+            patch_gather_flat_kernel<unsigned short><<<grid, 256, 0, stream>>>(
+                static_cast<const unsigned short*>(x), static_cast<unsigned short*>(a), g);
+        else
+            patch_gather_flat_kernel<unsigned char><<<grid, 256, 0, stream>>>(
+                static_cast<const unsigned char*>(x), static_cast<unsigned char*>(a), g);
+        return cudaGetLastError();
+    }
     long long blocks = (M + 7) / 8;
     const long long cap = static_cast<long long>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
