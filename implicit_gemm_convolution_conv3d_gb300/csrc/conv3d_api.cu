@@ -388,8 +388,9 @@ int make_plan(const Geo& g, int dtype, int num_sms, int smem_optin, size_t ws_av
         P->tma_row_bytes = (P->g_row_bytes + 15) / 16 * 16;
         P->amode = AM_GEMM_TMA;
         P->repack = 2;
-        P->repack_bytes = static_cast<size_t>((P->M * P->tma_row_bytes + 255) / 256 * 256) +
-                          static_cast<size_t>((g.K * P->tma_row_bytes + 255) / 256 * 256);
+        P->repack_bytes = static_cast<size_t>((P->M * P->tma_row_bytes + 255) / 256 * 256);
+        if (P->tma_row_bytes != P->g_row_bytes)   // weight rows copied to the pitch too
+            P->repack_bytes += static_cast<size_t>((g.K * P->tma_row_bytes + 255) / 256 * 256);
         if (ws_avail < P->repack_bytes) {
             set_error("the patch gather needs %s%lld bytes of workspace (conv_fwd_plan)", "",
                       static_cast<long long>(P->repack_bytes));
@@ -1220,6 +1221,10 @@ int plan_query(const Geo& g, bool ncdhw, int dtype, int num_sms, int* cls, int* 
     return CONV_OK;
 }
 
+// Patch class: the weight's rows (one patch of T*R*S*C elements each, KTRSC)
+// serve as GEMM rows in place when they are already at the TMA pitch.
+bool patch_weights_in_place(const Plan& P) { return P.g_row_bytes == P.tma_row_bytes; }
+
 int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
              const float* scale_x, const float* scale_w, const float* bias, int act, void* out,
              void* workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -1389,8 +1394,9 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
     const void* xa = x;
     const void* wa = w;
     if (P.repack == 2) {
-        // the patches gathered into GEMM rows, then the weights copied to the
-        // same 16-byte pitch, at the head of the workspace
+        // the patches gathered into GEMM rows at the head of the workspace,
+        // then (rows not a multiple of 16 bytes) the weights copied to the
+        // same 16-byte pitch after them
         unsigned char* wsb = static_cast<unsigned char*>(workspace);
         void* wc = wsb + (P.M * P.tma_row_bytes + 255) / 256 * 256;
         cudaError_t e = launch_patch_gather(
@@ -1398,14 +1404,16 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
             static_cast<int>(g.R), static_cast<int>(g.S), static_cast<int>(g.Do),
             static_cast<int>(g.Ho), static_cast<int>(g.Wo), wsb, P.tma_row_bytes, dev->num_sms,
             stream);
-        // each filter row is one patch of T*R*S*C elements (any byte count)
-        if (e == cudaSuccess)
+        // each filter row is one patch of T*R*S*C elements, already a GEMM row
+        // at the TMA pitch when its bytes are a multiple of 16 (read in place)
+        const bool w_in_place = patch_weights_in_place(P);
+        if (e == cudaSuccess && !w_in_place)
             e = launch_patch_gather(w, static_cast<int>(P.elt), g.K, 1, 1, 1,
                                     g.T * g.R * g.S * g.C, 1, 1, 1, 1, 1, 1, wc,
                                     P.tma_row_bytes, dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "patch gather launch");
         xa = wsb;
-        wa = wc;
+        wa = w_in_place ? w : wc;
     } else if (P.repack && P.phases == 2) {
         // the two aligned weight copies (plain, shifted by 8 bytes) at the head
         // of the workspace; x is read in place
@@ -1805,7 +1813,7 @@ int conv_fwd_kernel_launches(const int64_t x_dims[5], const int64_t w_dims[5],
     if ((rc = device_info(&dev))) return rc;
     Plan P;
     if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace_bytes, &P))) return rc;
-    int n = P.repack == 2 ? 2 : (P.repack ? 1 : 0);
+    int n = P.repack == 2 ? (patch_weights_in_place(P) ? 1 : 2) : (P.repack ? 1 : 0);
     int bounds[kMaxChunks + 1];
     n += P.slices > 1 ? plan_even_slices(P, P.slices, bounds) : 1;
     if (P.splits > 1) ++n;

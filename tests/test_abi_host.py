@@ -106,6 +106,16 @@ def test_plan_classifies_the_workloads(pkg):
     for k in (16, 14):
         p = pkg.conv_fwd_plan((8, 1, 224, 224, 3), (768, 1, k, k, 3), (1, k, k), 0, 1, 0, sms)
         assert p["class"] == "patch_gemm"
+        # gathered rows at a 16-byte pitch; weight rows that already are a
+        # multiple of 16 bytes (16*16*3 bf16 = 1536) are read in place, the
+        # 14*14*3 ones (1176 bytes) are copied to the 1184-byte pitch after them
+        m, row = 8 * (224 // k) ** 2, k * k * 3 * 2
+        pitch = (row + 15) // 16 * 16
+        up = lambda b: (b + 255) // 256 * 256
+        need = up(m * pitch) + (0 if row == pitch else up(768 * pitch))
+        if p["splits"] > 1:   # fp32 partials [splits, M, K] after the copies
+            need += p["splits"] * m * 768 * 4
+        assert p["workspace_bytes"] == need, (k, p["workspace_bytes"], need)
     assert {w.name for w in cw.WORKLOADS} >= {"tiny_conv3d_bf16", "video_conv3d_bf16"}
 
 
