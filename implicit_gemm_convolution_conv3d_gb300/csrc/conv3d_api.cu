@@ -1026,23 +1026,69 @@ long long tile_row_hi(const Plan& P, int mt) {
     return std::min<long long>(P.M, (mt + 1) * unit_rows);
 }
 
-// Bytes of x, as a prefix of whole (n, d) planes, that the output rows below
-// row_hi read: the last output plane (n, od) reaches input depth
-// od*sd - pd + (T-1)*dd at most, and output planes are in (n, d) order.
-long long x_prefix_bytes(const Geo& g, long long row_hi, long long plane_bytes) {
-    const long long q = (row_hi - 1) / (g.Ho * g.Wo);
+// The input that output rows [0, row_hi) read, in input planes ((n, d)
+// order, H rows of W*C elements each): planes [0, whole) entirely and rows
+// [0, rows) of planes [whole, part).  Output rows are output planes (n, od)
+// in order, then rows oh: the output planes before the last one read, at
+// most, every plane of the images before n and image n's planes up to depth
+// (od-1)*sd - pd + (T-1)*dd; the last one's rows up to oh read its planes up
+// to depth od*sd - pd + (T-1)*dd, input rows up to oh*sh - ph + (R-1)*dh.
+struct XReach {
+    long long whole, part, rows;
+};
+
+XReach x_reach(const Geo& g, long long row_hi) {
+    const long long r = row_hi - 1;
+    const long long oh = (r / g.Wo) % g.Ho;
+    const long long q = r / (g.Wo * g.Ho);
     const long long n = q / g.Do, od = q % g.Do;
-    const long long d = std::min<long long>(od * g.sd - g.pd + (g.T - 1) * g.dd, g.D - 1);
-    const long long planes = d < 0 ? n * g.D : n * g.D + d + 1;
-    return planes * plane_bytes;
+    const long long d_prev = std::min(g.D - 1, (od - 1) * g.sd - g.pd + (g.T - 1) * g.dd);
+    const long long d_last = std::min(g.D - 1, od * g.sd - g.pd + (g.T - 1) * g.dd);
+    const long long h = std::min(g.H - 1, oh * g.sh - g.ph + (g.R - 1) * g.dh);
+    XReach x;
+    x.whole = n * g.D + (od >= 1 ? std::max(d_prev, -1LL) + 1 : 0);
+    x.part = std::max(x.whole, n * g.D + std::max(d_last, -1LL) + 1);
+    x.rows = h < 0 ? 0 : h + 1;
+    return x;
+}
+
+// Copy (host to device, on stream s) the input rows within `need` that
+// `have` does not hold; ranges that meet go as one copy.
+cudaError_t copy_x_reach(const Geo& g, const XReach& have, const XReach& need,
+                         size_t plane_bytes, size_t row_bytes, const unsigned char* xh,
+                         unsigned char* xd, cudaStream_t s) {
+    auto held = [&](const XReach& r, long long p) {
+        return p < r.whole ? g.H : (p < r.part ? r.rows : 0);
+    };
+    size_t lo = 0, hi = 0;
+    for (long long p = have.whole; p < need.part; ++p) {
+        const long long a = held(have, p), b = held(need, p);
+        if (b <= a) continue;
+        const size_t s0 = static_cast<size_t>(p) * plane_bytes + static_cast<size_t>(a) * row_bytes;
+        const size_t s1 = static_cast<size_t>(p) * plane_bytes + static_cast<size_t>(b) * row_bytes;
+        if (hi > lo && s0 == hi) {
+            hi = s1;
+            continue;
+        }
+        if (hi > lo) {
+            cudaError_t e = cudaMemcpyAsync(xd + lo, xh + lo, hi - lo, cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) return e;
+        }
+        lo = s0;
+        hi = s1;
+    }
+    if (hi > lo) return cudaMemcpyAsync(xd + lo, xh + lo, hi - lo, cudaMemcpyHostToDevice, s);
+    return cudaSuccess;
 }
 
 // Split the m-tiles into chunks; bounds[0..n] (bounds[n] = m_tiles), returns n.
 // requested > 1: that many near-equal chunks.  requested == 0: chunks of
 // whole waves of units (a wave = the units the grid holds at once), so that
-// splitting the launch adds no partial waves: the first and last one block
-// long (short lead-in and tail), the rest shared evenly, at most 8 chunks.
-int plan_chunks(const Plan& P, int requested, int* bounds) {
+// splitting the launch adds no partial waves, the first one to four blocks
+// long, then a ramp of short chunks, the last one block long; at most
+// kMaxChunks chunks.
+int plan_chunks(const Plan& P, const Geo& g, long long x_row_bytes, long long w_bytes,
+                int requested, int* bounds) {
     const int MT = P.m_tiles;
     bounds[0] = 0;
     if (requested == 1 || MT < 2) {
@@ -1062,16 +1108,40 @@ int plan_chunks(const Plan& P, int requested, int* bounds) {
         bounds[1] = MT;
         return 1;
     }
-    const int n = static_cast<int>(std::min<long long>(8, nb));
-    long long blocks[8];
-    blocks[0] = 1;
-    if (n == 2) {
-        blocks[1] = nb - 1;
-    } else {
-        blocks[n - 1] = 1;
-        const long long mid = nb - 2, parts = n - 2;
-        for (int i = 0; i < parts; ++i) blocks[1 + i] = mid / parts + (i < mid % parts ? 1 : 0);
+    // the first chunk (whole blocks) runs as one wave per group of column
+    // tiles, each launched once its group's weights have landed: of up to
+    // four blocks (two or more left for the rest), take the length whose
+    // lead-in -- the input rows the chunk reads plus one weight group -- is
+    // the smallest (more blocks: more waves, so smaller weight groups)
+    const long long wpb = j * P.n_tiles / wave;   // waves per block
+    long long b0 = 1, best = -1;
+    for (long long b = 1; b <= 4 && (b == 1 || b <= nb - 2); ++b) {
+        const long long wv = b * wpb;
+        const long long groups =
+            (wv >= 2 && wv <= kMaxWGroups && P.n_tiles % wv == 0) ? wv : 1;
+        const XReach r = x_reach(g, tile_row_hi(P, static_cast<int>(b * j) - 1));
+        const long long lead = r.whole * g.H * x_row_bytes +
+                               (r.part - r.whole) * r.rows * x_row_bytes + w_bytes / groups;
+        if (best < 0 || lead < best) {
+            best = lead;
+            b0 = b;
+        }
     }
+    // then one block (the few input rows it adds are copied right after the
+    // weights, so it starts when the first chunk ends), then chunks doubling
+    // up to a sixth of the rest (each one's input copied while the one
+    // before runs), and one block last (a short copy-out after the last wave)
+    long long blocks[kMaxChunks];
+    int n = 0;
+    blocks[n++] = b0;
+    long long mid = nb - b0 - 1;   // blocks between the first and last chunk
+    const long long share = std::max(1LL, (mid + 5) / 6);
+    for (long long len = 1; mid > 0; len *= 2) {
+        const long long c = n == kMaxChunks - 2 ? mid : std::min({len, share, mid});
+        blocks[n++] = c;
+        mid -= c;
+    }
+    blocks[n++] = 1;
     long long acc = 0;
     for (int i = 0; i < n; ++i) {
         acc += blocks[i] * j;
@@ -1595,6 +1665,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         return rc;
     const long long plane_bytes = g.H * g.W * g.C * P.elt;
     const size_t x_bytes = static_cast<size_t>(g.N * g.D * plane_bytes);
+    const size_t x_row_bytes = static_cast<size_t>(g.W * g.C * P.elt);
     const size_t w_bytes = static_cast<size_t>(g.K * g.T * g.R * g.S * g.C * P.elt);
     const size_t row_bytes = static_cast<size_t>(g.K) * 2;   // one bf16 output row
     const unsigned char* xh = static_cast<const unsigned char*>(x_host);
@@ -1604,7 +1675,9 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
 
     int bounds[kMaxChunks + 1];
     const bool chunkable = !gemm_amode(P.amode) && P.splits == 1;
-    const int n = chunkable ? plan_chunks(P, chunks, bounds) : 1;
+    const int n = chunkable ? plan_chunks(P, g, static_cast<long long>(x_row_bytes),
+                                          static_cast<long long>(w_bytes), chunks, bounds)
+                            : 1;
     cudaError_t e;
     if (n == 1) {
         // one launch: copy in, convolve, copy out, all on the caller's stream
@@ -1665,20 +1738,20 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
                                pp->s_in);
     };
     if ((e = copy_w_group(0)) != cudaSuccess) what = "cudaMemcpyAsync (weights)";
-    size_t x_done = 0;
+    // input rows on the device so far; each slice first copies the rows it
+    // reads that are not there yet (the last one: everything left)
+    XReach x_have{0, 0, 0};
     for (int i = 0; i < n && !what; ++i) {
         const int mt0 = bounds[i], mt1 = bounds[i + 1];
         const long long row_lo = tile_row_lo(P, mt0), row_hi = tile_row_hi(P, mt1 - 1);
-        const size_t x_need =
-            i == n - 1 ? x_bytes : static_cast<size_t>(x_prefix_bytes(g, row_hi, plane_bytes));
-        if (x_need > x_done) {
-            if ((e = cudaMemcpyAsync(xd + x_done, xh + x_done, x_need - x_done,
-                                     cudaMemcpyHostToDevice, pp->s_in)) != cudaSuccess) {
-                what = "cudaMemcpyAsync (activation)";
-                break;
-            }
-            x_done = x_need;
+        const XReach x_need =
+            i == n - 1 ? XReach{g.N * g.D, g.N * g.D, 0} : x_reach(g, row_hi);
+        if ((e = copy_x_reach(g, x_have, x_need, static_cast<size_t>(plane_bytes), x_row_bytes,
+                              xh, xd, pp->s_in)) != cudaSuccess) {
+            what = "cudaMemcpyAsync (activation)";
+            break;
         }
+        x_have = x_need;
         if ((e = cudaEventRecord(pp->ev_in[i], pp->s_in)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(stream, pp->ev_in[i], 0)) != cudaSuccess) {
             what = "stream ordering";
@@ -1705,8 +1778,10 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
                                     : static_cast<int>(std::min<long long>(units, P.grid));
             if (overrides().log == 1)
                 std::fprintf(stderr, "conv_fwd_from_host: chunk %d m-tiles [%d, %d) n-tiles "
-                             "[%d, %d) rows [%lld, %lld) x prefix %zu B grid %d\n", i, mt0, mt1,
-                             k.n_tile0, k.n_tile0 + k.n_tiles, row_lo, row_hi, x_done, grid);
+                             "[%d, %d) rows [%lld, %lld) x planes %lld whole + %lld rows of "
+                             "[%lld, %lld) grid %d\n", i, mt0, mt1, k.n_tile0,
+                             k.n_tile0 + k.n_tiles, row_lo, row_hi, x_have.whole, x_have.rows,
+                             x_have.whole, x_have.part, grid);
             if ((e = launch_igemm(P.amode, P.fp8, &tm, k, grid, P.smem, stream)) != cudaSuccess)
                 what = "conv kernel launch";
         }

@@ -43,7 +43,11 @@ def _run(pkg, x, w, st, pa, di, chunks, pinned=True, sx=None, sw=None, stream=No
     hw.copy_(w.cpu())
     od = pkg.conv_out_dims(tuple(x.shape), tuple(w.shape), st, pa, di)
     hout = torch.full(od, float("nan"), dtype=torch.bfloat16, pin_memory=pinned)
+    # device buffers of NaN bytes (0xFF is NaN in bf16 and e4m3): a slice that
+    # read input rows or weights before their copy landed computes NaNs
     xd, wd = torch.empty_like(x), torch.empty_like(w)
+    xd.view(torch.uint8).fill_(0xFF)
+    wd.view(torch.uint8).fill_(0xFF)
     outd = torch.full(od, float("nan"), dtype=torch.bfloat16, device="cuda")
     ws = None if split_k else torch.empty(16, dtype=torch.uint8, device="cuda")
     pkg.conv_fwd_from_host(hx, hw, st, pa, di, scale_x=sx, scale_w=sw, out_host=hout, x_dev=xd,
@@ -65,6 +69,8 @@ CASES = [
     ((1, 8, 10, 20, 64), (72, 3, 1, 1, 64), 1, (1, 0, 0), 1),        # temporal
     ((2, 7, 6, 30, 32), (48, 5, 1, 1, 32), (2, 1, 1), (2, 0, 0), 1),  # temporal, stride 2
     ((1, 4, 9, 9, 32), (32, 3, 3, 3, 32), 1, (3, 1, 1), 1),           # planes read only padding
+    ((1, 5, 23, 6, 32), (48, 3, 3, 3, 32), (1, 2, 1), (1, 2, 1), 1),  # H stride: rows skipped
+    ((2, 4, 19, 5, 16), (40, 2, 3, 2, 16), 1, (0, 3, 1), (1, 3, 2)),  # H dilation, big pad
 ]
 
 
@@ -151,3 +157,4 @@ def test_host_pipeline_first_slice_split_over_weight_groups(pkg, capfd, bn):
     with pkg.overrides(tile=f"{bn},0,0,0,0", weight_groups=0):
         hout2 = _run(pkg, x, w, 1, 1, 1, 0)
     assert torch.equal(hout2.view(torch.int16), hout.view(torch.int16))
+

@@ -103,12 +103,18 @@ def test_video_conv3d_from_host_full_size(pkg):
     wh.copy_(w)
     hout = torch.empty(y.shape, dtype=torch.bfloat16, pin_memory=True)
     hout.fill_(float("nan"))
+    # NaN bytes in the device buffers: input rows or weights read before
+    # their copy landed would show as NaN outputs
     xd, wd = torch.empty_like(x), torch.empty_like(w)
+    xd.view(torch.uint8).fill_(0xFF)
+    wd.view(torch.uint8).fill_(0xFF)
     outd = torch.full(y.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
     pkg.conv_fwd_from_host(xh, wh, wl.stride, wl.pad, wl.dil, out_host=hout, x_dev=xd,
                            w_dev=wd, out_dev=outd)
     torch.cuda.synchronize()
     assert pkg.conv_get_device_status() == 0
+    assert torch.equal(xd.view(torch.int16), x.view(torch.int16))
+    assert torch.equal(wd.view(torch.int16), w.view(torch.int16))
     assert torch.equal(hout.view(torch.int16), y.cpu().view(torch.int16))
     plan = pkg.conv_fwd_plan(wl.x_shape, wl.w_shape, wl.stride, wl.pad, wl.dil)
     idx = _sample(tuple(y.shape), wl, plan["tile_n"])
