@@ -708,98 +708,210 @@ struct GatherFlat {
 };
 
 template <typename Word>
+__device__ __forceinline__ void gather_word(const Word* __restrict__ x, Word* __restrict__ a,
+                                            const GatherFlat& g, uint32_t w) {
+    const uint32_t m = fdiv(w, g.f_pitch);
+    const uint32_t i = w - m * g.f_pitch.d;
+    Word v = zero_word<Word>();
+    if (i < g.row_words) {
+        const uint32_t sid = fdiv(i, g.f_seg), off = i - sid * g.seg;
+        const uint32_t t = fdiv(sid, g.f_r), r = sid - t * g.R;
+        const uint32_t q1 = fdiv(m, g.f_wo), ow = m - q1 * g.f_wo.d;
+        const uint32_t q2 = fdiv(q1, g.f_ho), oh = q1 - q2 * g.f_ho.d;
+        const uint32_t n = fdiv(q2, g.f_do), od = q2 - n * g.f_do.d;
+        const uint32_t plane = (n * g.D + od * g.T + t) * g.H + oh * g.R + r;
+        v = __ldg(x + static_cast<size_t>(plane) * g.Wrow + ow * g.seg + off);
+    }
+    a[w] = v;
+}
+
+// One thread per word of the gathered rows; a second job (g1.total > 0:
+// the weights' rows, copied to the same pitch) takes the words after the
+// first job's, so both run in one launch.
+template <typename Word>
 __global__ void __launch_bounds__(256) patch_gather_flat_kernel(const Word* __restrict__ x,
-                                                                Word* __restrict__ a, GatherFlat g) {
+                                                                Word* __restrict__ a, GatherFlat g,
+                                                                const Word* __restrict__ x1,
+                                                                Word* __restrict__ a1,
+                                                                GatherFlat g1) {
     griddep_launch_dependents();
     const uint32_t step = gridDim.x * blockDim.x;
-    for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < g.total; w += step) {
-        const uint32_t m = fdiv(w, g.f_pitch);
-        const uint32_t i = w - m * g.f_pitch.d;
-        Word v = zero_word<Word>();
-        if (i < g.row_words) {
-            const uint32_t sid = fdiv(i, g.f_seg), off = i - sid * g.seg;
-            const uint32_t t = fdiv(sid, g.f_r), r = sid - t * g.R;
-            const uint32_t q1 = fdiv(m, g.f_wo), ow = m - q1 * g.f_wo.d;
-            const uint32_t q2 = fdiv(q1, g.f_ho), oh = q1 - q2 * g.f_ho.d;
-            const uint32_t n = fdiv(q2, g.f_do), od = q2 - n * g.f_do.d;
-            const uint32_t plane = (n * g.D + od * g.T + t) * g.H + oh * g.R + r;
-            v = __ldg(x + static_cast<size_t>(plane) * g.Wrow + ow * g.seg + off);
-        }
-        a[w] = v;
+    const uint32_t total = g.total + g1.total;   // below 2^31 (host check)
+    for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < total; w += step) {
+        if (w < g.total)
+            gather_word(x, a, g, w);
+        else
+            gather_word(x1, a1, g1, w - g.total);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
-                                long long W, long long C, int T, int R, int S, int Do, int Ho,
-                                int Wo, void* a, long long pitch_bytes, int num_sms,
-                                cudaStream_t stream) {
-    const long long M = N * Do * Ho * Wo;
-    const long long seg_b = static_cast<long long>(S) * C * elt, row_b = W * C * elt;
-    // one thread per word when every index fits in 32 bits: 16-, 4-, 2- or
-    // 1-byte words, whichever divides the segment, row and pitch bytes
-    const int wb = (seg_b % 16 == 0 && row_b % 16 == 0 && pitch_bytes % 16 == 0) ? 16
-                   : (seg_b % 4 == 0 && row_b % 4 == 0 && pitch_bytes % 4 == 0) ? 4
-                   : elt;
-    const long long total_w = M * (pitch_bytes / wb);
-    const long long x_words = N * D * H * (row_b / wb);
-    if (total_w > 0 && total_w < (1ll << 31) && x_words < (1ll << 31) && row_b % wb == 0 &&
-        seg_b % wb == 0 && pitch_bytes % wb == 0) {
-        GatherFlat g;
-        g.total = static_cast<uint32_t>(total_w);
-        g.seg = static_cast<uint32_t>(seg_b / wb);
-        g.row_words = static_cast<uint32_t>(static_cast<long long>(T) * R * g.seg);
-        g.T = static_cast<uint32_t>(T);
-        g.R = static_cast<uint32_t>(R);
-        g.H = static_cast<uint32_t>(H);
-        g.D = static_cast<uint32_t>(D);
-        g.Wrow = static_cast<uint32_t>(row_b / wb);
-        g.f_pitch = make_fastdiv(static_cast<uint32_t>(pitch_bytes / wb));
-        g.f_seg = make_fastdiv(g.seg);
-        g.f_r = make_fastdiv(g.R);
-        g.f_wo = make_fastdiv(static_cast<uint32_t>(Wo));
-        g.f_ho = make_fastdiv(static_cast<uint32_t>(Ho));
-        g.f_do = make_fastdiv(static_cast<uint32_t>(Do));
-        long long blk = (total_w + 255) / 256;
-        const long long cap = static_cast<long long>(num_sms) * 8;
-        if (blk > cap) blk = cap;
-        const unsigned grid = static_cast<unsigned>(blk < 1 ? 1 : blk);
-        if (wb == 16)
-            patch_gather_flat_kernel<uint4><<<grid, 256, 0, stream>>>(
-                static_cast<const uint4*>(x), static_cast<uint4*>(a), g);
-        else if (wb == 4)
-            patch_gather_flat_kernel<uint32_t><<<grid, 256, 0, stream>>>(
-                static_cast<const uint32_t*>(x), static_cast<uint32_t*>(a), g);
-        else if (wb == 2)
-            patch_gather_flat_kernel<unsigned short><<<grid, 256, 0, stream>>>(
-                static_cast<const unsigned short*>(x), static_cast<unsigned short*>(a), g);
-        else
-            patch_gather_flat_kernel<unsigned char><<<grid, 256, 0, stream>>>(
-                static_cast<const unsigned char*>(x), static_cast<unsigned char*>(a), g);
-        return cudaGetLastError();
-    }
-    long long blocks = (M + 7) / 8;
+namespace {
+
+// The geometry of one gather job: rows (n, od, oh, ow) of T*R*S*C elements
+// of x, each at `pitch_bytes`, in words of wb bytes.
+struct GatherJob {
+    long long N, D, H, W, C;
+    int T, R, S, Do, Ho, Wo;
+    long long seg_b, row_b, M;
+};
+
+GatherJob gather_job(int elt, long long N, long long D, long long H, long long W, long long C,
+                     int T, int R, int S, int Do, int Ho, int Wo) {
+    GatherJob j{N, D, H, W, C, T, R, S, Do, Ho, Wo, 0, 0, 0};
+    j.seg_b = static_cast<long long>(S) * C * elt;
+    j.row_b = W * C * elt;
+    j.M = N * Do * Ho * Wo;
+    return j;
+}
+
+bool word_fits(const GatherJob& j, long long pitch_bytes, int wb) {
+    return j.seg_b % wb == 0 && j.row_b % wb == 0 && pitch_bytes % wb == 0;
+}
+
+GatherFlat flat_params(const GatherJob& j, long long pitch_bytes, int wb) {
+    GatherFlat g;
+    g.total = static_cast<uint32_t>(j.M * (pitch_bytes / wb));
+    g.seg = static_cast<uint32_t>(j.seg_b / wb);
+    g.row_words = static_cast<uint32_t>(static_cast<long long>(j.T) * j.R * g.seg);
+    g.T = static_cast<uint32_t>(j.T);
+    g.R = static_cast<uint32_t>(j.R);
+    g.H = static_cast<uint32_t>(j.H);
+    g.D = static_cast<uint32_t>(j.D);
+    g.Wrow = static_cast<uint32_t>(j.row_b / wb);
+    g.f_pitch = make_fastdiv(static_cast<uint32_t>(pitch_bytes / wb));
+    g.f_seg = make_fastdiv(g.seg);
+    g.f_r = make_fastdiv(g.R);
+    g.f_wo = make_fastdiv(static_cast<uint32_t>(j.Wo));
+    g.f_ho = make_fastdiv(static_cast<uint32_t>(j.Ho));
+    g.f_do = make_fastdiv(static_cast<uint32_t>(j.Do));
+    return g;
+}
+
+// Words of the job's rows and of its x, against the flat kernel's 32-bit
+// indices (the two jobs of one launch together below 2^31).
+bool flat_ok(const GatherJob& j, long long pitch_bytes, int wb) {
+    const long long total_w = j.M * (pitch_bytes / wb);
+    const long long x_words = j.N * j.D * j.H * (j.row_b / wb);
+    return total_w > 0 && total_w < (1ll << 31) && x_words < (1ll << 31) &&
+           word_fits(j, pitch_bytes, wb);
+}
+
+template <typename Word>
+cudaError_t flat_launch(const void* x, void* a, const GatherFlat& g, const void* x1, void* a1,
+                        const GatherFlat& g1, int num_sms, cudaStream_t stream) {
+    long long blk = (static_cast<long long>(g.total) + g1.total + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blk > cap) blk = cap;
+    const unsigned grid = static_cast<unsigned>(blk < 1 ? 1 : blk);
+    patch_gather_flat_kernel<Word><<<grid, 256, 0, stream>>>(
+        static_cast<const Word*>(x), static_cast<Word*>(a), g, static_cast<const Word*>(x1),
+        static_cast<Word*>(a1), g1);
+    return cudaGetLastError();
+}
+
+// A warp per row (word counts past 32 bits).
+cudaError_t row_launch(const void* x, int elt, const GatherJob& j, void* a, long long pitch_bytes,
+                       int num_sms, cudaStream_t stream) {
+    long long blocks = (j.M + 7) / 8;
     const long long cap = static_cast<long long>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (seg_b % 16 == 0 && row_b % 16 == 0 && pitch_bytes % 16 == 0)
-        patch_gather_kernel<uint4><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint4*>(x), static_cast<uint4*>(a), M, D, H, row_b / 16,
-            seg_b / 16, T, R, Do, Ho, Wo, pitch_bytes / 16);
-    else if (seg_b % 4 == 0 && row_b % 4 == 0 && pitch_bytes % 4 == 0)
-        patch_gather_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint32_t*>(x), static_cast<uint32_t*>(a), M, D, H, row_b / 4,
-            seg_b / 4, T, R, Do, Ho, Wo, pitch_bytes / 4);
+    const unsigned grid = static_cast<unsigned>(blocks);
+    if (word_fits(j, pitch_bytes, 16))
+        patch_gather_kernel<uint4><<<grid, 256, 0, stream>>>(
+            static_cast<const uint4*>(x), static_cast<uint4*>(a), j.M, j.D, j.H, j.row_b / 16,
+            j.seg_b / 16, j.T, j.R, j.Do, j.Ho, j.Wo, pitch_bytes / 16);
+    else if (word_fits(j, pitch_bytes, 4))
+        patch_gather_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+            static_cast<const uint32_t*>(x), static_cast<uint32_t*>(a), j.M, j.D, j.H,
+            j.row_b / 4, j.seg_b / 4, j.T, j.R, j.Do, j.Ho, j.Wo, pitch_bytes / 4);
     else if (elt == 2)
-        patch_gather_kernel<unsigned short><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const unsigned short*>(x), static_cast<unsigned short*>(a), M, D, H,
-            row_b / 2, seg_b / 2, T, R, Do, Ho, Wo, pitch_bytes / 2);
+        patch_gather_kernel<unsigned short><<<grid, 256, 0, stream>>>(
+            static_cast<const unsigned short*>(x), static_cast<unsigned short*>(a), j.M, j.D, j.H,
+            j.row_b / 2, j.seg_b / 2, j.T, j.R, j.Do, j.Ho, j.Wo, pitch_bytes / 2);
     else
-        patch_gather_kernel<unsigned char><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const unsigned char*>(x), static_cast<unsigned char*>(a), M, D, H, row_b,
-            seg_b, T, R, Do, Ho, Wo, pitch_bytes);
+        patch_gather_kernel<unsigned char><<<grid, 256, 0, stream>>>(
+            static_cast<const unsigned char*>(x), static_cast<unsigned char*>(a), j.M, j.D, j.H,
+            j.row_b, j.seg_b, j.T, j.R, j.Do, j.Ho, j.Wo, pitch_bytes);
     return cudaGetLastError();
+}
+
+// How the patches (and, with_w, the weights) are gathered: the word width,
+// whether the patches take the one-thread-per-word kernel, and whether the
+// weights share its launch.
+struct GatherPlan {
+    GatherJob jx, jw;
+    int wb;
+    bool flat_x, together;
+};
+
+GatherPlan gather_plan(int elt, long long N, long long D, long long H, long long W, long long C,
+                       int T, int R, int S, int Do, int Ho, int Wo, long long pitch_bytes,
+                       bool with_w, long long K) {
+    GatherPlan gp;
+    gp.jx = gather_job(elt, N, D, H, W, C, T, R, S, Do, Ho, Wo);
+    // the weights: K rows of T*R*S*C elements, each one "patch"
+    gp.jw = gather_job(elt, K, 1, 1, 1, static_cast<long long>(T) * R * S * C, 1, 1, 1, 1, 1, 1);
+    // one thread per word when every index fits in 32 bits: 16-, 4-, 2- or
+    // 1-byte words, the widest that divides the segment, row and pitch bytes
+    // (of both jobs when they share the launch)
+    auto widest = [&](bool both) {
+        for (int cand : {16, 4})
+            if (word_fits(gp.jx, pitch_bytes, cand) && (!both || word_fits(gp.jw, pitch_bytes, cand)))
+                return cand;
+        return elt;
+    };
+    // the weights share the launch when that keeps the patches' word width
+    gp.wb = widest(false);
+    gp.flat_x = flat_ok(gp.jx, pitch_bytes, gp.wb);
+    gp.together = with_w && K > 0 && gp.flat_x && widest(true) == gp.wb &&
+                  flat_ok(gp.jw, pitch_bytes, gp.wb) &&
+                  gp.jx.M * (pitch_bytes / gp.wb) + gp.jw.M * (pitch_bytes / gp.wb) < (1ll << 31);
+    return gp;
+}
+
+}  // namespace
+
+int patch_gather_launches(int elt, long long N, long long D, long long H, long long W, long long C,
+                          int T, int R, int S, int Do, int Ho, int Wo, long long pitch_bytes,
+                          bool with_w, long long K) {
+    const GatherPlan gp = gather_plan(elt, N, D, H, W, C, T, R, S, Do, Ho, Wo, pitch_bytes, with_w, K);
+    return (with_w && K > 0 && !gp.together) ? 2 : 1;
+}
+
+cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
+                                long long W, long long C, int T, int R, int S, int Do, int Ho,
+                                int Wo, void* a, long long pitch_bytes, const void* w,
+                                long long K, void* wc, int num_sms, cudaStream_t stream) {
+    const bool two = w != nullptr && K > 0;
+    const GatherPlan gp = gather_plan(elt, N, D, H, W, C, T, R, S, Do, Ho, Wo, pitch_bytes, two, K);
+    const GatherJob& jx = gp.jx;
+    const GatherJob& jw = gp.jw;
+    const int wb = gp.wb;
+    const bool flat_x = gp.flat_x, together = gp.together;
+    if (flat_x) {
+        const GatherFlat gx = flat_params(jx, pitch_bytes, wb);
+        GatherFlat gw{};
+        if (together) gw = flat_params(jw, pitch_bytes, wb);
+        cudaError_t e;
+        if (wb == 16)
+            e = flat_launch<uint4>(x, a, gx, w, wc, gw, num_sms, stream);
+        else if (wb == 4)
+            e = flat_launch<uint32_t>(x, a, gx, w, wc, gw, num_sms, stream);
+        else if (wb == 2)
+            e = flat_launch<unsigned short>(x, a, gx, w, wc, gw, num_sms, stream);
+        else
+            e = flat_launch<unsigned char>(x, a, gx, w, wc, gw, num_sms, stream);
+        if (e != cudaSuccess || !two || together) return e;
+    } else {
+        cudaError_t e = row_launch(x, elt, jx, a, pitch_bytes, num_sms, stream);
+        if (e != cudaSuccess || !two) return e;
+    }
+    // the weights in a launch of their own
+    return launch_patch_gather(w, elt, K, 1, 1, 1, static_cast<long long>(T) * R * S * C, 1, 1, 1,
+                               1, 1, 1, wc, pitch_bytes, nullptr, 0, nullptr, num_sms, stream);
 }
 
 cudaError_t launch_transpose_pad(const void* src, long long R, long long C, void* dst,

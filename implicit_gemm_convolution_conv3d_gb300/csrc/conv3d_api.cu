@@ -1469,18 +1469,15 @@ int fwd_impl(const Geo& g, bool ncdhw, const void* x, const void* w, int dtype,
         // same 16-byte pitch after them
         unsigned char* wsb = static_cast<unsigned char*>(workspace);
         void* wc = wsb + (P.M * P.tma_row_bytes + 255) / 256 * 256;
+        // each filter row is one patch of T*R*S*C elements, already a GEMM row
+        // at the TMA pitch when its bytes are a multiple of 16 (read in place),
+        // else copied to that pitch by the same launch as the patches
+        const bool w_in_place = patch_weights_in_place(P);
         cudaError_t e = launch_patch_gather(
             x, static_cast<int>(P.elt), g.N, g.D, g.H, g.W, g.C, static_cast<int>(g.T),
             static_cast<int>(g.R), static_cast<int>(g.S), static_cast<int>(g.Do),
-            static_cast<int>(g.Ho), static_cast<int>(g.Wo), wsb, P.tma_row_bytes, dev->num_sms,
-            stream);
-        // each filter row is one patch of T*R*S*C elements, already a GEMM row
-        // at the TMA pitch when its bytes are a multiple of 16 (read in place)
-        const bool w_in_place = patch_weights_in_place(P);
-        if (e == cudaSuccess && !w_in_place)
-            e = launch_patch_gather(w, static_cast<int>(P.elt), g.K, 1, 1, 1,
-                                    g.T * g.R * g.S * g.C, 1, 1, 1, 1, 1, 1, wc,
-                                    P.tma_row_bytes, dev->num_sms, stream);
+            static_cast<int>(g.Ho), static_cast<int>(g.Wo), wsb, P.tma_row_bytes,
+            w_in_place ? nullptr : w, g.K, wc, dev->num_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "patch gather launch");
         xa = wsb;
         wa = w_in_place ? w : wc;
@@ -1888,7 +1885,13 @@ int conv_fwd_kernel_launches(const int64_t x_dims[5], const int64_t w_dims[5],
     if ((rc = device_info(&dev))) return rc;
     Plan P;
     if ((rc = make_plan(g, dtype, dev->num_sms, dev->smem_optin, workspace_bytes, &P))) return rc;
-    int n = P.repack == 2 ? (patch_weights_in_place(P) ? 1 : 2) : (P.repack ? 1 : 0);
+    int n = P.repack ? 1 : 0;
+    if (P.repack == 2)   // the patch gather, with the weights' copy unless read in place
+        n = patch_gather_launches(static_cast<int>(P.elt), g.N, g.D, g.H, g.W, g.C,
+                                  static_cast<int>(g.T), static_cast<int>(g.R),
+                                  static_cast<int>(g.S), static_cast<int>(g.Do),
+                                  static_cast<int>(g.Ho), static_cast<int>(g.Wo), P.tma_row_bytes,
+                                  !patch_weights_in_place(P), g.K);
     int bounds[kMaxChunks + 1];
     n += P.slices > 1 ? plan_even_slices(P, P.slices, bounds) : 1;
     if (P.splits > 1) ++n;

@@ -241,11 +241,17 @@ cudaError_t launch_row_repack(const void* src0, void* dst0, long long rows0, con
                               cudaStream_t stream);
 
 // Patch gather of a stride == filter convolution: row (n, od, oh, ow) of `a`
-// (pitch_bytes per row, tail zeroed) is the patch's T*R*S*C elements.
+// (pitch_bytes per row, tail zeroed) is the patch's T*R*S*C elements.  With
+// w != NULL, the K filter rows of w (T*R*S*C elements each) are copied to
+// `wc` at the same pitch too, in the same launch when the word counts allow.
 cudaError_t launch_patch_gather(const void* x, int elt, long long N, long long D, long long H,
                                 long long W, long long C, int T, int R, int S, int Do, int Ho,
-                                int Wo, void* a, long long pitch_bytes, int num_sms,
-                                cudaStream_t stream);
+                                int Wo, void* a, long long pitch_bytes, const void* w,
+                                long long K, void* wc, int num_sms, cudaStream_t stream);
+// Kernel launches launch_patch_gather makes for that problem (1 or 2).
+int patch_gather_launches(int elt, long long N, long long D, long long H, long long W, long long C,
+                          int T, int R, int S, int Do, int Ho, int Wo, long long pitch_bytes,
+                          bool with_w, long long K);
 
 // 16-bit transpose: dst[c, r] = src[r, c] for src [R, C] dense, dst rows of
 // P >= R elements with [R, P) zero-filled.
