@@ -707,32 +707,50 @@ struct GatherFlat {
     uint32_t total, row_words, T, R, H, D, Wrow, seg;
 };
 
-template <typename Word>
-__device__ __forceinline__ void gather_word(const Word* __restrict__ x, Word* __restrict__ a,
+// One 16-byte word of the gathered rows (output word w, the rows' pitch
+// in 16-byte words), assembled from P = 16 / sizeof(In) pieces of the
+// patch: piece i of a row is element run `off` of segment sid = (t, r), the
+// pieces past the row's T*R*S*C elements zero.  In is the widest piece the
+// segments' alignment allows (16, 4, 2 or 1 bytes).
+template <typename In>
+__device__ __forceinline__ void gather_word(const In* __restrict__ x, uint4* __restrict__ a,
                                             const GatherFlat& g, uint32_t w) {
+    constexpr int P = 16 / static_cast<int>(sizeof(In));
     const uint32_t m = fdiv(w, g.f_pitch);
-    const uint32_t i = w - m * g.f_pitch.d;
-    Word v = zero_word<Word>();
-    if (i < g.row_words) {
-        const uint32_t sid = fdiv(i, g.f_seg), off = i - sid * g.seg;
-        const uint32_t t = fdiv(sid, g.f_r), r = sid - t * g.R;
-        const uint32_t q1 = fdiv(m, g.f_wo), ow = m - q1 * g.f_wo.d;
-        const uint32_t q2 = fdiv(q1, g.f_ho), oh = q1 - q2 * g.f_ho.d;
-        const uint32_t n = fdiv(q2, g.f_do), od = q2 - n * g.f_do.d;
-        const uint32_t plane = (n * g.D + od * g.T + t) * g.H + oh * g.R + r;
-        v = __ldg(x + static_cast<size_t>(plane) * g.Wrow + ow * g.seg + off);
+    const uint32_t i0 = (w - m * g.f_pitch.d) * P;   // first piece of this word
+    const uint32_t q1 = fdiv(m, g.f_wo), ow = m - q1 * g.f_wo.d;
+    const uint32_t q2 = fdiv(q1, g.f_ho), oh = q1 - q2 * g.f_ho.d;
+    const uint32_t n = fdiv(q2, g.f_do), od = q2 - n * g.f_do.d;
+    uint32_t sid = fdiv(i0, g.f_seg), off = i0 - sid * g.seg;
+    union {
+        uint4 v;
+        In p[P];
+    } u;
+#pragma unroll
+    for (int k = 0; k < P; ++k) {
+        if (i0 + k < g.row_words) {
+            const uint32_t t = fdiv(sid, g.f_r), r = sid - t * g.R;
+            const uint32_t plane = (n * g.D + od * g.T + t) * g.H + oh * g.R + r;
+            u.p[k] = __ldg(x + static_cast<size_t>(plane) * g.Wrow + ow * g.seg + off);
+        } else {
+            u.p[k] = zero_word<In>();
+        }
+        if (++off == g.seg) {
+            off = 0;
+            ++sid;
+        }
     }
-    a[w] = v;
+    a[w] = u.v;
 }
 
-// One thread per word of the gathered rows; a second job (g1.total > 0:
-// the weights' rows, copied to the same pitch) takes the words after the
-// first job's, so both run in one launch.
-template <typename Word>
-__global__ void __launch_bounds__(256) patch_gather_flat_kernel(const Word* __restrict__ x,
-                                                                Word* __restrict__ a, GatherFlat g,
-                                                                const Word* __restrict__ x1,
-                                                                Word* __restrict__ a1,
+// One thread per 16-byte word of the gathered rows; a second job (g1.total
+// > 0: the weights' rows, copied to the same pitch) takes the words after
+// the first job's, so both run in one launch.
+template <typename In>
+__global__ void __launch_bounds__(256) patch_gather_flat_kernel(const In* __restrict__ x,
+                                                                uint4* __restrict__ a, GatherFlat g,
+                                                                const In* __restrict__ x1,
+                                                                uint4* __restrict__ a1,
                                                                 GatherFlat g1) {
     griddep_launch_dependents();
     const uint32_t step = gridDim.x * blockDim.x;
@@ -744,10 +762,6 @@ __global__ void __launch_bounds__(256) patch_gather_flat_kernel(const Word* __re
             gather_word(x1, a1, g1, w - g.total);
     }
 }
-
-}  // namespace
-
-namespace {
 
 // The geometry of one gather job: rows (n, od, oh, ow) of T*R*S*C elements
 // of x, each at `pitch_bytes`, in words of wb bytes.
@@ -772,7 +786,7 @@ bool word_fits(const GatherJob& j, long long pitch_bytes, int wb) {
 
 GatherFlat flat_params(const GatherJob& j, long long pitch_bytes, int wb) {
     GatherFlat g;
-    g.total = static_cast<uint32_t>(j.M * (pitch_bytes / wb));
+    g.total = static_cast<uint32_t>(j.M * (pitch_bytes / 16));
     g.seg = static_cast<uint32_t>(j.seg_b / wb);
     g.row_words = static_cast<uint32_t>(static_cast<long long>(j.T) * j.R * g.seg);
     g.T = static_cast<uint32_t>(j.T);
@@ -780,7 +794,7 @@ GatherFlat flat_params(const GatherJob& j, long long pitch_bytes, int wb) {
     g.H = static_cast<uint32_t>(j.H);
     g.D = static_cast<uint32_t>(j.D);
     g.Wrow = static_cast<uint32_t>(j.row_b / wb);
-    g.f_pitch = make_fastdiv(static_cast<uint32_t>(pitch_bytes / wb));
+    g.f_pitch = make_fastdiv(static_cast<uint32_t>(pitch_bytes / 16));
     g.f_seg = make_fastdiv(g.seg);
     g.f_r = make_fastdiv(g.R);
     g.f_wo = make_fastdiv(static_cast<uint32_t>(j.Wo));
@@ -789,25 +803,26 @@ GatherFlat flat_params(const GatherJob& j, long long pitch_bytes, int wb) {
     return g;
 }
 
-// Words of the job's rows and of its x, against the flat kernel's 32-bit
-// indices (the two jobs of one launch together below 2^31).
+// Pieces of the job's rows and of its x against the flat kernel's 32-bit
+// indices (the 16-byte output words of the two jobs of one launch together
+// below 2^31), and a pitch of whole 16-byte words.
 bool flat_ok(const GatherJob& j, long long pitch_bytes, int wb) {
-    const long long total_w = j.M * (pitch_bytes / wb);
+    const long long pieces = j.M * (pitch_bytes / wb);
     const long long x_words = j.N * j.D * j.H * (j.row_b / wb);
-    return total_w > 0 && total_w < (1ll << 31) && x_words < (1ll << 31) &&
-           word_fits(j, pitch_bytes, wb);
+    return pitch_bytes % 16 == 0 && pieces > 0 && pieces < (1ll << 31) &&
+           x_words < (1ll << 31) && word_fits(j, pitch_bytes, wb);
 }
 
-template <typename Word>
+template <typename In>
 cudaError_t flat_launch(const void* x, void* a, const GatherFlat& g, const void* x1, void* a1,
                         const GatherFlat& g1, int num_sms, cudaStream_t stream) {
     long long blk = (static_cast<long long>(g.total) + g1.total + 255) / 256;
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blk > cap) blk = cap;
     const unsigned grid = static_cast<unsigned>(blk < 1 ? 1 : blk);
-    patch_gather_flat_kernel<Word><<<grid, 256, 0, stream>>>(
-        static_cast<const Word*>(x), static_cast<Word*>(a), g, static_cast<const Word*>(x1),
-        static_cast<Word*>(a1), g1);
+    patch_gather_flat_kernel<In><<<grid, 256, 0, stream>>>(
+        static_cast<const In*>(x), static_cast<uint4*>(a), g, static_cast<const In*>(x1),
+        static_cast<uint4*>(a1), g1);
     return cudaGetLastError();
 }
 
@@ -854,9 +869,9 @@ GatherPlan gather_plan(int elt, long long N, long long D, long long H, long long
     gp.jx = gather_job(elt, N, D, H, W, C, T, R, S, Do, Ho, Wo);
     // the weights: K rows of T*R*S*C elements, each one "patch"
     gp.jw = gather_job(elt, K, 1, 1, 1, static_cast<long long>(T) * R * S * C, 1, 1, 1, 1, 1, 1);
-    // one thread per word when every index fits in 32 bits: 16-, 4-, 2- or
-    // 1-byte words, the widest that divides the segment, row and pitch bytes
-    // (of both jobs when they share the launch)
+    // one thread per 16-byte output word when every index fits in 32 bits,
+    // read in 16-, 4-, 2- or 1-byte pieces: the widest that divides the
+    // segment, row and pitch bytes (of both jobs when they share the launch)
     auto widest = [&](bool both) {
         for (int cand : {16, 4})
             if (word_fits(gp.jx, pitch_bytes, cand) && (!both || word_fits(gp.jw, pitch_bytes, cand)))
@@ -868,7 +883,7 @@ GatherPlan gather_plan(int elt, long long N, long long D, long long H, long long
     gp.flat_x = flat_ok(gp.jx, pitch_bytes, gp.wb);
     gp.together = with_w && K > 0 && gp.flat_x && widest(true) == gp.wb &&
                   flat_ok(gp.jw, pitch_bytes, gp.wb) &&
-                  gp.jx.M * (pitch_bytes / gp.wb) + gp.jw.M * (pitch_bytes / gp.wb) < (1ll << 31);
+                  (gp.jx.M + gp.jw.M) * (pitch_bytes / 16) < (1ll << 31);
     return gp;
 }
 

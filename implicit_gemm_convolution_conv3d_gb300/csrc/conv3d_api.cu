@@ -1709,10 +1709,10 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         (e = cudaStreamWaitEvent(pp->s_in, pp->start, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(pp->s_out, pp->start, 0)) != cudaSuccess)
         return cuda_fail(e, "stream ordering");
-    // The first slice (one block: whole waves over all column tiles) runs as
-    // one wave per group of column tiles, each launched once that group's
+    // The first slice (whole blocks: whole waves over all column tiles) runs
+    // as one wave per group of column tiles, each launched once that group's
     // weight rows have landed: the lead-in before the first kernel copies one
-    // group's weights and the slice's input planes, not all the weights.
+    // group's weights and the input rows the slice reads, not all the weights.
     int wgroups = 1, gtiles = P.n_tiles;
     {
         const long long wave = P.grid >> P.pair;
