@@ -160,6 +160,13 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": hi}
 
 
+# GPU cycles of spinning after each flush, before a step's start event: the
+# device stays busy while the host enqueues the step, so a step of tens of
+# microseconds is timed as the device runs it (not paced by the binding's
+# enqueue of its launches); outside the timed region
+SLEEP_CYCLES = 200_000
+
+
 class Timer:
     """Per-step CUDA-event timing on the launching stream, L2 flushed between steps."""
 
@@ -173,6 +180,7 @@ class Timer:
         stream = torch.cuda.current_stream()
         for i in range(self.steps):
             self.flush.zero_()
+            torch.cuda._sleep(SLEEP_CYCLES)
             self.ev[i][0].record(stream)
             fn()
             self.ev[i][1].record(stream)
@@ -481,7 +489,8 @@ def workload_config(wl):
             "w_shape": list(wl.w_shape), "w_layout": wl.w_layout, "stride": list(wl.stride),
             "pad": list(wl.pad), "dil": list(wl.dil), "M": M, "N": N, "R": R,
             "flop_per_step": flops(wl),
-            "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps"}
+            "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps, then "
+                  f"{SLEEP_CYCLES} GPU cycles of sleep before each step's start event"}
 
 
 def run_backward(pkg, wl, device, steps, warmup, flush):
