@@ -274,14 +274,19 @@ int conv_fwd_ncdhw_plan(const int64_t x_dims[5], const int64_t w_dims[5], const 
  *   scale_x, scale_w  device pointers or NULL, as for conv_fwd
  *   workspace, workspace_bytes  as for conv_fwd
  *   chunks            0: automatic; 1: no overlap; n > 1: n slices (<= 32)
- * The output rows are cut into slices of whole waves of work units.  Slice
- * i's input planes ((n, d) planes of x, a growing prefix) are copied on a
- * library-owned copy-in stream, the kernel for slice i's output rows runs on
- * `stream` once they have landed, and slice i's output rows go back on a
- * copy-out stream while slice i+1 computes.  The weights are copied first:
- * when the first slice spans several waves over all column tiles, only the
- * rows of its first group of column tiles come before its input planes, and
- * that slice runs as one launch per group, each after its rows have landed.
+ * The output rows are cut into slices of whole waves of work units (with
+ * chunks == 0: a first slice of one to four blocks of waves, chosen for the
+ * fewest bytes ahead of its first launch, then one block, then slices
+ * doubling up to a sixth of the rest, and one block last).  Before slice i
+ * runs, the input rows it reads that are not on the device yet -- whole
+ * (n, d) planes of x up to its last output plane's reach, and the leading H
+ * rows of the planes that plane reaches -- are copied on a library-owned
+ * copy-in stream; the kernel for slice i's output rows runs on `stream`
+ * once they have landed, and slice i's output rows go back on a copy-out
+ * stream while slice i+1 computes.  When the first slice spans several
+ * waves over all column tiles, only the weight rows of its first group of
+ * column tiles come before its first launch, and that slice runs as one
+ * launch per group, each after its rows have landed.
  * Work queued on `stream` before the call runs before the copies; work
  * queued after it runs after the last copy: synchronise `stream` before
  * reading out_host.  Point-output GEMM and split-K plans run unsliced (copy
