@@ -240,6 +240,30 @@ def conv_fwd_ncdhw_plan(x_shape, w_shape, stride=1, pad=0, dil=1,
             "splits": sp, "ctas": ctas, "workspace_bytes": int(ws.value)}
 
 
+def conv_fwd_from_host_slices(x_shape, w_shape, stride=1, pad=0, dil=1,
+                              dtype: int = CONV_DTYPE_BF16, num_sms: int = 0,
+                              workspace_bytes: int = 0, chunks: int = 0) -> dict:
+    """The slices conv_fwd_from_host cuts this problem into: per slice its
+    output rows (lo, hi) and the input it reads, (whole, part, rows) = (n, d)
+    planes [0, whole) entirely and rows [0, rows) of planes [whole, part);
+    and the first slice's weight groups.  ``num_sms > 0`` plans host-only."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    groups = ctypes.c_int(0)
+    rows = (ctypes.c_int64 * 64)()
+    reach = (ctypes.c_int64 * 96)()
+    _check(lib.conv_fwd_from_host_slices(_I64_5(*x_shape), _I64_5(*w_shape),
+                                         _I32_3(*_triple(stride)), _I32_3(*_triple(pad)),
+                                         _I32_3(*_triple(dil)), int(dtype), int(num_sms),
+                                         ctypes.c_size_t(int(workspace_bytes)), int(chunks),
+                                         ctypes.byref(n), rows, reach, ctypes.byref(groups)),
+           "conv_fwd_from_host_slices")
+    k = n.value
+    return {"rows": [(rows[2 * i], rows[2 * i + 1]) for i in range(k)],
+            "reach": [(reach[3 * i], reach[3 * i + 1], reach[3 * i + 2]) for i in range(k)],
+            "weight_groups": groups.value}
+
+
 def conv_fwd_workspace_size(x_shape, w_shape, stride=1, pad=0, dil=1,
                             dtype: int = CONV_DTYPE_BF16) -> int:
     """Workspace bytes conv_fwd uses for this problem on the current device
@@ -731,7 +755,8 @@ __all__ = [
     "conv_fwd", "conv_fwd_noalloc", "conv_fwd_plan", "conv_out_dims", "conv_get_device_status",
     "conv_set_wait_limit_ns", "pack_ncdhw_bf16_to_ndhwc", "pack_ncdhw_bf16_to_ndhwc_fp8",
     "conv3d", "conv2d", "conv1d", "load_library", "ConvError", "LIB_PATH",
-    "conv_fwd_from_host", "conv_fwd_kernel_launches", "conv_fwd_ncdhw",
+    "conv_fwd_from_host", "conv_fwd_from_host_slices", "conv_fwd_kernel_launches",
+    "conv_fwd_ncdhw",
     "conv_fwd_ncdhw_plan", "conv_bwd_point_workspace_bytes", "conv_bwd_data_point",
     "conv_bwd_weight_point", "conv_fwd_workspace_size", "conv_get_device_status_stream",
     "set_overrides", "overrides", "conv_fwd_ncdhw_fp8", "conv_fwd_ncdhw_fp8_workspace_size",

@@ -1168,6 +1168,39 @@ int plan_even_slices(const Plan& P, int n, int* bounds) {
     return n;
 }
 
+// The slices conv_fwd_from_host runs plan P in: m-tile bounds, and the
+// first slice's weight groups (gtiles column tiles each) when it spans
+// several waves over all column tiles.  Point-output GEMM and split-K plans
+// run unsliced.
+struct SlicePlan {
+    int n;
+    int bounds[kMaxChunks + 1];
+    int wgroups, gtiles;
+};
+
+SlicePlan plan_slices(const Plan& P, const Geo& g, int chunks) {
+    SlicePlan sp;
+    const long long x_row_bytes = g.W * g.C * P.elt;
+    const long long w_bytes = g.K * g.T * g.R * g.S * g.C * P.elt;
+    const bool chunkable = !gemm_amode(P.amode) && P.splits == 1;
+    sp.bounds[0] = 0;
+    sp.bounds[1] = P.m_tiles;
+    sp.n = chunkable ? plan_chunks(P, g, x_row_bytes, w_bytes, chunks, sp.bounds) : 1;
+    sp.wgroups = 1;
+    sp.gtiles = P.n_tiles;
+    if (sp.n > 1) {
+        const long long wave = P.grid >> P.pair;
+        const long long units0 = static_cast<long long>(sp.bounds[1] - sp.bounds[0]) * P.n_tiles;
+        const long long waves0 = units0 % wave == 0 ? units0 / wave : 0;
+        if (waves0 >= 2 && waves0 <= kMaxWGroups && P.n_tiles % waves0 == 0 &&
+            overrides().weight_groups != 0) {
+            sp.wgroups = static_cast<int>(waves0);
+            sp.gtiles = P.n_tiles / sp.wgroups;
+        }
+    }
+    return sp;
+}
+
 }  // namespace
 
 size_t splitk_workspace_bytes(const int64_t x_dims[5], const int64_t w_dims[5],
@@ -1670,11 +1703,9 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
     unsigned char* oh = static_cast<unsigned char*>(out_host);
     const unsigned char* od = static_cast<const unsigned char*>(out_dev);
 
-    int bounds[kMaxChunks + 1];
-    const bool chunkable = !gemm_amode(P.amode) && P.splits == 1;
-    const int n = chunkable ? plan_chunks(P, g, static_cast<long long>(x_row_bytes),
-                                          static_cast<long long>(w_bytes), chunks, bounds)
-                            : 1;
+    const SlicePlan sp = plan_slices(P, g, chunks);
+    const int n = sp.n;
+    const int* bounds = sp.bounds;
     cudaError_t e;
     if (n == 1) {
         // one launch: copy in, convolve, copy out, all on the caller's stream
@@ -1713,17 +1744,7 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
     // as one wave per group of column tiles, each launched once that group's
     // weight rows have landed: the lead-in before the first kernel copies one
     // group's weights and the input rows the slice reads, not all the weights.
-    int wgroups = 1, gtiles = P.n_tiles;
-    {
-        const long long wave = P.grid >> P.pair;
-        const long long units0 = static_cast<long long>(bounds[1] - bounds[0]) * P.n_tiles;
-        const long long waves0 = units0 % wave == 0 ? units0 / wave : 0;
-        if (waves0 >= 2 && waves0 <= kMaxWGroups && P.n_tiles % waves0 == 0 &&
-            overrides().weight_groups != 0) {
-            wgroups = static_cast<int>(waves0);
-            gtiles = P.n_tiles / wgroups;
-        }
-    }
+    const int wgroups = sp.wgroups, gtiles = sp.gtiles;
     const size_t w_row = w_bytes / static_cast<size_t>(g.K);   // one filter's bytes
     auto copy_w_group = [&](int s) -> cudaError_t {
         const long long r0 = static_cast<long long>(s) * gtiles * P.BN;
@@ -1806,6 +1827,46 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
         if (!what) return cuda_fail(e2, "stream ordering");
     }
     if (what) return cuda_fail(e, what);
+    return CONV_OK;
+}
+
+int conv_fwd_from_host_slices(const int64_t x_dims[5], const int64_t w_dims[5],
+                              const int stride[3], const int pad[3], const int dil[3], int dtype,
+                              int num_sms, size_t workspace_bytes, int chunks, int* n_slices,
+                              int64_t* rows, int64_t* reach, int* weight_groups) {
+    Geo g;
+    int rc = make_geo(x_dims, w_dims, stride, pad, dil, &g);
+    if (rc) return rc;
+    if (!n_slices || !rows || !reach || !weight_groups) {
+        set_error("null output pointer");
+        return CONV_ERR_INVALID;
+    }
+    if (chunks < 0) {
+        set_error("chunks must be >= 0");
+        return CONV_ERR_INVALID;
+    }
+    int sms = num_sms, smem = 232448;
+    if (sms <= 0) {
+        DeviceInfo* d = nullptr;
+        if ((rc = device_info(&d))) return rc;
+        sms = d->num_sms;
+        smem = d->smem_optin;
+    }
+    Plan P;
+    if ((rc = make_plan(g, dtype, sms, smem, workspace_bytes, &P))) return rc;
+    const SlicePlan sp = plan_slices(P, g, chunks);
+    *n_slices = sp.n;
+    *weight_groups = sp.wgroups;
+    for (int i = 0; i < sp.n; ++i) {
+        const long long lo = sp.n == 1 ? 0 : tile_row_lo(P, sp.bounds[i]);
+        const long long hi = sp.n == 1 ? P.M : tile_row_hi(P, sp.bounds[i + 1] - 1);
+        const XReach r = i == sp.n - 1 ? XReach{g.N * g.D, g.N * g.D, 0} : x_reach(g, hi);
+        rows[2 * i] = lo;
+        rows[2 * i + 1] = hi;
+        reach[3 * i] = r.whole;
+        reach[3 * i + 1] = r.part;
+        reach[3 * i + 2] = r.rows;
+    }
     return CONV_OK;
 }
 

@@ -303,6 +303,25 @@ int conv_fwd_from_host(const void* x_host, const int64_t x_dims[5], const void* 
                        void* out_host, void* x_dev, void* w_dev, void* out_dev, void* workspace,
                        size_t workspace_bytes, int chunks, cudaStream_t stream);
 
+/* The slices conv_fwd_from_host would cut this problem into (the same plan
+ * and rule; a query: nothing is launched or copied).  num_sms > 0 plans for
+ * that SM count without touching a device (232448 bytes of shared memory
+ * per block), 0 for the current device; workspace_bytes and chunks as given
+ * to conv_fwd_from_host (0: no workspace).  Writes *n_slices (1..32),
+ * *weight_groups (the launches the first slice runs as, one per group of
+ * column tiles), and for slice i:
+ *   rows[2i], rows[2i+1]   its output rows [lo, hi) (row = (n, od, oh, ow));
+ *   reach[3i .. 3i+2]      (whole, part, rows): the input on the device once
+ *                          its copy-in has landed, as (n, d) planes of x,
+ *                          planes [0, whole) entirely and rows [0, rows) of
+ *                          planes [whole, part); the last slice: all of x.
+ * rows holds 64 and reach 96 entries.  Returns CONV_ERR_INVALID for a null
+ * pointer or chunks < 0, else as conv_fwd_plan. */
+int conv_fwd_from_host_slices(const int64_t x_dims[5], const int64_t w_dims[5],
+                              const int stride[3], const int pad[3], const int dil[3], int dtype,
+                              int num_sms, size_t workspace_bytes, int chunks, int* n_slices,
+                              int64_t* rows, int64_t* reach, int* weight_groups);
+
 /* Backward passes of the point-output conv (MIOpen PR #10912 "Use a single
  * GEMM for point-output conv in all three directions": backward data and
  * backward weights of patch-embedding shapes, each one GEMM).  Shapes: zero

@@ -158,3 +158,24 @@ def test_host_pipeline_first_slice_split_over_weight_groups(pkg, capfd, bn):
         hout2 = _run(pkg, x, w, 1, 1, 1, 0)
     assert torch.equal(hout2.view(torch.int16), hout.view(torch.int16))
 
+
+
+def test_slice_query_matches_the_launches(pkg, capfd):
+    """conv_fwd_from_host_slices (the current device) names the output rows
+    and weight groups conv_fwd_from_host then launches."""
+    xs, ws = (1, 8, 48, 48, 64), (1024, 3, 3, 3, 64)
+    x, w = _operands(xs, ws, 60)
+    with pkg.overrides(tile="128,0,0,0,0"):
+        plan = pkg.conv_fwd_from_host_slices(xs, ws, 1, 1, 1, workspace_bytes=16)
+        with pkg.overrides(tile="128,0,0,0,0", log=1):
+            _run(pkg, x, w, 1, 1, 1, 0)
+            log = capfd.readouterr().err
+    lines = [ln for ln in log.splitlines() if ln.startswith("conv_fwd_from_host: chunk ")]
+    seen = []
+    for ln in lines:
+        lo, hi = (int(v) for v in ln.split("rows [")[1].split(")")[0].split(", "))
+        if not seen or seen[-1] != (lo, hi):
+            seen.append((lo, hi))
+    assert seen == [tuple(r) for r in plan["rows"]], (seen, plan)
+    first = [ln for ln in lines if ln.split()[2] == "0"]
+    assert len(first) == plan["weight_groups"]
